@@ -1,0 +1,479 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged KV-cache decode path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload mha|gqa|long|mixed|tiny]
+
+One step = one pass of the whole decode hot path over one batch: the new
+token's K/V of every sequence is written through its slot (slots come from
+the host block pool), then single-query paged attention runs over every
+sequence (and the partition merge where a sequence was split).  The default
+workload is the 7B-shaped MHA decode layer: 64 sequences, 32 heads, head size
+128, block size 16, fp16, attended lengths uniform in [1, 2048], physical
+blocks drawn from a seeded permutation of a 10,000-block pool.
+
+`value` is the algorithmic K/V bytes the step reads (sum over sequences of
+L * num_kv_heads * head_size * 2 * element size) per second of device time,
+summed over ranks, with all inputs resident in HBM.  `e2e` is the same metric
+when every step also copies its inputs from pinned host memory and reads the
+outputs back.  With N > 1 (torchrun) every rank runs its own replica: the path
+has no exchange step, so there is no collective in the timed work.
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload.
+"""
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_75_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode seqs/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture, keyed by workload, with the hash of the kernel source it was taken
+# on; reported only while the source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode_impl.cuh", "decode_launch.cuh", "decode_api.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_75_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; nvidia-smi fallback)
+# ---------------------------------------------------------------------------
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+           0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, device_index=0, period_s=0.01):
+        self.samples, self.reasons, self.max_mhz = [], 0, None
+        self.period = period_s
+        self._stop = threading.Event()
+        self._nvml = None
+        self._handle = ctypes.c_void_p()
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            props = torch.cuda.get_device_properties(device_index)
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self._handle)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self._handle)) != 0:
+                    raise OSError("nvml handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(self._handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml = nv
+        except Exception:
+            self._nvml = None
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _sample(self):
+        if self._nvml is not None:
+            mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, ctypes.byref(mhz))
+            f = getattr(self._nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            f(self._handle, ctypes.byref(rs))
+            return mhz.value, rs.value
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                              "--format=csv,noheader,nounits", "-i", "0"], capture_output=True, text=True,
+                             timeout=5).stdout.strip().split(",")
+        if self.max_mhz is None:
+            self.max_mhz = int(out[1])
+        return int(out[0]), int(out[2].strip(), 16)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                mhz, rs = self._sample()
+                self.samples.append(mhz)
+                self.reasons |= rs
+            except Exception:
+                pass
+            self._stop.wait(self.period)
+
+    def __enter__(self):
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        try:
+            mhz, rs = self._sample()  # at least one sample at the end of the region
+            self.samples.append(mhz)
+            self.reasons |= rs
+        except Exception:
+            pass
+        self._stop.set()
+        self._thread.join()
+
+    def summary(self):
+        names = [n for b, n in REASONS.items() if self.reasons & b and n != "gpu_idle"]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": names, "samples": len(self.samples)}
+
+
+# ---------------------------------------------------------------------------
+# multi-process helpers (replicas; no collective in the timed work)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def aggregate(elapsed_ms: float, units: float, world: int):
+    """(max elapsed over ranks, sum of units over ranks)."""
+    if world == 1:
+        return elapsed_ms, units
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+class DecodeStep:
+    """Inputs of one decode step resident on the device."""
+
+    def __init__(self, case: W.PagedCase, device, partition_size=0, name=""):
+        import paged_kv_cache_75_gb300 as pk
+        self.pk = pk
+        self.name = name
+        self.case = case
+        self.device = device
+        lens = case.seq_lens.cpu().numpy().astype(np.int64)
+        self.lens_np = lens
+        B = len(lens)
+        self.B = B
+        # a1: the slot of each sequence's newest token (position L-1) via the
+        # host block pool holding exactly this block table
+        bt = case.block_table.cpu().numpy()
+        self.slots_np = self._slots_from_pool(bt, lens, case.block_size, case.num_blocks)
+        g = torch.Generator(device=device)
+        g.manual_seed(12345)
+        self.k_new = W.random_values(g, (B, case.num_kv_heads, case.head_size), case.q_dtype, device)
+        self.v_new = W.random_values(g, (B, case.num_kv_heads, case.head_size), case.q_dtype, device)
+        self.slots = torch.from_numpy(self.slots_np).to(device)
+        self.cache = pk.KVCache(case.k_cache, case.v_cache, case.k_scale, case.v_scale)
+        self.q = case.q
+        self.bt = case.block_table.to(device)
+        self.lens = case.seq_lens.to(device)
+        self.max_len = int(lens.max())
+        self.P = partition_size
+        self.out = torch.empty_like(self.q)
+        ws = pk.pa_decode_workspace_size(B, case.num_heads, case.head_size, self.max_len, case.block_size,
+                                         partition_size)
+        self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
+        self.kv_bytes = case.kv_bytes()
+        P = partition_size or 512
+        self.split = self.max_len > P
+        self.launches_per_step = 2 + (1 if self.split else 0)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    @staticmethod
+    def _slots_from_pool(bt, lens, bs, nb):
+        import paged_kv_cache_75_gb300 as pk
+        # free order that hands out exactly the table's blocks: first the
+        # blocks of every sequence's older tokens, sequence by sequence, then
+        # the blocks that only the newest tokens open
+        order, seen = [], set()
+        for b in range(len(lens)):
+            for j in range(W.pages_for(lens[b] - 1, bs)):
+                order.append(int(bt[b, j]))
+        for b in range(len(lens)):
+            if W.pages_for(lens[b], bs) > W.pages_for(lens[b] - 1, bs):
+                order.append(int(bt[b, W.pages_for(lens[b], bs) - 1]))
+        seen = set(order)
+        order += [i for i in range(nb) if i not in seen]
+        pool = pk.BlockPool(nb, bs, order)
+        slots = np.empty(len(lens), np.int64)
+        for b, L in enumerate(lens):
+            pool.add_seq(b)
+            if L > 1:
+                pool.append(b, int(L) - 1)
+        for b in range(len(lens)):
+            s, cow = pool.append(b, 1)
+            slots[b] = s[0]
+        return slots
+
+    def write(self):
+        self.pk.pa_kv_cache_write(self.cache, self.k_new, self.v_new, self.slots, self.status)
+
+    def decode(self, q=None, out=None, bt=None, lens=None):
+        self.pk.pa_decode(self.out if out is None else out, self.q if q is None else q, self.cache,
+                          self.bt if bt is None else bt, self.lens if lens is None else lens, self.max_len,
+                          self.case.scale, self.P, self.ws, self.status)
+
+
+def build_workload(name, device):
+    if name == "mha":
+        return W.mha_decode(device=device), "mha_decode_64seq_32h_d128_bs16_fp16_len_u1_2048_pool10000"
+    if name == "gqa":
+        return W.gqa_shared_decode(device=device), "gqa_decode_256seq_32q8kv_d128_bs16_bf16_lognormal1000_shared4"
+    if name == "long":
+        return W.long_fp8_decode(device=device), "long_decode_8seq_64q8kv_d128_bs32_e4m3_len_u32k_128k_p512"
+    if name == "tiny":
+        case = W.tiny_decode(device=device)
+        case.seq_lens = torch.tensor([31, 33, 71], dtype=torch.int32, device=device)
+        return case, "tiny_decode_3seq_4h_d64_bs32_fp16_worked_example"
+    raise ValueError(name)
+
+
+def timed_decode(step: DecodeStep, steps, warmup, world):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.write()
+        step.decode()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for i in range(steps):
+            step.write()
+            evs[i][0].record(stream)
+            step.decode()
+            evs[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    decode_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    st = int(step.status.item())
+    if st != 0:
+        raise RuntimeError("device status %d during the benchmark" % st)
+    return total_ms, decode_ms, clk.summary()
+
+
+def timed_e2e(step: DecodeStep, steps, warmup, world):
+    """Same step through the public API with host buffers: each step copies
+    q, the new K/V, slots, block table and lengths from pinned host memory and
+    reads the output back."""
+    host = {n: t.cpu().pin_memory() for n, t in (("q", step.q), ("k", step.k_new), ("v", step.v_new),
+                                                 ("slots", step.slots), ("bt", step.bt), ("lens", step.lens))}
+    dev = {n: torch.empty_like(t, device=step.device) for n, t in host.items()}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    pk = step.pk
+
+    def one():
+        for n, t in host.items():
+            dev[n].copy_(t, non_blocking=True)
+        pk.pa_kv_cache_write(step.cache, dev["k"], dev["v"], dev["slots"], step.status)
+        step.decode(q=dev["q"], out=step.out, bt=dev["bt"], lens=dev["lens"])
+        out_host.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        one()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end), h2d, d2h
+
+
+def oracle_decode_seconds(case: W.PagedCase, seq_idx, nthreads, q_bits, kc, vc, bt, lens):
+    import oracle
+    idx = np.asarray(seq_idx)
+    t0 = time.perf_counter()
+    _, _, rc = oracle.decode(q_bits[idx], case.q_dtype, kc, vc, case.kv_dtype, bt[idx], lens[idx], case.scale,
+                             case.k_scale, case.v_scale, nthreads=nthreads, want_codes=True)
+    dt = time.perf_counter() - t0
+    assert rc == 0
+    return dt
+
+
+def cpu_sample_indices(case, budget_bytes):
+    """Every k-th sequence so that the sample's KV bytes stay within budget."""
+    lens = case.seq_lens.cpu().numpy().astype(np.int64)
+    per = case.num_kv_heads * case.head_size * 2 * W.ELEM_BYTES[case.kv_dtype]
+    total = int(lens.sum()) * per
+    k = max(1, int(np.ceil(total / budget_bytes)))
+    idx = np.arange(0, len(lens), k)
+    return idx, int(lens[idx].sum()) * per
+
+
+def cpu_baseline(case, budget_s=10.0):
+    """The oracle, as it stands, on all host cores over a bounded sample."""
+    import oracle
+    cores = os.cpu_count() or 1
+    n = oracle.num_threads(cores)
+    q_bits, kc, vc = W.as_bits(case.q), W.as_bits(case.k_cache), W.as_bits(case.v_cache)
+    bt = case.block_table.cpu().numpy()
+    lens = case.seq_lens.cpu().numpy()
+    idx, sample_bytes = cpu_sample_indices(case, 2e9)
+    reps, spent = 0, 0.0
+    while spent < budget_s and reps < 50:
+        spent += oracle_decode_seconds(case, idx, n, q_bits, kc, vc, bt, lens)
+        reps += 1
+    gbs = sample_bytes * reps / spent / 1e9
+    return {"value": round(gbs, 3), "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": "oracle decode (fp64) over %d of %d sequences (%.1f MB of KV), %d passes in %.1f s"
+                      % (len(idx), case.num_seqs, sample_bytes / 1e6, reps, spent)}
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    case, wname = build_workload(args.workload, dev)
+    step = DecodeStep(case, dev, args.partition_size, wname)
+    total_ms, decode_ms, clocks = timed_decode(step, args.steps, args.warmup, world)
+    total_ms, kv_sum = aggregate(total_ms, float(step.kv_bytes) * args.steps, world)
+    seqs_sum = aggregate(0.0, float(step.B) * args.steps, world)[1]
+    ms_per_step = total_ms / args.steps
+    value = kv_sum / (total_ms / 1e3) / 1e9
+    e2e_ms, h2d, d2h = timed_e2e(step, args.steps, args.warmup, world)
+    e2e_ms, kv_e2e = aggregate(e2e_ms, float(step.kv_bytes) * args.steps, world)
+    hbm, _, _, peak_kind = measured_peaks()
+    achieved = step.kv_bytes / (decode_ms / 1e3) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = NCU_TRAFFIC.get((args.workload, src_hash))
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "storage_dtype": {0: "f16", 1: "bf16", 2: "e4m3"}[case.kv_dtype],
+        "data": "synthetic",
+        "config": {"workload": wname, "num_seqs": step.B, "num_heads": case.num_heads,
+                   "num_kv_heads": case.num_kv_heads, "head_size": case.head_size, "block_size": case.block_size,
+                   "num_blocks": case.num_blocks, "kv_bytes_per_step": step.kv_bytes,
+                   "partition_size": args.partition_size or 512,
+                   "l2": "inputs larger than L2 (%.2f GB of K/V read per step > 129 MB L2)" % (step.kv_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "seqs_per_s_per_layer": round(seqs_sum / (total_ms / 1e3), 1),
+        "hbm_frac_of_8000": round(value / world / 8000.0, 4),
+        "clocks": clocks,
+        "e2e": {"value": round(kv_e2e / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "pa_decode (paged_decode_kernel + partition merge)",
+                     "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_kind": "of %s" % peak_kind,
+                     "traffic": traffic, "decode_ms": round(decode_ms, 5), "kernel_src": src_hash},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The CPU oracle on the host cores, each step a bounded sample."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    case, wname = build_workload(args.workload, "cpu")
+    cores = os.cpu_count() or 1
+    n = oracle.num_threads(cores)
+    q_bits, kc, vc = W.as_bits(case.q), W.as_bits(case.k_cache), W.as_bits(case.v_cache)
+    bt = case.block_table.numpy()
+    lens = case.seq_lens.numpy()
+    idx, sample_bytes = cpu_sample_indices(case, 3e8)
+    for _ in range(args.warmup):
+        oracle_decode_seconds(case, idx, n, q_bits, kc, vc, bt, lens)
+    spent = 0.0
+    for _ in range(args.steps):
+        spent += oracle_decode_seconds(case, idx, n, q_bits, kc, vc, bt, lens)
+    value = sample_bytes * args.steps / spent / 1e9
+    sample = "oracle decode (fp64) over %d of %d sequences (%.1f MB of KV) per step" % (
+        len(idx), case.num_seqs, sample_bytes / 1e6)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(spent / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wname, "num_seqs": case.num_seqs, "sampled_seqs": len(idx)},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny"], default="mha")
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

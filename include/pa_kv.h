@@ -1,0 +1,238 @@
+/*
+ * pa_kv.h -- C ABI of the paged KV-cache attention library (libpa_kv.so).
+ *
+ * PagedAttention keeps each sequence's keys and values in fixed-size blocks
+ * of `block_size` tokens per KV head; the blocks sit at arbitrary physical
+ * block ids and a per-sequence block table maps logical block j (tokens
+ * j*block_size .. (j+1)*block_size-1) to its physical id.  Sources:
+ *   - vLLM PagedAttention design doc ("分页注意力机制", vllm.ooos.top):
+ *     sections 输入参数 (q, k_cache, v_cache, out), 概念 (sequence, context,
+ *     block), QK, Softmax, Value, Output.
+ *   - "Paged 어텐션" (data-sketchers.com transformers paged-attention wiki):
+ *     "Decode 경로" (block_table [batch, max_blocks_per_seq], -1 =
+ *     unallocated, cache_seqlens, in-place cache update) and "Varlen 경로"
+ *     (cu_seq_lens_q / cu_seq_lens_k, max_seqlen_q / max_seqlen_k).
+ *   - "Как работает paged attention? (детально)" (aivaro.ru answers/837):
+ *     sections 3.2 BlockManager, 3.3 copy-on-write, 4.1-4.2 allocation and
+ *     deallocation, 5.1 block-wise attention.
+ *   - vLLM paper summary (easyvpn24.com/25506.html): sections 2-4.
+ *
+ * Conventions for every call below:
+ *   - Device pointers point to memory the caller owns (e.g. torch tensors);
+ *     the device calls allocate nothing.  All device work is queued on
+ *     `stream` (a cudaStream_t; NULL = the legacy default stream) and is
+ *     asynchronous; the call returns once the work is queued.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and launches
+ *     nothing.  A failed launch returns PA_ERR_CUDA.
+ *   - Errors that depend on device data (a block id outside the pool, a slot
+ *     outside the cache, a length above the stated maximum, a wait that ran
+ *     out of time) are written to *dev_status (a device int32 the caller
+ *     zeroes; may be NULL): the first error code wins.  The kernels never trap.
+ *   - Cache layout (both K and V): [num_blocks][num_kv_heads][block_size]
+ *     [head_size], row-major, so one (block, kv head) page is one contiguous
+ *     block_size*head_size run.
+ *   - GQA: query head h reads KV head h / (num_heads / num_kv_heads);
+ *     num_heads must be a multiple of num_kv_heads.
+ *   - Pool handles (pa_pool_*) hold host memory only and are not thread-safe.
+ */
+#ifndef PA_KV_H
+#define PA_KV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* the same type as cudaStream_t */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,  /* bad pointer, size, shape or length */
+    PA_ERR_UNSUPPORTED = 2,  /* valid, but a head size / dtype / block size not built */
+    PA_ERR_OOM = 3,          /* the block pool has too few free blocks */
+    PA_ERR_CUDA = 4,         /* a CUDA launch or query failed */
+    PA_ERR_TIMEOUT = 5,      /* device: a bounded wait ran out (dev_status only) */
+    PA_ERR_BAD_BLOCK = 6     /* device: block id or slot outside the cache */
+} pa_status;
+
+typedef enum {
+    PA_F16 = 0,       /* IEEE binary16 */
+    PA_BF16 = 1,      /* bfloat16 */
+    PA_FP8_E4M3 = 2   /* OCP FP8 E4M3 (finite-only "fn"), KV cache only */
+} pa_dtype;
+
+/* Description of one layer's paged KV cache (device memory owned by the
+ * caller).  k_cache / v_cache: [num_blocks][num_kv_heads][block_size]
+ * [head_size] elements of kv_dtype, 16-byte aligned.  For PA_FP8_E4M3 a
+ * stored code c means the value c * k_scale (keys) or c * v_scale (values);
+ * the scales are ignored for 16-bit caches. ("FP8 KV Cache" in the vLLM
+ * feature list on "ChunkLlama", docsearch.algolia.com.) */
+typedef struct {
+    void* k_cache;
+    void* v_cache;
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t head_size;
+    pa_dtype kv_dtype;
+    float k_scale;
+    float v_scale;
+} pa_kv_cache;
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_str(pa_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t pa_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Write new K/V rows into their cache slots.
+ * "Paged 어텐션", Decode 경로 (the cache is updated in place through the
+ * block table); "Как работает paged attention?" 4.1 step 5 (the new token's
+ * KV goes to its position in the physical block); vLLM paper summary §3.
+ *
+ * k, v: device, [num_tokens][num_kv_heads][head_size] of in_dtype (F16 or
+ *   BF16); consecutive tokens are token_stride elements apart (>=
+ *   num_kv_heads*head_size; lets k/v be views into a fused qkv buffer).
+ * slot_mapping: device int64 [num_tokens]; slot s means physical block
+ *   s / block_size, offset s % block_size; s < 0 skips the token (padding).
+ *   A slot >= num_blocks*block_size is skipped and reported as
+ *   PA_ERR_BAD_BLOCK in *dev_status.
+ * A 16-bit cache must have kv_dtype == in_dtype: the bits are moved
+ *   unchanged.  An E4M3 cache stores e4m3_satfinite(round-to-nearest-even(
+ *   (float)x / scale)), the division done in IEEE binary32.
+ * Several tokens with the same slot: which one lands is unspecified.
+ * ------------------------------------------------------------------------- */
+pa_status pa_kv_cache_write(const pa_kv_cache* cache, const void* k, const void* v,
+                            pa_dtype in_dtype, int64_t num_tokens, int64_t token_stride,
+                            const int64_t* slot_mapping, int32_t* dev_status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Copy whole physical blocks (all KV heads, K and V): the device half of
+ * copy-on-write ("Как работает paged attention?" 3.3: a shared block is
+ * copied before a sequence writes into it).
+ * src_dst_pairs: device int32 [n][2] = (source id, destination id).  A pair
+ * with an id outside [0, num_blocks) is skipped and reported as
+ * PA_ERR_BAD_BLOCK.  Destinations must be distinct and not also sources.
+ * ------------------------------------------------------------------------- */
+pa_status pa_copy_blocks(const pa_kv_cache* cache, const int32_t* src_dst_pairs, int32_t n,
+                         int32_t* dev_status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Single-query decode attention over the paged cache.
+ * vLLM PagedAttention design doc (whole walk-through: QK, Softmax, Value,
+ * Output; the grid axis over context partitions); "Paged 어텐션" Decode 경로.
+ *
+ * For every sequence b and query head h, with L = seq_lens[b] and
+ * kvh = h / (num_heads / num_kv_heads):
+ *     s_t = scale * sum_d q[b][h][d] * K_b[t][d]      for t < L
+ *     out[b][h][:] = sum_t softmax(s)_t * V_b[t][:]
+ * where K_b[t] = k_cache[block_table[b][t / block_size]][kvh][t % block_size]
+ * (times k_scale for E4M3), V_b likewise.  L = 0 gives out = 0.  Positions
+ * t >= L take no part (they may hold anything, NaN included).
+ *
+ * out, q: device [num_seqs][num_heads][head_size] of q_dtype (F16 or BF16),
+ *   16-byte aligned.  q_dtype must equal kv_dtype for 16-bit caches; an E4M3
+ *   cache takes F16 or BF16 queries.  out is rounded to nearest even.
+ * block_table: device int32 [num_seqs][max_blocks_per_seq]; only the first
+ *   ceil(L / block_size) entries of a row are read; each must be in
+ *   [0, num_blocks), otherwise PA_ERR_BAD_BLOCK is reported and that page is
+ *   left out.
+ * seq_lens: device int32 [num_seqs], the attended lengths ("cache_seqlens"
+ *   counting the token just written).  Each must be <= max_seq_len and
+ *   <= max_blocks_per_seq*block_size, otherwise PA_ERR_INVALID_ARG is
+ *   reported and the sequence's output is 0.
+ * partition_size: tokens per context partition (a multiple of block_size),
+ *   0 = automatic.  A sequence longer than one partition is split; the
+ *   partitions' partial results go to `workspace` and a second kernel merges
+ *   them by their log-sum-exp.
+ * workspace: device scratch of at least pa_decode_workspace_size(...) bytes,
+ *   16-byte aligned (may be NULL when that size is 0).
+ * Supported: head_size 64 or 128; block_size 16, 32 or 64;
+ *   num_heads / num_kv_heads in {1, 2, 4, 8}.
+ * ------------------------------------------------------------------------- */
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                                int32_t max_seq_len, int32_t block_size, int32_t partition_size);
+
+pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                    const int32_t* block_table, int32_t max_blocks_per_seq,
+                    const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                    int32_t num_heads, float scale, int32_t partition_size, void* workspace,
+                    size_t workspace_bytes, int32_t* dev_status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Varlen prefill (and mixed prefill + decode) attention over the paged cache.
+ * "Paged 어텐션" Varlen 경로 (cu_seq_lens_q/k index a batch of sequences of
+ * different lengths; max_seqlen_q/k bound them); keys and values are read
+ * from the paged cache through block_table as in the Decode 경로; causal
+ * masking per block as in "Как работает paged attention?" 5.1.
+ *
+ * Sequence b owns query rows cu_seq_lens_q[b] .. cu_seq_lens_q[b+1]-1 of q
+ * and has Lk = cu_seq_lens_k[b+1] - cu_seq_lens_k[b] keys at logical
+ * positions 0..Lk-1 of its block-table row (the new tokens' K/V must already
+ * be in the cache, e.g. by pa_kv_cache_write).  With Lq query rows, query i
+ * sits at position Lk - Lq + i; with causal != 0 it sees keys j <= Lk - Lq + i
+ * (bottom-right alignment), otherwise all Lk keys.  A row that sees no key
+ * outputs 0.
+ * q, out: device [total_q][num_heads][head_size] of q_dtype (BF16 or F16,
+ *   equal to kv_dtype), total_q = cu_seq_lens_q[num_seqs].
+ * cu_seq_lens_q, cu_seq_lens_k: device int32 [num_seqs + 1], non-decreasing,
+ *   starting at 0.  max_seqlen_q / max_seqlen_k must bound the lengths
+ *   (a longer sequence is reported as PA_ERR_INVALID_ARG and left at 0).
+ * Supported: head_size 128; block_size 16, 32 or 64; 16-bit caches.
+ * ------------------------------------------------------------------------- */
+pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                            const int32_t* block_table, int32_t max_blocks_per_seq,
+                            const int32_t* cu_seq_lens_q, const int32_t* cu_seq_lens_k,
+                            int32_t num_seqs, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                            int32_t num_heads, float scale, int32_t causal, int32_t* dev_status,
+                            pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block pool ("Как работает paged attention?" 3.2 BlockManager, 3.3,
+ * 4.1, 4.2; vLLM paper summary §2-4).  Host memory only.
+ *
+ * The free list is FIFO: allocation takes its head, a freed block goes to
+ * its tail.  free_order (nullable, a permutation of 0..num_blocks-1) sets the
+ * initial order; NULL means 0, 1, 2, ...
+ * pa_pool_append(seq, n): positions len .. len+n-1 get slots; a position in a
+ *   logical block not yet mapped gets a new block (reference count 1).  If the
+ *   last block is shared (reference count > 1) and not full, it is first
+ *   replaced by a private block taken from the free list: the (old, new) pair
+ *   is written to cow_pairs_out (room for 2 int32) and *n_cow_out = 1; the
+ *   caller copies it with pa_copy_blocks before writing the slots.  If the
+ *   free list cannot supply every block the append needs, nothing changes and
+ *   PA_ERR_OOM is returned.  slots_out: host int64 [n].
+ * pa_pool_fork(parent, child): the child shares all of the parent's blocks
+ *   (each reference count + 1) and its length.
+ * pa_pool_free_seq: each block's reference count - 1, in logical order; a
+ *   block reaching 0 goes to the tail of the free list.
+ * pa_pool_block_table: host int32 [n][max_blocks] rows, -1 padded, and host
+ *   int32 lens_out[n] (nullable).  A sequence with more blocks than
+ *   max_blocks gives PA_ERR_INVALID_ARG.
+ * Sequence ids are arbitrary int64 keys; an unknown id gives
+ * PA_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+pa_status pa_pool_create(int64_t num_blocks, int32_t block_size, const int32_t* free_order,
+                         void** pool_out);
+void pa_pool_destroy(void* pool);
+pa_status pa_pool_add_seq(void* pool, int64_t seq_id);
+pa_status pa_pool_append(void* pool, int64_t seq_id, int32_t n_tokens, int64_t* slots_out,
+                         int32_t* cow_pairs_out, int32_t* n_cow_out);
+pa_status pa_pool_fork(void* pool, int64_t parent, int64_t child);
+pa_status pa_pool_free_seq(void* pool, int64_t seq_id);
+pa_status pa_pool_block_table(void* pool, const int64_t* seq_ids, int32_t n, int32_t max_blocks,
+                              int32_t* table_out, int32_t* lens_out);
+int64_t pa_pool_num_free(void* pool);
+int32_t pa_pool_ref_count(void* pool, int64_t block);
+int32_t pa_pool_seq_len(void* pool, int64_t seq_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_KV_H */

@@ -1,0 +1,268 @@
+"""ctypes marshalling for libpa_kv.so (see include/pa_kv.h for semantics)."""
+import ctypes as C
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+PA_F16, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+_TORCH_CODE = {torch.float16: PA_F16, torch.bfloat16: PA_BF16, torch.float8_e4m3fn: PA_FP8_E4M3}
+
+library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa_kv.so")
+_lib = None
+
+
+class PaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, pa_status_str(status), status))
+
+
+class _Cache(C.Structure):
+    _fields_ = [("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("num_blocks", C.c_int64),
+                ("block_size", C.c_int32), ("num_kv_heads", C.c_int32), ("head_size", C.c_int32),
+                ("kv_dtype", C.c_int), ("k_scale", C.c_float), ("v_scale", C.c_float)]
+
+
+def library():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise RuntimeError("libpa_kv.so is missing: run __graft_entry__.build() "
+                               "(or python -m paged_kv_cache_75_gb300.build)")
+        L = C.CDLL(library_path)
+        vp, i32, i64, sz, f32 = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float
+        pc = C.POINTER(_Cache)
+        sig = {
+            "pa_status_str": ([C.c_int], C.c_char_p),
+            "pa_version": ([], i32),
+            "pa_kv_cache_write": ([pc, vp, vp, C.c_int, i64, i64, vp, vp, vp], C.c_int),
+            "pa_copy_blocks": ([pc, vp, i32, vp, vp], C.c_int),
+            "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+            "pa_decode": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, sz, vp, vp],
+                          C.c_int),
+            "pa_prefill_varlen": ([vp, vp, C.c_int, pc, vp, i32, vp, vp, i32, i32, i32, i32, f32, i32,
+                                   vp, vp], C.c_int),
+            "pa_pool_create": ([i64, i32, vp, C.POINTER(vp)], C.c_int),
+            "pa_pool_destroy": ([vp], None),
+            "pa_pool_add_seq": ([vp, i64], C.c_int),
+            "pa_pool_append": ([vp, i64, i32, vp, vp, vp], C.c_int),
+            "pa_pool_fork": ([vp, i64, i64], C.c_int),
+            "pa_pool_free_seq": ([vp, i64], C.c_int),
+            "pa_pool_block_table": ([vp, vp, i32, i32, vp, vp], C.c_int),
+            "pa_pool_num_free": ([vp], i64),
+            "pa_pool_ref_count": ([vp, i64], i32),
+            "pa_pool_seq_len": ([vp, i64], i32),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def pa_status_str(status: int) -> str:
+    return library().pa_status_str(int(status)).decode()
+
+
+def pa_version() -> int:
+    return library().pa_version()
+
+
+def _check(status, where):
+    if status != 0:
+        raise PaError(status, where)
+
+
+def torch_dtype_code(dt) -> int:
+    if dt not in _TORCH_CODE:
+        raise TypeError("unsupported dtype %s" % dt)
+    return _TORCH_CODE[dt]
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(t: torch.Tensor):
+    return C.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _need(t, name, dtype=None, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a tensor" % name)
+    if cuda and not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+@dataclass
+class KVCache:
+    """One layer's paged cache: k_cache, v_cache [num_blocks, num_kv_heads,
+    block_size, head_size] (float16 / bfloat16 / float8_e4m3fn)."""
+    k_cache: torch.Tensor
+    v_cache: torch.Tensor
+    k_scale: float = 1.0
+    v_scale: float = 1.0
+
+    def __post_init__(self):
+        _need(self.k_cache, "k_cache")
+        _need(self.v_cache, "v_cache")
+        if self.k_cache.shape != self.v_cache.shape or self.k_cache.dtype != self.v_cache.dtype:
+            raise ValueError("k_cache and v_cache must match")
+        if self.k_cache.dim() != 4:
+            raise ValueError("cache must be [num_blocks, num_kv_heads, block_size, head_size]")
+
+    @property
+    def num_blocks(self):
+        return self.k_cache.shape[0]
+
+    @property
+    def num_kv_heads(self):
+        return self.k_cache.shape[1]
+
+    @property
+    def block_size(self):
+        return self.k_cache.shape[2]
+
+    @property
+    def head_size(self):
+        return self.k_cache.shape[3]
+
+    @property
+    def dtype_code(self):
+        return torch_dtype_code(self.k_cache.dtype)
+
+    def c_struct(self) -> _Cache:
+        nb, hkv, bs, d = self.k_cache.shape
+        return _Cache(self.k_cache.data_ptr(), self.v_cache.data_ptr(), nb, bs, hkv, d,
+                      self.dtype_code, float(self.k_scale), float(self.v_scale))
+
+
+def pa_kv_cache_write(cache: KVCache, k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                      dev_status: Optional[torch.Tensor] = None):
+    """k, v: [T, num_kv_heads, head_size] (or [T, >= num_kv_heads*head_size]
+    rows with a common token stride); slot_mapping int64 [T] (< 0 skips)."""
+    _need(slot_mapping, "slot_mapping", torch.int64)
+    T = slot_mapping.shape[0]
+    for name, t in (("k", k), ("v", v)):
+        if not t.is_cuda or t.stride(-1) != 1 or t.shape[0] != T:
+            raise ValueError("%s must be a CUDA tensor of [T, ...] rows" % name)
+    if k.stride(0) != v.stride(0) or k.dtype != v.dtype:
+        raise ValueError("k and v must share dtype and token stride")
+    cs = cache.c_struct()
+    st = library().pa_kv_cache_write(C.byref(cs), _ptr(k), _ptr(v), torch_dtype_code(k.dtype), T,
+                                     k.stride(0), _ptr(slot_mapping), _ptr(dev_status), _stream(k))
+    _check(st, "pa_kv_cache_write")
+
+
+def pa_copy_blocks(cache: KVCache, src_dst_pairs: torch.Tensor, dev_status: Optional[torch.Tensor] = None):
+    _need(src_dst_pairs, "src_dst_pairs", torch.int32)
+    cs = cache.c_struct()
+    n = src_dst_pairs.numel() // 2
+    st = library().pa_copy_blocks(C.byref(cs), _ptr(src_dst_pairs), n, _ptr(dev_status),
+                                  _stream(cache.k_cache))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_decode_workspace_size(num_seqs, num_heads, head_size, max_seq_len, block_size, partition_size=0) -> int:
+    return int(library().pa_decode_workspace_size(num_seqs, num_heads, head_size, max_seq_len,
+                                                  block_size, partition_size))
+
+
+def pa_decode(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,
+              seq_lens: torch.Tensor, max_seq_len: int, scale: float, partition_size: int = 0,
+              workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None):
+    """out, q: [num_seqs, num_heads, head_size]; block_table int32 [num_seqs,
+    max_blocks_per_seq]; seq_lens int32 [num_seqs] (attended lengths)."""
+    _need(q, "q")
+    _need(out, "out", q.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, H, D = q.shape
+    if workspace is not None:
+        _need(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    cs = cache.c_struct()
+    st = library().pa_decode(_ptr(out), _ptr(q), torch_dtype_code(q.dtype), C.byref(cs), _ptr(block_table),
+                             block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), H, float(scale),
+                             int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(q))
+    _check(st, "pa_decode")
+
+
+def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,
+                      cu_seq_lens_q: torch.Tensor, cu_seq_lens_k: torch.Tensor, max_seqlen_q: int,
+                      max_seqlen_k: int, scale: float, causal: bool = True,
+                      dev_status: Optional[torch.Tensor] = None):
+    """q, out: [total_q, num_heads, head_size]; cu_seq_lens_q/k int32 [B+1]."""
+    _need(q, "q")
+    _need(out, "out", q.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(cu_seq_lens_q, "cu_seq_lens_q", torch.int32)
+    _need(cu_seq_lens_k, "cu_seq_lens_k", torch.int32)
+    H = q.shape[1]
+    B = cu_seq_lens_q.shape[0] - 1
+    cs = cache.c_struct()
+    st = library().pa_prefill_varlen(_ptr(out), _ptr(q), torch_dtype_code(q.dtype), C.byref(cs),
+                                     _ptr(block_table), block_table.shape[1], _ptr(cu_seq_lens_q),
+                                     _ptr(cu_seq_lens_k), B, int(max_seqlen_q), int(max_seqlen_k), H,
+                                     float(scale), 1 if causal else 0, _ptr(dev_status), _stream(q))
+    _check(st, "pa_prefill_varlen")
+
+
+class BlockPool:
+    """Host block pool (FIFO free list, reference counts, fork, copy-on-write)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        L = library()
+        self._h = C.c_void_p()
+        order = None
+        if free_order is not None:
+            order = (C.c_int32 * num_blocks)(*[int(x) for x in free_order])
+        _check(L.pa_pool_create(num_blocks, block_size, order, C.byref(self._h)), "pa_pool_create")
+        self.block_size = block_size
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.pa_pool_destroy(self._h)
+            self._h = None
+
+    def add_seq(self, seq_id: int):
+        _check(library().pa_pool_add_seq(self._h, seq_id), "pa_pool_add_seq")
+
+    def append(self, seq_id: int, n: int):
+        """Returns (slots list, cow pairs list)."""
+        slots = (C.c_int64 * max(n, 1))()
+        cow = (C.c_int32 * 2)()
+        ncow = C.c_int32(0)
+        _check(library().pa_pool_append(self._h, seq_id, n, slots, cow, C.byref(ncow)), "pa_pool_append")
+        return list(slots[:n]), [(cow[0], cow[1])] if ncow.value else []
+
+    def fork(self, parent: int, child: int):
+        _check(library().pa_pool_fork(self._h, parent, child), "pa_pool_fork")
+
+    def free_seq(self, seq_id: int):
+        _check(library().pa_pool_free_seq(self._h, seq_id), "pa_pool_free_seq")
+
+    def block_table(self, seq_ids, max_blocks: int):
+        n = len(seq_ids)
+        ids = (C.c_int64 * max(n, 1))(*seq_ids)
+        table = (C.c_int32 * max(n * max_blocks, 1))()
+        lens = (C.c_int32 * max(n, 1))()
+        _check(library().pa_pool_block_table(self._h, ids, n, max_blocks, table, lens), "pa_pool_block_table")
+        return [list(table[r * max_blocks:(r + 1) * max_blocks]) for r in range(n)], list(lens[:n])
+
+    def num_free(self) -> int:
+        return library().pa_pool_num_free(self._h)
+
+    def ref_count(self, block: int) -> int:
+        return library().pa_pool_ref_count(self._h, block)
+
+    def seq_len(self, seq_id: int) -> int:
+        return library().pa_pool_seq_len(self._h, seq_id)

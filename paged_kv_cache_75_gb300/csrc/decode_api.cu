@@ -1,0 +1,115 @@
+// pa_decode / pa_decode_workspace_size: argument checks and dispatch.
+#include <cmath>
+
+#include "decode_launch.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kAutoPartition = 512;
+
+int resolve_partition(int partition_size, int block_size) {
+    if (partition_size == 0) {
+        int p = kAutoPartition;
+        return p % block_size == 0 ? p : block_size * ((p + block_size - 1) / block_size);
+    }
+    return partition_size;
+}
+
+int max_parts_of(int max_seq_len, int partition) {
+    return max_seq_len <= partition ? 1 : (max_seq_len + partition - 1) / partition;
+}
+
+struct WsLayout {
+    size_t lse_off, o_off, bytes;
+};
+
+WsLayout ws_layout(int64_t num_seqs, int64_t num_heads, int64_t head_size, int max_parts) {
+    WsLayout w{0, 0, 0};
+    if (max_parts <= 1) return w;
+    const size_t rows = static_cast<size_t>(num_seqs) * num_heads * max_parts;
+    w.lse_off = 0;
+    w.o_off = (rows * 4 + 255) & ~static_cast<size_t>(255);
+    w.bytes = w.o_off + rows * head_size * 4;
+    return w;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                                           int32_t max_seq_len, int32_t block_size,
+                                           int32_t partition_size) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0 || block_size <= 0 ||
+        partition_size < 0)
+        return 0;
+    const int P = resolve_partition(partition_size, block_size);
+    return ws_layout(num_seqs, num_heads, head_size, max_parts_of(max_seq_len, P)).bytes;
+}
+
+extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                               int32_t num_heads, float scale, int32_t partition_size,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               pa_stream_t stream) {
+    pa_status st = check_cache(cache);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
+        partition_size < 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (out == nullptr || q == nullptr || block_table == nullptr || seq_lens == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(out) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u))
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int group = num_heads / cache->num_kv_heads;
+    const int D = cache->head_size, bs = cache->block_size;
+    if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+    if (bs != 16 && bs != 32 && bs != 64) return PA_ERR_UNSUPPORTED;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+    if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (cache->kv_dtype != PA_FP8_E4M3 && cache->kv_dtype != q_dtype) return PA_ERR_UNSUPPORTED;
+    if (cache->kv_dtype == PA_FP8_E4M3 &&
+        !(cache->k_scale > 0.f && std::isfinite(cache->k_scale) && cache->v_scale > 0.f &&
+          std::isfinite(cache->v_scale)))
+        return PA_ERR_INVALID_ARG;
+    const int P = resolve_partition(partition_size, bs);
+    if (P % bs != 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
+    const int max_parts = max_parts_of(max_seq_len, P);
+    const WsLayout w = ws_layout(num_seqs, num_heads, D, max_parts);
+    if (w.bytes > 0 && (workspace == nullptr || workspace_bytes < w.bytes ||
+                        (reinterpret_cast<uintptr_t>(workspace) & 15u)))
+        return PA_ERR_INVALID_ARG;
+
+    DecodeParams p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = static_cast<const uint8_t*>(cache->k_cache);
+    p.v_cache = static_cast<const uint8_t*>(cache->v_cache);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.ws_lse = w.bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse_off) : nullptr;
+    p.ws_o = w.bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + w.o_off) : nullptr;
+    p.status = dev_status;
+    p.num_blocks = cache->num_blocks;
+    p.block_size = bs;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.num_heads = num_heads;
+    p.num_seqs = num_seqs;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_seq_len = max_seq_len;
+    p.partition = P;
+    p.max_parts = max_parts;
+    const float k_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->k_scale : 1.f;
+    p.qk_scale = scale * k_scale * 1.4426950408889634f;
+    p.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cache->kv_dtype == PA_F16) return launch_decode_f16(p, D, group, s);
+    if (cache->kv_dtype == PA_BF16) return launch_decode_bf16(p, D, group, s);
+    return q_dtype == PA_F16 ? launch_decode_fp8_qf16(p, D, group, s) : launch_decode_fp8_qbf16(p, D, group, s);
+}

@@ -1,0 +1,550 @@
+// Paged single-query decode attention: kernel templates.
+//
+// What it computes follows the vLLM PagedAttention design doc ("分页注意力机制",
+// vllm.ooos.top/design/paged_attention): for one sequence and query head,
+// scores s_t = scale * q . K_t over the context tokens reached through the
+// block table (section Key), softmax by max subtraction (section Softmax:
+// m(x), f(x), l(x)), masked tokens excluded (section qk_max 和 logits), then
+// the value-weighted sum (section Value) written per sequence and head
+// (section Output).  The doc's grid has a third axis over context partitions
+// whose partial outputs are merged afterwards; here that is a log-sum-exp
+// merge in a second kernel.  Inputs follow "Paged 어텐션" (Decode 경로):
+// block_table [batch, max_blocks_per_seq] and per-sequence cache lengths.
+//
+// How (GB300 design, not the doc's):
+//  * persistent CTAs walk a flattened list of work items (sequence,
+//    partition, KV head); every CTA builds the list's per-sequence prefix in
+//    shared memory from seq_lens, so short and long sequences share the GPU
+//    without a max_num_partitions-shaped grid;
+//  * one producer warp streams each (block, KV head) page -- one contiguous
+//    block_size*head_size run in the [blocks][kv_heads][block_size][head]
+//    layout -- into a ring of shared-memory stages with 1-D bulk async copies
+//    (cp.async.bulk), completion counted on mbarriers;
+//  * four consumer warps split each page's tokens; all G query heads of a KV
+//    head are handled together, so a page is read once per KV head (GQA);
+//  * per-warp online softmax in fp32 (exp2 domain), warp-shuffle QK
+//    reductions, and one cross-warp merge per work item;
+//  * every mbarrier wait is bounded (PA_ERR_TIMEOUT, no hang).
+#pragma once
+
+#include "common.cuh"
+
+namespace pa {
+
+struct DecodeParams {
+    void* out;
+    const void* q;
+    const uint8_t* k_cache;
+    const uint8_t* v_cache;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    float* ws_lse;  // [B*H*max_parts]
+    float* ws_o;    // [B*H*max_parts*D]
+    int32_t* status;
+    int64_t num_blocks;
+    int32_t block_size;
+    int32_t num_kv_heads;
+    int32_t num_heads;
+    int32_t num_seqs;
+    int32_t max_blocks;
+    int32_t max_seq_len;
+    int32_t partition;  // tokens per partition, multiple of block_size
+    int32_t max_parts;  // ceil(max_seq_len / partition)
+    int32_t stages;     // ring depth
+    float qk_scale;     // scale * k_scale * log2(e)
+    float v_scale;
+};
+
+template <int QDT, int KVDT, int D, int G>
+struct DecodeCfg {
+    static constexpr int NCW = 4;                     // consumer warps
+    static constexpr int THREADS = (NCW + 1) * 32;    // + one producer warp
+    static constexpr int TG = (G >= 8) ? 2 : 4;       // tokens per warp step
+    static constexpr int LPT = 32 / TG;               // lanes per token (QK)
+    static constexpr int EPL = D / LPT;               // key elements per lane
+    static constexpr int KB = dtype_traits<KVDT>::bytes;
+    static constexpr int QB = dtype_traits<QDT>::bytes;
+    static constexpr int TPI = NCW * TG;              // tokens per block step
+    static constexpr int DL = D / 32;                 // value elements per lane
+    static constexpr int VB = (EPL * KB < 16) ? EPL * KB : 16;  // K vector bytes
+    static constexpr int NV = EPL * KB / VB;          // K vectors per lane
+    static constexpr int ROWB = D * KB;               // bytes per token row
+    static constexpr int QBYTES = G * D * QB;         // one item's queries
+    static constexpr int MERGE_FLOATS = NCW * G * (D + 2);
+    static_assert(D % LPT == 0 && EPL * KB >= 4, "unsupported head size / group");
+};
+
+// shared memory carve-up (byte offsets from the 1 KB-aligned base)
+struct DecodeSmem {
+    uint32_t ring, qbuf, merge, prefix, bars, flags, total;
+    __host__ __device__ static DecodeSmem make(int stages, int page_bytes, int qbytes,
+                                               int merge_floats, int num_seqs) {
+        DecodeSmem s;
+        uint32_t o = 0;
+        s.ring = o;
+        o += static_cast<uint32_t>(stages) * 2u * page_bytes;
+        s.qbuf = o;
+        o += 2u * ((qbytes + 127u) & ~127u);
+        s.merge = o;
+        o += static_cast<uint32_t>(merge_floats) * 4u;
+        o = (o + 15u) & ~15u;
+        s.prefix = o;
+        o += (static_cast<uint32_t>(num_seqs) + 1u) * 4u;
+        o = (o + 7u) & ~7u;
+        s.bars = o;
+        o += (2u * stages + 4u) * 8u;
+        s.flags = o;
+        o += (static_cast<uint32_t>(stages) + 1u) * 4u;
+        s.total = (o + 127u) & ~127u;
+        return s;
+    }
+};
+
+// number of partitions a sequence of length L splits into (>= 1)
+__device__ __forceinline__ int parts_of(int L, int P) { return L <= P ? 1 : (L + P - 1) / P; }
+
+// A length is usable iff 0 <= L <= max_seq_len and L fits the table row.
+__device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
+    int L = __ldg(p.seq_lens + b);
+    if (L < 0 || L > p.max_seq_len || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks) * p.block_size)
+        return -1;
+    return L;
+}
+
+// prefix[b] = sum of parts over sequences < b; prefix[B] = total.
+// All threads of the block take part.
+__device__ inline void build_prefix(const DecodeParams& p, int32_t* prefix, int32_t* scratch) {
+    const int B = p.num_seqs;
+    const int nt = blockDim.x, t = threadIdx.x;
+    const int chunk = (B + nt - 1) / nt;
+    const int b0 = t * chunk, b1 = min(B, b0 + chunk);
+    int local = 0;
+    for (int b = b0; b < b1; ++b) {
+        int L = checked_len(p, b);
+        if (L < 0) report(p.status, PA_ERR_INVALID_ARG);
+        local += parts_of(L < 0 ? 0 : L, p.partition);
+    }
+    // inclusive scan inside the warp
+    const int lane = t & 31, warp = t >> 5;
+    int v = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    if (lane == 31) scratch[warp] = v;
+    __syncthreads();
+    if (t == 0) {
+        int run = 0;
+        for (int w = 0; w < (nt + 31) / 32; ++w) {
+            int x = scratch[w];
+            scratch[w] = run;
+            run += x;
+        }
+        prefix[B] = run;
+    }
+    __syncthreads();
+    int run = scratch[warp] + v - local;
+    for (int b = b0; b < b1; ++b) {
+        prefix[b] = run;
+        int L = checked_len(p, b);
+        run += parts_of(L < 0 ? 0 : L, p.partition);
+    }
+    __syncthreads();
+}
+
+struct Item {
+    int b, part, kvh, L, t1, j0, j1, nparts;
+};
+
+__device__ __forceinline__ Item decode_item(const DecodeParams& p, const int32_t* prefix, int i) {
+    Item it;
+    const int sp = i / p.num_kv_heads;
+    it.kvh = i - sp * p.num_kv_heads;
+    int lo = 0, hi = p.num_seqs - 1;  // largest b with prefix[b] <= sp
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= sp) lo = mid;
+        else hi = mid - 1;
+    }
+    it.b = lo;
+    it.part = sp - prefix[lo];
+    int L = checked_len(p, lo);
+    it.L = L < 0 ? 0 : L;
+    it.nparts = parts_of(it.L, p.partition);
+    const int t0 = it.part * p.partition;
+    it.t1 = min(it.L, t0 + p.partition);
+    it.j0 = t0 / p.block_size;
+    it.j1 = it.t1 > t0 ? (it.t1 + p.block_size - 1) / p.block_size : it.j0;
+    return it;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int QDT, int KVDT, int D, int G>
+__global__ void __launch_bounds__(DecodeCfg<QDT, KVDT, D, G>::THREADS)
+paged_decode_kernel(const DecodeParams p) {
+    using C = DecodeCfg<QDT, KVDT, D, G>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const int page_bytes = p.block_size * C::ROWB;
+    const DecodeSmem L = DecodeSmem::make(p.stages, page_bytes, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
+    uint8_t* ring = smem_raw + L.ring;
+    uint8_t* qbuf = smem_raw + L.qbuf;
+    float* merge = reinterpret_cast<float*>(smem_raw + L.merge);
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem_raw + L.prefix);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L.flags);
+    volatile int* page_ok = abort_flag + 1;
+    const int S = p.stages;
+    const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8u * S;
+    const uint32_t qfull0 = full0 + 16u * S, qempty0 = qfull0 + 16u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, C::NCW);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(qfull0 + 8u * s, 1);
+            mbar_init(qempty0 + 8u * s, C::NCW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // merge area doubles as scan scratch before the first item
+    build_prefix(p, prefix, reinterpret_cast<int32_t*>(merge));
+    const int n_items = prefix[p.num_seqs] * p.num_kv_heads;
+
+    if (warp == C::NCW) {
+        // ------------------------------ producer ------------------------------
+        const uint64_t policy = policy_evict_first();
+        uint32_t fill = 0;    // ring slots used so far by this CTA
+        uint32_t issued = 0;  // fills that started copies (all but bad pages)
+        uint32_t qn = 0;      // items issued so far
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++qn) {
+            const Item it = decode_item(p, prefix, i);
+            if (lane == 0) {
+                const uint32_t slot = qn & 1u;
+                if (qn >= 2) ok = mbar_wait(qempty0 + 8u * slot, ((qn >> 1) - 1) & 1u, p.status, abort_flag);
+                if (ok) {
+                    const uint8_t* src = static_cast<const uint8_t*>(p.q) +
+                                         (static_cast<int64_t>(it.b) * p.num_heads + it.kvh * G) * D * C::QB;
+                    mbar_expect_tx(qfull0 + 8u * slot, C::QBYTES);
+                    bulk_g2s(smem_addr(qbuf + slot * ((C::QBYTES + 127) & ~127)), src, C::QBYTES,
+                             qfull0 + 8u * slot);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            const int32_t* row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
+            for (int jb = it.j0; jb < it.j1 && ok; jb += 32) {
+                const int j = jb + lane;
+                int32_t id = j < it.j1 ? __ldg(row + j) : 0;
+                const int cnt = min(32, it.j1 - jb);
+                for (int k = 0; k < cnt; ++k) {
+                    const int32_t idk = __shfl_sync(0xffffffffu, id, k);
+                    if (lane == 0) {
+                        const uint32_t s = fill % S;
+                        if (fill >= static_cast<uint32_t>(S))
+                            ok = mbar_wait(empty0 + 8u * s, ((fill / S) - 1) & 1u, p.status, abort_flag);
+                        if (ok) {
+                            const bool good = idk >= 0 && idk < p.num_blocks;
+                            page_ok[s] = good ? 1 : 0;
+                            if (good) {
+                                const int64_t off = (static_cast<int64_t>(idk) * p.num_kv_heads + it.kvh) *
+                                                    static_cast<int64_t>(page_bytes);
+                                const uint32_t dst = smem_addr(ring) + s * 2u * page_bytes;
+                                mbar_expect_tx(full0 + 8u * s, 2u * page_bytes);
+                                bulk_g2s_hint(dst, p.k_cache + off, page_bytes, full0 + 8u * s, policy);
+                                bulk_g2s_hint(dst + page_bytes, p.v_cache + off, page_bytes, full0 + 8u * s,
+                                              policy);
+                                issued = fill + 1;
+                            } else {
+                                report(p.status, PA_ERR_BAD_BLOCK);
+                                mbar_arrive(full0 + 8u * s);
+                            }
+                        }
+                    }
+                    ++fill;
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                }
+            }
+        }
+        // do not leave while copies may still land: wait for every stage that
+        // was filled but (after an abort) possibly not consumed
+        if (lane == 0 && *abort_flag) {
+            const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+            const uint64_t t0 = global_timer_ns();
+            for (uint32_t f = first; f < issued; ++f) {
+                const uint32_t s = f % S;
+                while (!mbar_try_wait(full0 + 8u * s, (f / S) & 1u)) {
+                    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------- consumers ------------------------------
+    const int tg = lane / C::LPT;  // token slot of this lane in a warp step
+    const int c = lane % C::LPT;   // lane's chunk of the key row
+    uint32_t fill = 0;
+    uint32_t qn = 0;
+    for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++qn) {
+        const Item it = decode_item(p, prefix, i);
+        const uint32_t slot = qn & 1u;
+        bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8u * slot, (qn >> 1) & 1u, p.status, abort_flag));
+        // queries of this KV head's group, permuted like the key chunks
+        float qf[G][C::EPL];
+        {
+            const uint8_t* qs = qbuf + slot * ((C::QBYTES + 127) & ~127);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+#pragma unroll
+                for (int v = 0; v < C::NV; ++v) {
+                    const int e0 = (v * C::LPT + c) * C::VB / C::KB;  // first element of vector
+                    constexpr int EV = C::VB / C::KB;                 // elements per vector
+#pragma unroll
+                    for (int e = 0; e < EV; e += 2) {
+                        const uint32_t w = *reinterpret_cast<const uint32_t*>(qs + (g * D + e0 + e) * C::QB);
+                        const float2 f = kv_pair<QDT>(w);
+                        qf[g][v * EV + e] = f.x * p.qk_scale;
+                        qf[g][v * EV + e + 1] = f.y * p.qk_scale;
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty0 + 8u * slot);
+
+        float m[G], l[G], acc[G][C::DL];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int d = 0; d < C::DL; ++d) acc[g][d] = 0.f;
+        }
+
+        for (int j = it.j0; j < it.j1 && ok; ++j, ++fill) {
+            const uint32_t s = fill % S;
+            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8u * s, (fill / S) & 1u, p.status, abort_flag))) {
+                ok = false;
+                break;
+            }
+            const bool page_good = page_ok[s] != 0;
+            const uint8_t* Kp = ring + s * 2u * page_bytes;
+            const uint8_t* Vp = Kp + page_bytes;
+            for (int st = 0; st < p.block_size; st += C::TPI) {
+                const int tok = st + warp * C::TG + tg;
+                const int pos = j * p.block_size + tok;
+                const bool valid = page_good && pos < it.t1;
+                // ---- QK: partial dot over this lane's chunk, then reduce ----
+                float sc[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) sc[g] = 0.f;
+                const uint8_t* krow = Kp + tok * C::ROWB;
+#pragma unroll
+                for (int v = 0; v < C::NV; ++v) {
+                    const uint8_t* src = krow + (v * C::LPT + c) * C::VB;
+                    uint32_t w[4];
+                    if constexpr (C::VB == 16) {
+                        const uint4 x = *reinterpret_cast<const uint4*>(src);
+                        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+                    } else if constexpr (C::VB == 8) {
+                        const uint2 x = *reinterpret_cast<const uint2*>(src);
+                        w[0] = x.x; w[1] = x.y; w[2] = 0; w[3] = 0;
+                    } else {
+                        w[0] = *reinterpret_cast<const uint32_t*>(src); w[1] = w[2] = w[3] = 0;
+                    }
+                    constexpr int NW = C::VB / 4;  // 32-bit words per vector
+                    constexpr int EV = C::VB / C::KB;
+#pragma unroll
+                    for (int x = 0; x < NW; ++x) {
+                        if constexpr (C::KB == 2) {
+                            const float2 f = kv_pair<KVDT>(w[x]);
+#pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                sc[g] = fmaf(qf[g][v * EV + 2 * x], f.x, sc[g]);
+                                sc[g] = fmaf(qf[g][v * EV + 2 * x + 1], f.y, sc[g]);
+                            }
+                        } else {
+                            const float2 f0 = e4m3x2_to_f2(w[x]);
+                            const float2 f1 = e4m3x2_to_f2(w[x] >> 16);
+#pragma unroll
+                            for (int g = 0; g < G; ++g) {
+                                sc[g] = fmaf(qf[g][v * EV + 4 * x], f0.x, sc[g]);
+                                sc[g] = fmaf(qf[g][v * EV + 4 * x + 1], f0.y, sc[g]);
+                                sc[g] = fmaf(qf[g][v * EV + 4 * x + 2], f1.x, sc[g]);
+                                sc[g] = fmaf(qf[g][v * EV + 4 * x + 3], f1.y, sc[g]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+#pragma unroll
+                    for (int o = 1; o < C::LPT; o <<= 1) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], o);
+                    if (!valid) sc[g] = -INFINITY;
+                }
+                // ---- online softmax (per warp, exp2 domain) ----
+                float pr[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float tmax = sc[g];
+#pragma unroll
+                    for (int o = C::LPT; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+                    const float mnew = fmaxf(m[g], tmax);
+                    if (mnew == -INFINITY) {
+                        pr[g] = 0.f;
+                    } else {
+                        if (mnew > m[g]) {
+                            const float alpha = fast_exp2(m[g] - mnew);
+                            l[g] *= alpha;
+#pragma unroll
+                            for (int d = 0; d < C::DL; ++d) acc[g][d] *= alpha;
+                            m[g] = mnew;
+                        }
+                        pr[g] = fast_exp2(sc[g] - mnew);
+                    }
+                    l[g] += pr[g];
+                }
+                // ---- PV: every lane owns DL consecutive value columns ----
+#pragma unroll
+                for (int tt = 0; tt < C::TG; ++tt) {
+                    const uint8_t* vrow = Vp + (st + warp * C::TG + tt) * C::ROWB + lane * C::DL * C::KB;
+                    float vf[C::DL];
+                    if constexpr (C::KB == 2) {
+                        if constexpr (C::DL == 4) {
+                            const uint2 x = *reinterpret_cast<const uint2*>(vrow);
+                            const float2 a = kv_pair<KVDT>(x.x), b2 = kv_pair<KVDT>(x.y);
+                            vf[0] = a.x; vf[1] = a.y; vf[2] = b2.x; vf[3] = b2.y;
+                        } else {
+                            const float2 a = kv_pair<KVDT>(*reinterpret_cast<const uint32_t*>(vrow));
+                            vf[0] = a.x; vf[1] = a.y;
+                        }
+                    } else {
+                        if constexpr (C::DL == 4) {
+                            const uint32_t x = *reinterpret_cast<const uint32_t*>(vrow);
+                            const float2 a = e4m3x2_to_f2(x), b2 = e4m3x2_to_f2(x >> 16);
+                            vf[0] = a.x; vf[1] = a.y; vf[2] = b2.x; vf[3] = b2.y;
+                        } else {
+                            const float2 a = e4m3x2_to_f2(*reinterpret_cast<const uint16_t*>(vrow));
+                            vf[0] = a.x; vf[1] = a.y;
+                        }
+                    }
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float pg = __shfl_sync(0xffffffffu, pr[g], tt * C::LPT);
+#pragma unroll
+                        for (int d = 0; d < C::DL; ++d) acc[g][d] = fmaf(pg, vf[d], acc[g][d]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8u * s);
+        }
+
+        // ---- merge the four warps' partial softmax states ----
+        {
+            float* mw = merge + warp * G * (D + 2);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float lw = l[g];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+#pragma unroll
+                for (int d = 0; d < C::DL; ++d) mw[g * (D + 2) + lane * C::DL + d] = acc[g][d];
+                if (lane == 0) {
+                    mw[g * (D + 2) + D] = m[g];
+                    mw[g * (D + 2) + D + 1] = lw * (1.f / C::LPT);  // each token counted LPT times
+                }
+            }
+        }
+        named_bar_sync(1, C::NCW * 32);
+        {
+            const int tid = threadIdx.x;  // 0 .. NCW*32-1
+            const bool direct = it.nparts == 1;
+            for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
+                const int g = (2 * e) / D, d = (2 * e) % D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, merge[(w * G + g) * (D + 2) + D]);
+                float o0 = 0.f, o1 = 0.f, lsum = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int w = 0; w < C::NCW; ++w) {
+                        const float* mw = merge + (w * G + g) * (D + 2);
+                        const float a = fast_exp2(mw[D] - M);
+                        lsum = fmaf(a, mw[D + 1], lsum);
+                        o0 = fmaf(a, mw[d], o0);
+                        o1 = fmaf(a, mw[d + 1], o1);
+                    }
+                    const float inv = p.v_scale / lsum;
+                    o0 *= inv;
+                    o1 *= inv;
+                }
+                const int h = it.kvh * G + g;
+                const int64_t bh = static_cast<int64_t>(it.b) * p.num_heads + h;
+                if (direct) {
+                    using T = typename dtype_traits<QDT>::storage;
+                    T* out = static_cast<T*>(p.out) + bh * D + d;
+                    out[0] = dtype_traits<QDT>::from_f(o0);
+                    out[1] = dtype_traits<QDT>::from_f(o1);
+                } else {
+                    const int64_t r = bh * p.max_parts + it.part;
+                    *reinterpret_cast<float2*>(p.ws_o + r * D + d) = make_float2(o0, o1);
+                    if (d == 0) p.ws_lse[r] = M == -INFINITY ? -INFINITY : M + __log2f(lsum);
+                }
+            }
+        }
+        named_bar_sync(1, C::NCW * 32);
+    }
+}
+
+// Log-sum-exp merge of the partitions of every (sequence, head) that was
+// split.  One warp per (sequence, head); lanes own D/32 output columns.
+template <int QDT, int D>
+__global__ void __launch_bounds__(256)
+paged_decode_reduce_kernel(const DecodeParams p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t bh = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+    if (bh >= static_cast<int64_t>(p.num_seqs) * p.num_heads) return;
+    const int b = static_cast<int>(bh / p.num_heads);
+    const int Lc = checked_len(p, b);
+    const int L = Lc < 0 ? 0 : Lc;
+    const int np = parts_of(L, p.partition);
+    if (np <= 1) return;
+    const float* lse = p.ws_lse + bh * p.max_parts;
+    float M = -INFINITY;
+    for (int i = lane; i < np; i += 32) M = fmaxf(M, lse[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    constexpr int DL = D / 32;
+    float acc[DL];
+#pragma unroll
+    for (int d = 0; d < DL; ++d) acc[d] = 0.f;
+    float wsum = 0.f;
+    if (M != -INFINITY) {
+        const float* o = p.ws_o + bh * p.max_parts * D + lane * DL;
+        for (int i = 0; i < np; ++i) {
+            const float w = fast_exp2(lse[i] - M);
+            wsum += w;
+#pragma unroll
+            for (int d = 0; d < DL; ++d) acc[d] = fmaf(w, o[static_cast<int64_t>(i) * D + d], acc[d]);
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    using T = typename dtype_traits<QDT>::storage;
+    T* out = static_cast<T*>(p.out) + bh * D + lane * DL;
+#pragma unroll
+    for (int d = 0; d < DL; ++d) out[d] = dtype_traits<QDT>::from_f(acc[d] * inv);
+}
+
+}  // namespace pa

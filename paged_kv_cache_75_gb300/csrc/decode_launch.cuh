@@ -1,0 +1,65 @@
+// Host-side launch of the paged decode kernels for one (q dtype, KV dtype)
+// pair; included by the per-dtype translation units.
+#pragma once
+
+#include <cmath>
+
+#include "decode_impl.cuh"
+#include "launch.h"
+
+namespace pa {
+
+// ring depth: as many (K, V) page pairs as fit in about 64 KB, at least 2
+inline int decode_stages(int page_bytes) {
+    int s = (64 * 1024) / (2 * page_bytes);
+    return s < 2 ? 2 : (s > 8 ? 8 : s);
+}
+
+template <int QDT, int KVDT, int D, int G>
+pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
+    using C = DecodeCfg<QDT, KVDT, D, G>;
+    const int page_bytes = p.block_size * C::ROWB;
+    p.stages = decode_stages(page_bytes);
+    const DecodeSmem L = DecodeSmem::make(p.stages, page_bytes, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
+    const int smem = static_cast<int>(L.total) + 1024;  // slack for the 1 KB base alignment
+    if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
+    auto kern = paged_decode_kernel<QDT, KVDT, D, G>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, smem) != cudaSuccess ||
+        per_sm <= 0)
+        return PA_ERR_CUDA;
+    const int sms = device_sm_count();
+    const int64_t max_items = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    const int grid = static_cast<int>(max_items < cap ? max_items : cap);
+    if (grid <= 0) return PA_OK;
+    kern<<<grid, C::THREADS, smem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (p.max_parts > 1) {
+        const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_heads;
+        const int rgrid = static_cast<int>((pairs + 7) / 8);
+        paged_decode_reduce_kernel<QDT, D><<<rgrid, 256, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+template <int QDT, int KVDT>
+pa_status launch_decode_dtype(const DecodeParams& p, int head_size, int group, cudaStream_t s) {
+#define PA_CASE(D, G) \
+    if (head_size == D && group == G) return launch_decode_t<QDT, KVDT, D, G>(p, s);
+    PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
+    PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
+#undef PA_CASE
+    return PA_ERR_UNSUPPORTED;
+}
+
+// one per translation unit
+pa_status launch_decode_f16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
+pa_status launch_decode_bf16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
+pa_status launch_decode_fp8_qf16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
+pa_status launch_decode_fp8_qbf16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
+
+}  // namespace pa

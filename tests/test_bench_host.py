@@ -1,0 +1,70 @@
+"""Host logic of bench.py: the slot computation through the native pool
+agrees with the oracle's slot formula, the CPU sample is bounded, and the
+multi-rank aggregation (max time, summed units) works over gloo with two
+ranks on the CPU."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+import bench
+import oracle
+from paged_kv_cache_75_gb300 import build as pkg_build
+from paged_kv_cache_75_gb300 import workloads as W
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pkg_build.build()
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_bench_slots_match_oracle(bs):
+    rng = np.random.default_rng(bs)
+    lens = rng.integers(1, 300, size=40)
+    lens[:4] = [1, bs, bs + 1, 2 * bs]
+    nb = sum(W.pages_for(x, bs) for x in lens) + 17
+    bt = W.assign_blocks(rng, lens, bs, nb)
+    got = bench.DecodeStep._slots_from_pool(bt, lens, bs, nb)
+    exp = oracle.slot_mapping(bt, bs, np.arange(len(lens)), lens - 1)
+    assert np.array_equal(got, exp)
+
+
+def test_p2_tiny_workload_slots():
+    case, _ = bench.build_workload("tiny", "cpu")
+    lens = case.seq_lens.numpy()
+    got = bench.DecodeStep._slots_from_pool(case.block_table.numpy(), lens, 32, 8)
+    assert list(got) == [94, 32, 198]
+
+
+def test_cpu_sample_is_bounded():
+    case = W.make_decode_case(1, [1000] * 64, 8, 8, 128, 16, 4100, W.F16, W.F16)
+    idx, nbytes = bench.cpu_sample_indices(case, case.kv_bytes() / 4)
+    assert nbytes <= case.kv_bytes() / 4 + 1 and len(idx) == 16
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t, u = bench.aggregate(float(rank + 1) * 10.0, 100.0 + rank, world)
+    q.put((rank, t, u))
+    dist.destroy_process_group()
+
+
+def test_aggregate_two_ranks_gloo():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+    assert res == [(0, 20.0, 201.0), (1, 20.0, 201.0)]

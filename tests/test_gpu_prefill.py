@@ -1,0 +1,137 @@
+"""GPU parity of pa_prefill_varlen against the oracle: the varlen worked
+example, ragged random batches, causal and not, and the mixed
+prefill + decode workload (sampled rows)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_75_gb300 as pk
+from golden_io import read_golden
+from gpu_util import assert_close, dev_status
+from paged_kv_cache_75_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def make(seed, lq, lk, H, Hkv, bs, dtype=W.BF16, D=128, extra_blocks=3):
+    g = torch.Generator().manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    nb = sum(W.pages_for(x, bs) for x in lk) + extra_blocks
+    mb = max(1, max(W.pages_for(x, bs) for x in lk))
+    bt = W.assign_blocks(rng, lk, bs, nb, mb)
+    q = W.random_values(g, (sum(lq), H, D), dtype)
+    kc = W.random_values(g, (nb, Hkv, bs, D), dtype)
+    vc = W.random_values(g, (nb, Hkv, bs, D), dtype)
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    return q, kc, vc, bt, cu_q, cu_k
+
+
+def run_gpu(q, kc, vc, bt, cu_q, cu_k, scale, causal, dtype, max_q=None, max_k=None, status=None):
+    lq = np.diff(cu_q)
+    lk = np.diff(cu_k)
+    out = torch.empty_like(q, device=DEV)
+    st = dev_status() if status is None else status
+    pk.pa_prefill_varlen(out, q.to(DEV), pk.KVCache(kc.to(DEV), vc.to(DEV)), torch.as_tensor(bt).to(DEV),
+                         torch.as_tensor(cu_q).to(DEV), torch.as_tensor(cu_k).to(DEV),
+                         int(lq.max()) if max_q is None else max_q, int(lk.max()) if max_k is None else max_k,
+                         scale, causal, st)
+    torch.cuda.synchronize()
+    return W.as_bits(out), int(st.item())
+
+
+def run_oracle(q, kc, vc, bt, cu_q, cu_k, scale, causal, dtype):
+    _, ref, rc = oracle.prefill(W.as_bits(q), dtype, W.as_bits(kc), W.as_bits(vc), dtype, bt, cu_q, cu_k,
+                                scale, causal)
+    assert rc == 0
+    return ref
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_p2_varlen_example(causal):
+    gold = read_golden("p2_varlen_example.txt")
+    lq, lk = gold["query_lens"], gold["key_lens"]
+    q, kc, vc, bt, cu_q, cu_k = make(1, lq, lk, 8, 2, 16)
+    assert list(cu_q) == gold["cu_seq_lens_q"] and list(cu_k) == gold["cu_seq_lens_k"]
+    out, st = run_gpu(q, kc, vc, bt, cu_q, cu_k, 0.088, causal, W.BF16, gold["max_seqlen_q"][0],
+                      gold["max_seqlen_k"][0])
+    assert st == 0
+    ref = run_oracle(q, kc, vc, bt, cu_q, cu_k, 0.088, causal, W.BF16)
+    assert_close(out, ref, W.BF16, W.BF16)
+    assert np.all(out[:10] == 0)  # r0 has no keys: exact zeros
+
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.F16])
+@pytest.mark.parametrize("bs", [16, 32, 64])
+@pytest.mark.parametrize("G", [1, 4])
+@pytest.mark.parametrize("causal", [True, False])
+def test_prefill_ragged(dtype, bs, G, causal):
+    lq = [1, 64, 65, 130, 0, 17, 200, 3]
+    prior = [0, 10, 300, 0, 5, 64, 129, 0]
+    lk = [a + b for a, b in zip(lq, prior)]
+    lk[7] = 1  # fewer keys than queries
+    q, kc, vc, bt, cu_q, cu_k = make(2 + bs + G, lq, lk, 2 * G, 2, bs, dtype)
+    out, st = run_gpu(q, kc, vc, bt, cu_q, cu_k, 0.1, causal, dtype)
+    assert st == 0
+    ref = run_oracle(q, kc, vc, bt, cu_q, cu_k, 0.1, causal, dtype)
+    assert_close(out, ref, dtype, dtype)
+
+
+def test_single_query_rows_match_decode():
+    lens = [33, 1, 700, 64]
+    case = W.make_decode_case(3, lens, 8, 2, 128, 16, 60, W.BF16, W.BF16)
+    cu_q = np.arange(5, dtype=np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    out_p, st = run_gpu(case.q, case.k_cache, case.v_cache, case.block_table.numpy(), cu_q, cu_k, case.scale,
+                        True, W.BF16)
+    assert st == 0
+    ref = run_oracle(case.q, case.k_cache, case.v_cache, case.block_table.numpy(), cu_q, cu_k, case.scale, True,
+                     W.BF16)
+    assert_close(out_p, ref, W.BF16, W.BF16)
+
+
+def test_status_on_bad_block_and_length():
+    q, kc, vc, bt, cu_q, cu_k = make(4, [5, 9], [40, 9], 4, 2, 16)
+    bt2 = bt.copy()
+    bt2[0, 1] = 999
+    _, st = run_gpu(q, kc, vc, bt2, cu_q, cu_k, 0.1, True, W.BF16)
+    assert st == 6
+    _, st = run_gpu(q, kc, vc, bt, cu_q, cu_k, 0.1, True, W.BF16, max_k=20)
+    assert st == 1
+
+
+def test_full_mixed_varlen_sampled():
+    """The mixed batch (8 prefill + 120 decode sequences) in one call; the
+    oracle checks the first and last 16 query rows of every prefill sequence
+    (bottom-right alignment makes a row subset a valid sub-batch) and 20
+    decode rows."""
+    case = W.mixed_varlen(device=DEV)
+    lq = np.array(case.meta["query_lens"])
+    lk = np.array(case.meta["key_lens"])
+    cu_q = case.cu_seq_lens_q.cpu().numpy()
+    out = torch.empty_like(case.q)
+    st = dev_status()
+    pk.pa_prefill_varlen(out, case.q, pk.KVCache(case.k_cache, case.v_cache), case.block_table,
+                         case.cu_seq_lens_q, case.cu_seq_lens_k, int(lq.max()), int(lk.max()), case.scale, True, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    out_bits = W.as_bits(out)
+    q_bits = W.as_bits(case.q)
+    kc, vc = W.as_bits(case.k_cache), W.as_bits(case.v_cache)
+    bt = case.block_table.cpu().numpy()
+    rows, sub_q, sub_k, seqs = [], [], [], []
+    for b in list(range(8)) + list(range(8, 128, 6)):
+        r = min(16, lq[b])
+        prior = lk[b] - lq[b]
+        # first r rows: a sequence of r queries over prior + r keys
+        rows.append(np.arange(cu_q[b], cu_q[b] + r)); sub_q.append(r); sub_k.append(prior + r); seqs.append(b)
+        if lq[b] > r:  # last r rows: r queries over all keys
+            rows.append(np.arange(cu_q[b + 1] - r, cu_q[b + 1])); sub_q.append(r); sub_k.append(lk[b]); seqs.append(b)
+    rows = np.concatenate(rows)
+    cq = np.concatenate([[0], np.cumsum(sub_q)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(sub_k)]).astype(np.int32)
+    _, ref, rc = oracle.prefill(q_bits[rows], W.BF16, kc, vc, W.BF16, bt[seqs], cq, ck, case.scale, True)
+    assert rc == 0
+    assert_close(out_bits[rows], ref, W.BF16, W.BF16, "mixed sampled")
