@@ -248,9 +248,12 @@ class DecodeStep:
                           self.case.scale, self.P, self.ws, self.status)
 
 
-def build_workload(name, device):
+def build_workload(name, device, num_seqs=None, pool_blocks=None):
     if name == "mha":
-        return W.mha_decode(device=device), "mha_decode_64seq_32h_d128_bs16_fp16_len_u1_2048_pool10000"
+        B = num_seqs or 64
+        nb = pool_blocks or 10_000
+        tag = "mha_decode_%dseq_32h_d128_bs16_fp16_len_u1_2048_pool%d" % (B, nb)
+        return W.mha_decode(device=device, B=B, num_blocks=nb), tag
     if name == "gqa":
         return W.gqa_shared_decode(device=device), "gqa_decode_256seq_32q8kv_d128_bs16_bf16_lognormal1000_shared4"
     if name == "long":
@@ -372,7 +375,7 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    case, wname = build_workload(args.workload, dev)
+    case, wname = build_workload(args.workload, dev, args.num_seqs, args.pool_blocks)
     step = DecodeStep(case, dev, args.partition_size, wname)
     total_ms, decode_ms, clocks = timed_decode(step, args.steps, args.warmup, world)
     total_ms, kv_sum = aggregate(total_ms, float(step.kv_bytes) * args.steps, world)
@@ -466,6 +469,8 @@ def main():
     ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny"], default="mha")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-seqs", type=int, default=None, help="mha workload: sequences (smaller profiling case)")
+    ap.add_argument("--pool-blocks", type=int, default=None, help="mha workload: physical blocks in the pool")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -416,8 +416,11 @@ paged_decode_kernel(const DecodeParams p) {
                     l[g] += pr[g];
                 }
                 // ---- PV: every lane owns DL consecutive value columns ----
+                // (masked rows are skipped, not multiplied by 0: they may hold NaN)
+                const int tok0 = j * p.block_size + st + warp * C::TG;
 #pragma unroll
                 for (int tt = 0; tt < C::TG; ++tt) {
+                    if (!page_good || tok0 + tt >= it.t1) continue;  // warp-uniform
                     const uint8_t* vrow = Vp + (st + warp * C::TG + tt) * C::ROWB + lane * C::DL * C::KB;
                     float vf[C::DL];
                     if constexpr (C::KB == 2) {

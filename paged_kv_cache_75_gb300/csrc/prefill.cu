@@ -105,6 +105,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// (lo, hi) weights -> packed 16-bit pair, plus (bf16 only) the packed
+// residual pair that the first rounding dropped
+template <int DT>
+__device__ __forceinline__ void split_pair(float lo, float hi, uint32_t& main, uint32_t& rest) {
+    main = pack2<DT>(lo, hi);
+    if constexpr (DT == PA_BF16) {
+        const float lo_r = __uint_as_float(main << 16), hi_r = __uint_as_float(main & 0xffff0000u);
+        rest = pack2<DT>(lo - lo_r, hi - hi_r);
+    } else {
+        rest = 0u;
+    }
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -314,13 +327,17 @@ __global__ void __launch_bounds__(kThreads, 2) paged_prefill_mma_kernel(const Pr
                 o[n][3] *= al_b;
             }
             // ---- O += P V ----
+            // P goes to the tensor cores in V's 16-bit type.  fp16 keeps 11
+            // significant bits of each weight; bf16 keeps only 8, so for bf16
+            // P is carried as hi + lo (two bf16 terms, ~16 bits) and the
+            // product is taken twice.
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {  // 16 keys per k-step
-                uint32_t pa[4];
-                pa[0] = pack2<DT>(s[2 * kk][0], s[2 * kk][1]);
-                pa[1] = pack2<DT>(s[2 * kk][2], s[2 * kk][3]);
-                pa[2] = pack2<DT>(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-                pa[3] = pack2<DT>(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+                uint32_t pa[4], pl[4];
+                split_pair<DT>(s[2 * kk][0], s[2 * kk][1], pa[0], pl[0]);
+                split_pair<DT>(s[2 * kk][2], s[2 * kk][3], pa[1], pl[1]);
+                split_pair<DT>(s[2 * kk + 1][0], s[2 * kk + 1][1], pa[2], pl[2]);
+                split_pair<DT>(s[2 * kk + 1][2], s[2 * kk + 1][3], pa[3], pl[3]);
 #pragma unroll
                 for (int np = 0; np < 8; ++np) {  // pairs of 8-column blocks of D
                     uint32_t vb[4];
@@ -329,6 +346,10 @@ __global__ void __launch_bounds__(kThreads, 2) paged_prefill_mma_kernel(const Pr
                     ldsm_x4_t(vb, smem_addr(sV[buf]) + swz(key, np * 2 + (mi >> 1)));
                     mma16816<DT>(o[2 * np], pa, vb[0], vb[1]);
                     mma16816<DT>(o[2 * np + 1], pa, vb[2], vb[3]);
+                    if constexpr (DT == PA_BF16) {
+                        mma16816<DT>(o[2 * np], pl, vb[0], vb[1]);
+                        mma16816<DT>(o[2 * np + 1], pl, vb[2], vb[3]);
+                    }
                 }
             }
             __syncthreads();  // the buffer is refilled next iteration
