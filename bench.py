@@ -188,10 +188,9 @@ class DecodeStep:
         self.lens_np = lens
         B = len(lens)
         self.B = B
-        # a1: the slot of each sequence's newest token (position L-1) via the
-        # host block pool holding exactly this block table
+        # a1: the slot of each sequence's newest token (position L-1)
         bt = case.block_table.cpu().numpy()
-        self.slots_np = self._slots_from_pool(bt, lens, case.block_size, case.num_blocks)
+        self.slots_np = pk.pa_slot_mapping(bt, case.block_size, np.arange(B, dtype=np.int32), lens - 1)
         g = torch.Generator(device=device)
         g.manual_seed(12345)
         self.k_new = W.random_values(g, (B, case.num_kv_heads, case.head_size), case.q_dtype, device)
@@ -212,32 +211,6 @@ class DecodeStep:
         self.split = self.max_len > P
         self.launches_per_step = 2 + (1 if self.split else 0)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-
-    @staticmethod
-    def _slots_from_pool(bt, lens, bs, nb):
-        import paged_kv_cache_75_gb300 as pk
-        # free order that hands out exactly the table's blocks: first the
-        # blocks of every sequence's older tokens, sequence by sequence, then
-        # the blocks that only the newest tokens open
-        order, seen = [], set()
-        for b in range(len(lens)):
-            for j in range(W.pages_for(lens[b] - 1, bs)):
-                order.append(int(bt[b, j]))
-        for b in range(len(lens)):
-            if W.pages_for(lens[b], bs) > W.pages_for(lens[b] - 1, bs):
-                order.append(int(bt[b, W.pages_for(lens[b], bs) - 1]))
-        seen = set(order)
-        order += [i for i in range(nb) if i not in seen]
-        pool = pk.BlockPool(nb, bs, order)
-        slots = np.empty(len(lens), np.int64)
-        for b, L in enumerate(lens):
-            pool.add_seq(b)
-            if L > 1:
-                pool.append(b, int(L) - 1)
-        for b in range(len(lens)):
-            s, cow = pool.append(b, 1)
-            slots[b] = s[0]
-        return slots
 
     def write(self):
         self.pk.pa_kv_cache_write(self.cache, self.k_new, self.v_new, self.slots, self.status)

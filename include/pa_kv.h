@@ -193,6 +193,20 @@ pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtype, const pa
                             pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Slots of new tokens from a block table (host arrays): "Как работает paged
+ * attention?" 4.1 (logical block = pos / block_size, offset pos % block_size);
+ * vLLM paper summary §3.  For token i of sequence seq_idx[i] at position
+ * pos[i]: slot = block_table[seq][pos / block_size] * block_size
+ * + pos % block_size.  An entry < 0 (unallocated) or a position past the row
+ * gives slot -1.  block_table: host int32 [num_seqs][max_blocks]; seq_idx:
+ * host int32 [n] in [0, num_seqs); pos: host int64 [n] >= 0; slots_out: host
+ * int64 [n].  Returns PA_ERR_INVALID_ARG for a bad sequence index or position.
+ * ------------------------------------------------------------------------- */
+pa_status pa_slot_mapping(const int32_t* block_table, int32_t num_seqs, int32_t max_blocks,
+                          int32_t block_size, const int32_t* seq_idx, const int64_t* pos, int64_t n,
+                          int64_t* slots_out);
+
+/* ---------------------------------------------------------------------------
  * Host block pool ("Как работает paged attention?" 3.2 BlockManager, 3.3,
  * 4.1, 4.2; vLLM paper summary §2-4).  Host memory only.
  *

@@ -55,6 +55,7 @@ def library():
             "pa_pool_num_free": ([vp], i64),
             "pa_pool_ref_count": ([vp, i64], i32),
             "pa_pool_seq_len": ([vp, i64], i32),
+            "pa_slot_mapping": ([vp, i32, i32, i32, vp, vp, i64, vp], C.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -214,6 +215,21 @@ def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_
                                      _ptr(cu_seq_lens_k), B, int(max_seqlen_q), int(max_seqlen_k), H,
                                      float(scale), 1 if causal else 0, _ptr(dev_status), _stream(q))
     _check(st, "pa_prefill_varlen")
+
+
+def pa_slot_mapping(block_table, block_size: int, seq_idx, pos):
+    """Host helper: slots of new tokens (numpy int32 table [B, max_blocks],
+    seq_idx int32 [n], pos int64 [n]) -> numpy int64 [n]."""
+    import numpy as np
+    bt = np.ascontiguousarray(block_table, np.int32)
+    si = np.ascontiguousarray(seq_idx, np.int32)
+    ps = np.ascontiguousarray(pos, np.int64)
+    out = np.empty(ps.shape[0], np.int64)
+    st = library().pa_slot_mapping(bt.ctypes.data_as(C.c_void_p), bt.shape[0], bt.shape[1], block_size,
+                                   si.ctypes.data_as(C.c_void_p), ps.ctypes.data_as(C.c_void_p), ps.shape[0],
+                                   out.ctypes.data_as(C.c_void_p))
+    _check(st, "pa_slot_mapping")
+    return out
 
 
 class BlockPool:

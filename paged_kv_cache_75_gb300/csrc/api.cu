@@ -53,6 +53,11 @@ int device_sm_count() {
     return query(&dev) ? g_sms[dev] : 0;
 }
 
+int current_device() {
+    int dev;
+    return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
 int device_max_smem_optin() {
     int dev;
     return query(&dev) ? g_smem[dev] : 0;

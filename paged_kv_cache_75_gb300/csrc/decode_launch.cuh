@@ -24,12 +24,9 @@ pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     const int smem = static_cast<int>(L.total) + 1024;  // slack for the 1 KB base alignment
     if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
     auto kern = paged_decode_kernel<QDT, KVDT, D, G>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return PA_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, smem) != cudaSuccess ||
-        per_sm <= 0)
-        return PA_ERR_CUDA;
+    static LaunchCache cache;
+    const int per_sm = blocks_per_sm(kern, C::THREADS, smem, cache);
+    if (per_sm <= 0) return PA_ERR_CUDA;
     const int sms = device_sm_count();
     const int64_t max_items = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.max_parts;
     const int64_t cap = static_cast<int64_t>(sms) * per_sm;

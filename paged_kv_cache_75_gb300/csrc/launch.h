@@ -2,6 +2,9 @@
 // queries.  Host code only.
 #pragma once
 
+#include <cuda_runtime.h>
+
+#include <atomic>
 #include <cstdint>
 
 #include "pa_kv.h"
@@ -20,5 +23,37 @@ int device_sm_count();
 
 // Largest dynamic shared memory a block may opt into on the current device.
 int device_max_smem_optin();
+
+// Current device ordinal, -1 on failure.
+int current_device();
+
+// Per-kernel launch facts cached across calls, so that a launch costs no
+// attribute or occupancy query after the first one: the dynamic-smem opt-in
+// is raised once per device, and the last (device, smem) -> blocks-per-SM
+// answer is remembered.
+struct LaunchCache {
+    std::atomic<uint64_t> optin_devices{0};  // bit d: attribute set on device d
+    std::atomic<uint64_t> occ{0};            // device << 48 | smem << 16 | blocks
+};
+
+template <typename Kernel>
+int blocks_per_sm(Kernel kern, int threads, int smem, LaunchCache& c) {
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64 || smem < 0 || smem >= (1 << 24)) return 0;
+    const uint64_t bit = 1ull << dev;
+    if (!(c.optin_devices.load(std::memory_order_relaxed) & bit)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 device_max_smem_optin()) != cudaSuccess)
+            return 0;
+        c.optin_devices.fetch_or(bit);
+    }
+    const uint64_t key = (static_cast<uint64_t>(dev) << 48) | (static_cast<uint64_t>(smem) << 16);
+    const uint64_t v = c.occ.load(std::memory_order_relaxed);
+    if ((v & ~0xffffull) == key && (v & 0xffffull) != 0) return static_cast<int>(v & 0xffffull);
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) return 0;
+    c.occ.store(key | static_cast<uint64_t>(n & 0xffff), std::memory_order_relaxed);
+    return n;
+}
 
 }  // namespace pa

@@ -182,6 +182,24 @@ int32_t pa_pool_ref_count(void* pool, int64_t block) {
     return p->ref[block];
 }
 
+pa_status pa_slot_mapping(const int32_t* block_table, int32_t num_seqs, int32_t max_blocks,
+                          int32_t block_size, const int32_t* seq_idx, const int64_t* pos, int64_t n,
+                          int64_t* slots_out) {
+    if (n < 0 || num_seqs < 0 || max_blocks < 0 || block_size <= 0 ||
+        (n > 0 && (block_table == nullptr || seq_idx == nullptr || pos == nullptr || slots_out == nullptr)))
+        return PA_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        const int32_t b = seq_idx[i];
+        if (b < 0 || b >= num_seqs || pos[i] < 0) return PA_ERR_INVALID_ARG;
+        const int64_t logical = pos[i] / block_size;
+        const int32_t phys = logical < max_blocks
+                                 ? block_table[static_cast<int64_t>(b) * max_blocks + logical]
+                                 : -1;
+        slots_out[i] = phys < 0 ? -1 : static_cast<int64_t>(phys) * block_size + pos[i] % block_size;
+    }
+    return PA_OK;
+}
+
 int32_t pa_pool_seq_len(void* pool, int64_t seq_id) {
     Pool* p = as_pool(pool);
     if (p == nullptr) return -1;

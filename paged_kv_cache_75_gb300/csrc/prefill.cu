@@ -435,13 +435,10 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
 
     const int smem = kQBytes + 4 * kTileBytes + (num_seqs + 1) * 4;
     if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
+    static LaunchCache cache_bf16, cache_f16;
     auto kern = q_dtype == PA_BF16 ? paged_prefill_mma_kernel<PA_BF16> : paged_prefill_mma_kernel<PA_F16>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return PA_ERR_CUDA;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess ||
-        per_sm <= 0)
-        return PA_ERR_CUDA;
+    const int per_sm = blocks_per_sm(kern, kThreads, smem, q_dtype == PA_BF16 ? cache_bf16 : cache_f16);
+    if (per_sm <= 0) return PA_ERR_CUDA;
     const int64_t max_items = static_cast<int64_t>(num_seqs) * ((max_seqlen_q + kBM - 1) / kBM) * num_heads;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);

@@ -21,22 +21,28 @@ def _lib():
     pkg_build.build()
 
 
-@pytest.mark.parametrize("bs", [16, 32])
-def test_bench_slots_match_oracle(bs):
+@pytest.mark.parametrize("bs", [4, 16, 32])
+def test_slot_mapping_helper_matches_oracle(bs):
+    import paged_kv_cache_75_gb300 as pk
     rng = np.random.default_rng(bs)
     lens = rng.integers(1, 300, size=40)
     lens[:4] = [1, bs, bs + 1, 2 * bs]
     nb = sum(W.pages_for(x, bs) for x in lens) + 17
     bt = W.assign_blocks(rng, lens, bs, nb)
-    got = bench.DecodeStep._slots_from_pool(bt, lens, bs, nb)
-    exp = oracle.slot_mapping(bt, bs, np.arange(len(lens)), lens - 1)
+    seq = rng.integers(0, 40, size=500).astype(np.int32)
+    pos = rng.integers(0, 300 + 2 * bs, size=500)
+    got = pk.pa_slot_mapping(bt, bs, seq, pos)
+    exp = oracle.slot_mapping(bt, bs, seq, pos)
     assert np.array_equal(got, exp)
+    with pytest.raises(pk.PaError):
+        pk.pa_slot_mapping(bt, bs, np.array([40], np.int32), np.array([0]))
 
 
-def test_p2_tiny_workload_slots():
+def test_p2_example_slots_through_the_helper():
+    import paged_kv_cache_75_gb300 as pk
     case, _ = bench.build_workload("tiny", "cpu")
-    lens = case.seq_lens.numpy()
-    got = bench.DecodeStep._slots_from_pool(case.block_table.numpy(), lens, 32, 8)
+    got = pk.pa_slot_mapping(case.block_table.numpy(), 32, np.arange(3, dtype=np.int32),
+                             case.seq_lens.numpy().astype(np.int64) - 1)
     assert list(got) == [94, 32, 198]
 
 
