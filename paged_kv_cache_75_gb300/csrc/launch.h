@@ -42,8 +42,12 @@ int blocks_per_sm(Kernel kern, int threads, int smem, LaunchCache& c) {
     if (dev < 0 || dev >= 64 || smem < 0 || smem >= (1 << 24)) return 0;
     const uint64_t bit = 1ull << dev;
     if (!(c.optin_devices.load(std::memory_order_relaxed) & bit)) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 device_max_smem_optin()) != cudaSuccess)
+        // opt in to everything the block may use next to its static smem
+        cudaFuncAttributes attr;
+        if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return 0;
+        const int room = device_max_smem_optin() - static_cast<int>(attr.sharedSizeBytes);
+        if (room < smem ||
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, room) != cudaSuccess)
             return 0;
         c.optin_devices.fetch_or(bit);
     }
