@@ -165,6 +165,36 @@ pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cach
                     size_t workspace_bytes, int32_t* dev_status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * pa_decode for callers that cannot allocate device memory.  (The pages have
+ * no counterpart: this is a property of the library, not of the method.)
+ *
+ * Some callers cannot call cudaMalloc: a plugin or embedded runtime whose host
+ * program owns all device memory through its own allocator, or a serving loop
+ * that must not call cudaMalloc/cudaFree because they can synchronise the
+ * device.  This call takes the same arguments as pa_decode minus the
+ * workspace: the split-K partial results go to a scratch array of
+ * PA_DECODE_STATIC_WS_BYTES that is built into the library and held by every
+ * GPU that loads it until the process exits.  It allocates nothing.
+ *   - A call whose pa_decode_workspace_size(...) exceeds
+ *     PA_DECODE_STATIC_WS_BYTES returns PA_ERR_UNSUPPORTED and launches
+ *     nothing (use pa_decode with a workspace of your own instead).
+ *   - The first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress, with that device current) and remembers it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array and finds the previous
+ *     call's data in it; nothing needs clearing, but calls whose kernels
+ *     overlap on the GPU (e.g. on two unordered streams) race and give wrong
+ *     results.  Order them on one stream.
+ * ------------------------------------------------------------------------- */
+#define PA_DECODE_STATIC_WS_BYTES (16u * 1024u * 1024u)
+
+pa_status pa_decode_static_ws(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                              const int32_t* block_table, int32_t max_blocks_per_seq,
+                              const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                              int32_t num_heads, float scale, int32_t partition_size,
+                              int32_t* dev_status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Varlen prefill (and mixed prefill + decode) attention over the paged cache.
  * "Paged 어텐션" Varlen 경로 (cu_seq_lens_q/k index a batch of sequences of
  * different lengths; max_seqlen_q/k bound them); keys and values are read

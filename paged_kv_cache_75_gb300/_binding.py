@@ -56,6 +56,8 @@ def library():
             "pa_pool_ref_count": ([vp, i64], i32),
             "pa_pool_seq_len": ([vp, i64], i32),
             "pa_slot_mapping": ([vp, i32, i32, i32, vp, vp, i64, vp], C.c_int),
+            "pa_decode_static_ws": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, vp],
+                                    C.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -195,6 +197,24 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: t
                              block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), H, float(scale),
                              int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(q))
     _check(st, "pa_decode")
+
+
+def pa_decode_static_ws(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, max_seq_len: int, scale: float, partition_size: int = 0,
+                        dev_status: Optional[torch.Tensor] = None):
+    """pa_decode without a workspace argument: the library's built-in scratch
+    (for callers that cannot allocate device memory; see include/pa_kv.h)."""
+    _need(q, "q")
+    _need(out, "out", q.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, H, D = q.shape
+    cs = cache.c_struct()
+    st = library().pa_decode_static_ws(_ptr(out), _ptr(q), torch_dtype_code(q.dtype), C.byref(cs),
+                                       _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+                                       int(max_seq_len), H, float(scale), int(partition_size),
+                                       _ptr(dev_status), _stream(q))
+    _check(st, "pa_decode_static_ws")
 
 
 def pa_prefill_varlen(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,
