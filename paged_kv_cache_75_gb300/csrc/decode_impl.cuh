@@ -185,6 +185,43 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// chunk of B bytes (16, 8 or 4) from shared memory into 32-bit words
+template <int B>
+__device__ __forceinline__ void load_chunk(const uint8_t* src, uint32_t (&w)[4]) {
+    if constexpr (B == 16) {
+        const uint4 x = *reinterpret_cast<const uint4*>(src);
+        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    } else if constexpr (B == 8) {
+        const uint2 x = *reinterpret_cast<const uint2*>(src);
+        w[0] = x.x; w[1] = x.y; w[2] = 0u; w[3] = 0u;
+    } else {
+        w[0] = *reinterpret_cast<const uint32_t*>(src); w[1] = w[2] = w[3] = 0u;
+    }
+}
+
+// a0 += q.lo * k.lo, a1 += q.hi * k.hi on packed 16-bit pairs; the products
+// of two 16-bit floats are exact in fp32, so this equals fp32 FMAs on the
+// widened values (one rounding per FMA)
+template <int DT>
+__device__ __forceinline__ void fma_mixed2(float& a0, float& a1, uint32_t q, uint32_t k) {
+    if constexpr (DT == PA_BF16) {
+        asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\tmov.b32 {ql, qh}, %2;\n\tmov.b32 {kl, kh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, ql, kl, %0;\n\tfma.rn.f32.bf16 %1, qh, kh, %1;\n\t}"
+            : "+f"(a0), "+f"(a1) : "r"(q), "r"(k));
+    } else {
+        asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\tmov.b32 {ql, qh}, %2;\n\tmov.b32 {kl, kh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, ql, kl, %0;\n\tfma.rn.f32.f16 %1, qh, kh, %1;\n\t}"
+            : "+f"(a0), "+f"(a1) : "r"(q), "r"(k));
+    }
+}
+
+// (a0, a1) += p * (v0, v1) as one packed fp32 FMA
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float p, float v0, float v1) {
+    asm("{\n\t.reg .b64 a, pp, vv;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 pp, {%2, %2};\n\t"
+        "mov.b64 vv, {%3, %4};\n\tfma.rn.f32x2 a, pp, vv, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1) : "f"(p), "f"(v0), "f"(v1));
+}
+
 template <int QDT, int KVDT, int D, int G>
 __global__ void __launch_bounds__(DecodeCfg<QDT, KVDT, D, G>::THREADS)
 paged_decode_kernel(const DecodeParams p) {
@@ -224,6 +261,8 @@ paged_decode_kernel(const DecodeParams p) {
         // ------------------------------ producer ------------------------------
         const uint64_t policy = policy_evict_first();
         uint32_t fill = 0;    // ring slots used so far by this CTA
+        uint32_t stage = 0;   // fill % S
+        uint32_t phase = 0;   // (fill / S) & 1
         uint32_t issued = 0;  // fills that started copies (all but bad pages)
         uint32_t qn = 0;      // items issued so far
         bool ok = true;
@@ -242,48 +281,52 @@ paged_decode_kernel(const DecodeParams p) {
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             const int32_t* row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
+            const int64_t head_off = static_cast<int64_t>(it.kvh) * page_bytes;
+            const int64_t blk_stride = static_cast<int64_t>(p.num_kv_heads) * page_bytes;
             for (int jb = it.j0; jb < it.j1 && ok; jb += 32) {
                 const int j = jb + lane;
-                int32_t id = j < it.j1 ? __ldg(row + j) : 0;
+                const int32_t id = j < it.j1 ? __ldg(row + j) : 0;
                 const int cnt = min(32, it.j1 - jb);
                 for (int k = 0; k < cnt; ++k) {
                     const int32_t idk = __shfl_sync(0xffffffffu, id, k);
                     if (lane == 0) {
-                        const uint32_t s = fill % S;
                         if (fill >= static_cast<uint32_t>(S))
-                            ok = mbar_wait(empty0 + 8u * s, ((fill / S) - 1) & 1u, p.status, abort_flag);
+                            ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status, abort_flag);
                         if (ok) {
                             const bool good = idk >= 0 && idk < p.num_blocks;
-                            page_ok[s] = good ? 1 : 0;
+                            page_ok[stage] = good ? 1 : 0;
+                            const uint32_t bar = full0 + 8u * stage;
                             if (good) {
-                                const int64_t off = (static_cast<int64_t>(idk) * p.num_kv_heads + it.kvh) *
-                                                    static_cast<int64_t>(page_bytes);
-                                const uint32_t dst = smem_addr(ring) + s * 2u * page_bytes;
-                                mbar_expect_tx(full0 + 8u * s, 2u * page_bytes);
-                                bulk_g2s_hint(dst, p.k_cache + off, page_bytes, full0 + 8u * s, policy);
-                                bulk_g2s_hint(dst + page_bytes, p.v_cache + off, page_bytes, full0 + 8u * s,
-                                              policy);
+                                const int64_t off = idk * blk_stride + head_off;
+                                const uint32_t dst = smem_addr(ring) + stage * 2u * page_bytes;
+                                mbar_expect_tx(bar, 2u * page_bytes);
+                                bulk_g2s_hint(dst, p.k_cache + off, page_bytes, bar, policy);
+                                bulk_g2s_hint(dst + page_bytes, p.v_cache + off, page_bytes, bar, policy);
                                 issued = fill + 1;
                             } else {
                                 report(p.status, PA_ERR_BAD_BLOCK);
-                                mbar_arrive(full0 + 8u * s);
+                                mbar_arrive(bar);
                             }
                         }
                     }
                     ++fill;
+                    if (++stage == static_cast<uint32_t>(S)) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                 }
             }
         }
-        // do not leave while copies may still land: wait for every stage that
-        // was filled but (after an abort) possibly not consumed
+        // do not leave while copies may still land: after an abort, wait
+        // (bounded) for every stage that was filled but maybe not consumed
         if (lane == 0 && *abort_flag) {
             const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
             const uint64_t t0 = global_timer_ns();
             for (uint32_t f = first; f < issued; ++f) {
-                const uint32_t s = f % S;
-                while (!mbar_try_wait(full0 + 8u * s, (f / S) & 1u)) {
+                const uint32_t st = f % S;
+                while (!mbar_try_wait(full0 + 8u * st, (f / S) & 1u)) {
                     if (global_timer_ns() - t0 > kWaitLimitNs) break;
                 }
             }
@@ -292,30 +335,42 @@ paged_decode_kernel(const DecodeParams p) {
     }
 
     // ------------------------------- consumers ------------------------------
-    const int tg = lane / C::LPT;  // token slot of this lane in a warp step
-    const int c = lane % C::LPT;   // lane's chunk of the key row
-    uint32_t fill = 0;
+    // A warp is TG token groups of LPT lanes.  In every step of TPI tokens of a
+    // page, group tg takes token st + warp*TG + tg; lane c of the group owns
+    // the row chunks {v*LPT + c} (VB bytes each) of that token's key row (its
+    // share of the dot product) and of its value row (its share of the
+    // output).  Each group keeps its own online-softmax state, so a step needs
+    // no exchange between groups; groups and warps are merged once per item.
+    const int tg = lane / C::LPT, c = lane % C::LPT;
+    constexpr int EV = C::VB / C::KB;          // elements per row chunk
+    constexpr bool kMixed = C::KB == 2;        // 16-bit KV: mixed-precision FMA on packed pairs
+    constexpr float kTau = 8.f;                // lazy-rescale threshold (log2 units)
+    uint32_t stage = 0, phase = 0;             // ring position
     uint32_t qn = 0;
     for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++qn) {
         const Item it = decode_item(p, prefix, i);
         const uint32_t slot = qn & 1u;
         bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8u * slot, (qn >> 1) & 1u, p.status, abort_flag));
-        // queries of this KV head's group, permuted like the key chunks
-        float qf[G][C::EPL];
+        // queries of this KV head's group, in the lane's chunk order
+        uint32_t qw[G][kMixed ? C::EPL / 2 : 1];  // packed pairs (16-bit KV)
+        float qf[G][kMixed ? 1 : C::EPL];         // floats (E4M3 KV)
         {
             const uint8_t* qs = qbuf + slot * ((C::QBYTES + 127) & ~127);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
 #pragma unroll
                 for (int v = 0; v < C::NV; ++v) {
-                    const int e0 = (v * C::LPT + c) * C::VB / C::KB;  // first element of vector
-                    constexpr int EV = C::VB / C::KB;                 // elements per vector
+                    const int e0 = (v * C::LPT + c) * EV;
 #pragma unroll
                     for (int e = 0; e < EV; e += 2) {
                         const uint32_t w = *reinterpret_cast<const uint32_t*>(qs + (g * D + e0 + e) * C::QB);
-                        const float2 f = kv_pair<QDT>(w);
-                        qf[g][v * EV + e] = f.x * p.qk_scale;
-                        qf[g][v * EV + e + 1] = f.y * p.qk_scale;
+                        if constexpr (kMixed) {
+                            qw[g][(v * EV + e) / 2] = w;
+                        } else {
+                            const float2 f = kv_pair<QDT>(w);
+                            qf[g][v * EV + e] = f.x;
+                            qf[g][v * EV + e + 1] = f.y;
+                        }
                     }
                 }
             }
@@ -323,150 +378,145 @@ paged_decode_kernel(const DecodeParams p) {
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty0 + 8u * slot);
 
-        float m[G], l[G], acc[G][C::DL];
+        float m[G], l[G], acc[G][C::EPL];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             m[g] = -INFINITY;
             l[g] = 0.f;
 #pragma unroll
-            for (int d = 0; d < C::DL; ++d) acc[g][d] = 0.f;
+            for (int e = 0; e < C::EPL; ++e) acc[g][e] = 0.f;
         }
 
-        for (int j = it.j0; j < it.j1 && ok; ++j, ++fill) {
-            const uint32_t s = fill % S;
-            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8u * s, (fill / S) & 1u, p.status, abort_flag))) {
+        for (int j = it.j0; j < it.j1 && ok; ++j) {
+            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8u * stage, phase, p.status, abort_flag))) {
                 ok = false;
                 break;
             }
-            const bool page_good = page_ok[s] != 0;
-            const uint8_t* Kp = ring + s * 2u * page_bytes;
+            const bool page_good = page_ok[stage] != 0;
+            const uint8_t* Kp = ring + stage * 2u * page_bytes;
             const uint8_t* Vp = Kp + page_bytes;
             for (int st = 0; st < p.block_size; st += C::TPI) {
                 const int tok = st + warp * C::TG + tg;
-                const int pos = j * p.block_size + tok;
-                const bool valid = page_good && pos < it.t1;
-                // ---- QK: partial dot over this lane's chunk, then reduce ----
+                const bool valid = page_good && j * p.block_size + tok < it.t1;
+                const uint8_t* krow = Kp + tok * C::ROWB + c * C::VB;
+                const uint8_t* vrow = Vp + tok * C::ROWB + c * C::VB;
+                // ---- QK: this lane's chunks, then a butterfly over the group ----
                 float sc[G];
+                {
+                    float s0[G], s1[G];
 #pragma unroll
-                for (int g = 0; g < G; ++g) sc[g] = 0.f;
-                const uint8_t* krow = Kp + tok * C::ROWB;
+                    for (int g = 0; g < G; ++g) s0[g] = s1[g] = 0.f;
 #pragma unroll
-                for (int v = 0; v < C::NV; ++v) {
-                    const uint8_t* src = krow + (v * C::LPT + c) * C::VB;
-                    uint32_t w[4];
-                    if constexpr (C::VB == 16) {
-                        const uint4 x = *reinterpret_cast<const uint4*>(src);
-                        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-                    } else if constexpr (C::VB == 8) {
-                        const uint2 x = *reinterpret_cast<const uint2*>(src);
-                        w[0] = x.x; w[1] = x.y; w[2] = 0; w[3] = 0;
-                    } else {
-                        w[0] = *reinterpret_cast<const uint32_t*>(src); w[1] = w[2] = w[3] = 0;
-                    }
-                    constexpr int NW = C::VB / 4;  // 32-bit words per vector
-                    constexpr int EV = C::VB / C::KB;
+                    for (int v = 0; v < C::NV; ++v) {
+                        uint32_t w[4];
+                        load_chunk<C::VB>(krow + v * C::LPT * C::VB, w);
+                        constexpr int NW = C::VB / 4;
 #pragma unroll
-                    for (int x = 0; x < NW; ++x) {
-                        if constexpr (C::KB == 2) {
-                            const float2 f = kv_pair<KVDT>(w[x]);
+                        for (int x = 0; x < NW; ++x) {
+                            if constexpr (kMixed) {
 #pragma unroll
-                            for (int g = 0; g < G; ++g) {
-                                sc[g] = fmaf(qf[g][v * EV + 2 * x], f.x, sc[g]);
-                                sc[g] = fmaf(qf[g][v * EV + 2 * x + 1], f.y, sc[g]);
+                                for (int g = 0; g < G; ++g) fma_mixed2<KVDT>(s0[g], s1[g], qw[g][(v * EV) / 2 + x], w[x]);
+                            } else {
+                                const float2 f0 = e4m3x2_to_f2(w[x]);
+                                const float2 f1 = e4m3x2_to_f2(w[x] >> 16);
+                                const int e = v * EV + 4 * x;
+#pragma unroll
+                                for (int g = 0; g < G; ++g) {
+                                    s0[g] = fmaf(qf[g][e], f0.x, s0[g]);
+                                    s1[g] = fmaf(qf[g][e + 1], f0.y, s1[g]);
+                                    s0[g] = fmaf(qf[g][e + 2], f1.x, s0[g]);
+                                    s1[g] = fmaf(qf[g][e + 3], f1.y, s1[g]);
+                                }
                             }
-                        } else {
-                            const float2 f0 = e4m3x2_to_f2(w[x]);
-                            const float2 f1 = e4m3x2_to_f2(w[x] >> 16);
-#pragma unroll
-                            for (int g = 0; g < G; ++g) {
-                                sc[g] = fmaf(qf[g][v * EV + 4 * x], f0.x, sc[g]);
-                                sc[g] = fmaf(qf[g][v * EV + 4 * x + 1], f0.y, sc[g]);
-                                sc[g] = fmaf(qf[g][v * EV + 4 * x + 2], f1.x, sc[g]);
-                                sc[g] = fmaf(qf[g][v * EV + 4 * x + 3], f1.y, sc[g]);
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-#pragma unroll
-                    for (int o = 1; o < C::LPT; o <<= 1) sc[g] += __shfl_xor_sync(0xffffffffu, sc[g], o);
-                    if (!valid) sc[g] = -INFINITY;
-                }
-                // ---- online softmax (per warp, exp2 domain) ----
-                float pr[G];
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float tmax = sc[g];
-#pragma unroll
-                    for (int o = C::LPT; o < 32; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-                    const float mnew = fmaxf(m[g], tmax);
-                    if (mnew == -INFINITY) {
-                        pr[g] = 0.f;
-                    } else {
-                        if (mnew > m[g]) {
-                            const float alpha = fast_exp2(m[g] - mnew);
-                            l[g] *= alpha;
-#pragma unroll
-                            for (int d = 0; d < C::DL; ++d) acc[g][d] *= alpha;
-                            m[g] = mnew;
-                        }
-                        pr[g] = fast_exp2(sc[g] - mnew);
-                    }
-                    l[g] += pr[g];
-                }
-                // ---- PV: every lane owns DL consecutive value columns ----
-                // (masked rows are skipped, not multiplied by 0: they may hold NaN)
-                const int tok0 = j * p.block_size + st + warp * C::TG;
-#pragma unroll
-                for (int tt = 0; tt < C::TG; ++tt) {
-                    if (!page_good || tok0 + tt >= it.t1) continue;  // warp-uniform
-                    const uint8_t* vrow = Vp + (st + warp * C::TG + tt) * C::ROWB + lane * C::DL * C::KB;
-                    float vf[C::DL];
-                    if constexpr (C::KB == 2) {
-                        if constexpr (C::DL == 4) {
-                            const uint2 x = *reinterpret_cast<const uint2*>(vrow);
-                            const float2 a = kv_pair<KVDT>(x.x), b2 = kv_pair<KVDT>(x.y);
-                            vf[0] = a.x; vf[1] = a.y; vf[2] = b2.x; vf[3] = b2.y;
-                        } else {
-                            const float2 a = kv_pair<KVDT>(*reinterpret_cast<const uint32_t*>(vrow));
-                            vf[0] = a.x; vf[1] = a.y;
-                        }
-                    } else {
-                        if constexpr (C::DL == 4) {
-                            const uint32_t x = *reinterpret_cast<const uint32_t*>(vrow);
-                            const float2 a = e4m3x2_to_f2(x), b2 = e4m3x2_to_f2(x >> 16);
-                            vf[0] = a.x; vf[1] = a.y; vf[2] = b2.x; vf[3] = b2.y;
-                        } else {
-                            const float2 a = e4m3x2_to_f2(*reinterpret_cast<const uint16_t*>(vrow));
-                            vf[0] = a.x; vf[1] = a.y;
                         }
                     }
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        const float pg = __shfl_sync(0xffffffffu, pr[g], tt * C::LPT);
+                        float t = s0[g] + s1[g];
 #pragma unroll
-                        for (int d = 0; d < C::DL; ++d) acc[g][d] = fmaf(pg, vf[d], acc[g][d]);
+                        for (int o = 1; o < C::LPT; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                        sc[g] = valid ? t * p.qk_scale : -INFINITY;
+                    }
+                }
+                // ---- online softmax of this group (lazy rescale) ----
+                float pr[G];
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (sc[g] > m[g] + kTau) {
+                        const float a = fast_exp2(m[g] - sc[g]);  // 0 when m = -inf
+                        l[g] *= a;
+#pragma unroll
+                        for (int e = 0; e < C::EPL; ++e) acc[g][e] *= a;
+                        m[g] = sc[g];
+                    }
+                    pr[g] = valid ? fast_exp2(sc[g] - m[g]) : 0.f;
+                    l[g] += pr[g];
+                }
+                // ---- PV over this lane's value chunks (masked rows are not read) ----
+                if (valid) {
+#pragma unroll
+                    for (int v = 0; v < C::NV; ++v) {
+                        uint32_t w[4];
+                        load_chunk<C::VB>(vrow + v * C::LPT * C::VB, w);
+                        constexpr int NW = C::VB / 4;
+#pragma unroll
+                        for (int x = 0; x < NW; ++x) {
+                            if constexpr (kMixed) {
+                                const float2 f = kv_pair<KVDT>(w[x]);
+                                const int e = v * EV + 2 * x;
+#pragma unroll
+                                for (int g = 0; g < G; ++g) ffma2(acc[g][e], acc[g][e + 1], pr[g], f.x, f.y);
+                            } else {
+                                const float2 f0 = e4m3x2_to_f2(w[x]);
+                                const float2 f1 = e4m3x2_to_f2(w[x] >> 16);
+                                const int e = v * EV + 4 * x;
+#pragma unroll
+                                for (int g = 0; g < G; ++g) {
+                                    ffma2(acc[g][e], acc[g][e + 1], pr[g], f0.x, f0.y);
+                                    ffma2(acc[g][e + 2], acc[g][e + 3], pr[g], f1.x, f1.y);
+                                }
+                            }
+                        }
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(empty0 + 8u * s);
+            if (lane == 0) mbar_arrive(empty0 + 8u * stage);
+            if (++stage == static_cast<uint32_t>(S)) {
+                stage = 0;
+                phase ^= 1u;
+            }
         }
 
-        // ---- merge the four warps' partial softmax states ----
+        // ---- merge the token groups of this warp, then the warps ----
         {
             float* mw = merge + warp * G * (D + 2);
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                float lw = l[g];
+                float M = m[g];
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+                for (int o = C::LPT; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                const float f = M == -INFINITY ? 0.f : fast_exp2(m[g] - M);
+                float lw = l[g] * f;
 #pragma unroll
-                for (int d = 0; d < C::DL; ++d) mw[g * (D + 2) + lane * C::DL + d] = acc[g][d];
+                for (int o = C::LPT; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+#pragma unroll
+                for (int e = 0; e < C::EPL; ++e) {
+                    float a = acc[g][e] * f;
+#pragma unroll
+                    for (int o = C::LPT; o < 32; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                    acc[g][e] = a;
+                }
+                if (tg == 0) {
+#pragma unroll
+                    for (int v = 0; v < C::NV; ++v)
+#pragma unroll
+                        for (int e = 0; e < EV; ++e)
+                            mw[g * (D + 2) + (v * C::LPT + c) * EV + e] = acc[g][v * EV + e];
+                }
                 if (lane == 0) {
-                    mw[g * (D + 2) + D] = m[g];
-                    mw[g * (D + 2) + D + 1] = lw * (1.f / C::LPT);  // each token counted LPT times
+                    mw[g * (D + 2) + D] = M;
+                    mw[g * (D + 2) + D + 1] = lw;
                 }
             }
         }
