@@ -228,9 +228,12 @@ def build_workload(name, device, num_seqs=None, pool_blocks=None):
         tag = "mha_decode_%dseq_32h_d128_bs16_fp16_len_u1_2048_pool%d" % (B, nb)
         return W.mha_decode(device=device, B=B, num_blocks=nb), tag
     if name == "gqa":
-        return W.gqa_shared_decode(device=device), "gqa_decode_256seq_32q8kv_d128_bs16_bf16_lognormal1000_shared4"
+        groups = (num_seqs or 256) // 4
+        return (W.gqa_shared_decode(device=device, groups=groups),
+                "gqa_decode_%dseq_32q8kv_d128_bs16_bf16_lognormal1000_shared4" % (4 * groups))
     if name == "long":
-        return W.long_fp8_decode(device=device), "long_decode_8seq_64q8kv_d128_bs32_e4m3_len_u32k_128k_p512"
+        B = num_seqs or 8
+        return W.long_fp8_decode(device=device, B=B), "long_decode_%dseq_64q8kv_d128_bs32_e4m3_len_u32k_128k_p512" % B
     if name == "tiny":
         case = W.tiny_decode(device=device)
         case.seq_lens = torch.tensor([31, 33, 71], dtype=torch.int32, device=device)
@@ -442,7 +445,7 @@ def main():
     ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny"], default="mha")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--num-seqs", type=int, default=None, help="mha workload: sequences (smaller profiling case)")
+    ap.add_argument("--num-seqs", type=int, default=None, help="sequences (smaller profiling cases)")
     ap.add_argument("--pool-blocks", type=int, default=None, help="mha workload: physical blocks in the pool")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -109,7 +109,12 @@ extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const
     p.qk_scale = scale * k_scale * 1.4426950408889634f;
     p.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (cache->kv_dtype == PA_F16) return launch_decode_f16(p, D, group, s);
-    if (cache->kv_dtype == PA_BF16) return launch_decode_bf16(p, D, group, s);
-    return q_dtype == PA_F16 ? launch_decode_fp8_qf16(p, D, group, s) : launch_decode_fp8_qbf16(p, D, group, s);
+#define PA_BS(KV)                                                       \
+    if (bs == 16) return launch_decode_##KV##_bs16(p, q_dtype, D, group, s); \
+    if (bs == 32) return launch_decode_##KV##_bs32(p, q_dtype, D, group, s); \
+    return launch_decode_##KV##_bs64(p, q_dtype, D, group, s);
+    if (cache->kv_dtype == PA_F16) { PA_BS(f16) }
+    if (cache->kv_dtype == PA_BF16) { PA_BS(bf16) }
+    PA_BS(fp8)
+#undef PA_BS
 }

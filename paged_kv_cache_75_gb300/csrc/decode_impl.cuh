@@ -18,12 +18,14 @@
 //    without a max_num_partitions-shaped grid;
 //  * one producer warp streams each (block, KV head) page -- one contiguous
 //    block_size*head_size run in the [blocks][kv_heads][block_size][head]
-//    layout -- into a ring of shared-memory stages with 1-D bulk async copies
-//    (cp.async.bulk), completion counted on mbarriers;
-//  * four consumer warps split each page's tokens; all G query heads of a KV
+//    layout -- into a ring of shared-memory stages (32 tokens of K and V per
+//    stage) with 1-D bulk async copies (cp.async.bulk), completion counted on
+//    mbarriers;
+//  * four consumer warps split each stage's tokens; all G query heads of a KV
 //    head are handled together, so a page is read once per KV head (GQA);
-//  * per-warp online softmax in fp32 (exp2 domain), warp-shuffle QK
-//    reductions, and one cross-warp merge per work item;
+//  * each 8-lane token group keeps its own online softmax in fp32 (exp2
+//    domain, lazy rescale), QK with warp-shuffle reductions, and groups and
+//    warps are merged once per work item;
 //  * every mbarrier wait is bounded (PA_ERR_TIMEOUT, no hang).
 #pragma once
 
@@ -55,34 +57,47 @@ struct DecodeParams {
     float v_scale;
 };
 
-template <int QDT, int KVDT, int D, int G>
+template <int QDT, int KVDT, int D, int G, int BS>
 struct DecodeCfg {
-    static constexpr int NCW = 4;                     // consumer warps
+    static constexpr int GW = G < 4 ? G : 4;          // query heads per consumer warp
+    static constexpr int HG = G / GW;                 // head groups (warp sets)
+    static constexpr int TW = 4 / HG;                 // token warps per head group
+    static constexpr int NCW = TW * HG;               // consumer warps (4)
     static constexpr int THREADS = (NCW + 1) * 32;    // + one producer warp
-    static constexpr int TG = (G >= 8) ? 2 : 4;       // tokens per warp step
-    static constexpr int LPT = 32 / TG;               // lanes per token (QK)
-    static constexpr int EPL = D / LPT;               // key elements per lane
+    static constexpr int LPT = 8;                     // lanes per token
+    static constexpr int TG = 32 / LPT;               // tokens per warp step
+    static constexpr int EPL = D / LPT;               // row elements per lane
     static constexpr int KB = dtype_traits<KVDT>::bytes;
     static constexpr int QB = dtype_traits<QDT>::bytes;
-    static constexpr int TPI = NCW * TG;              // tokens per block step
-    static constexpr int DL = D / 32;                 // value elements per lane
-    static constexpr int VB = (EPL * KB < 16) ? EPL * KB : 16;  // K vector bytes
-    static constexpr int NV = EPL * KB / VB;          // K vectors per lane
+    static constexpr int TPI = TW * TG;               // tokens per block step
+    static constexpr int VB = (EPL * KB < 16) ? EPL * KB : 16;  // row chunk bytes
+    static constexpr int NV = EPL * KB / VB;          // row chunks per lane
+    static constexpr int EV = VB / KB;                // elements per chunk
+    static constexpr int PL = EPL / 2;                // element pairs per lane
     static constexpr int ROWB = D * KB;               // bytes per token row
+    static constexpr int PAGE = BS * ROWB;            // bytes of one (block, KV head) page
+    static constexpr int SPAGES = BS >= 32 ? 1 : 32 / BS;  // pages per ring stage
+    static constexpr int STOK = SPAGES * BS;          // tokens per ring stage
+    static constexpr int SUB = STOK / TPI;            // block steps per stage
+    static constexpr int STAGE_BYTES = 2 * SPAGES * PAGE;  // K pages, then V pages
     static constexpr int QBYTES = G * D * QB;         // one item's queries
-    static constexpr int MERGE_FLOATS = NCW * G * (D + 2);
-    static_assert(D % LPT == 0 && EPL * KB >= 4, "unsupported head size / group");
+    static constexpr int MERGE_FLOATS = NCW * GW * (D + 2);
+    // register cap: two 5-warp CTAs per SM when a warp holds 4 heads, three
+    // otherwise (a block's register share is counted in pairs of warps)
+    static constexpr int MAX_REGS = GW == 4 ? 168 : 128;
+    static_assert(EPL * KB >= 4 && EPL % 4 == 0, "unsupported head size");
+    static_assert(STOK % TPI == 0, "block size must be a multiple of the step");
 };
 
 // shared memory carve-up (byte offsets from the 1 KB-aligned base)
 struct DecodeSmem {
     uint32_t ring, qbuf, merge, prefix, bars, flags, total;
-    __host__ __device__ static DecodeSmem make(int stages, int page_bytes, int qbytes,
+    __host__ __device__ static DecodeSmem make(int stages, int stage_bytes, int qbytes,
                                                int merge_floats, int num_seqs) {
         DecodeSmem s;
         uint32_t o = 0;
         s.ring = o;
-        o += static_cast<uint32_t>(stages) * 2u * page_bytes;
+        o += static_cast<uint32_t>(stages) * stage_bytes;
         s.qbuf = o;
         o += 2u * ((qbytes + 127u) & ~127u);
         s.merge = o;
@@ -199,9 +214,9 @@ __device__ __forceinline__ void load_chunk(const uint8_t* src, uint32_t (&w)[4])
     }
 }
 
-// a0 += q.lo * k.lo, a1 += q.hi * k.hi on packed 16-bit pairs; the products
-// of two 16-bit floats are exact in fp32, so this equals fp32 FMAs on the
-// widened values (one rounding per FMA)
+// a0 += q.lo * k.lo, a1 += q.hi * k.hi on packed 16-bit pairs.  A product of
+// two 16-bit floats is exact in fp32, so this equals fp32 FMAs on the
+// widened values (one rounding per FMA).
 template <int DT>
 __device__ __forceinline__ void fma_mixed2(float& a0, float& a1, uint32_t q, uint32_t k) {
     if constexpr (DT == PA_BF16) {
@@ -215,31 +230,72 @@ __device__ __forceinline__ void fma_mixed2(float& a0, float& a1, uint32_t q, uin
     }
 }
 
-// (a0, a1) += p * (v0, v1) as one packed fp32 FMA
-__device__ __forceinline__ void ffma2(float& a0, float& a1, float p, float v0, float v1) {
-    asm("{\n\t.reg .b64 a, pp, vv;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 pp, {%2, %2};\n\t"
-        "mov.b64 vv, {%3, %4};\n\tfma.rn.f32x2 a, pp, vv, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
-        : "+f"(a0), "+f"(a1) : "f"(p), "f"(v0), "f"(v1));
+// two E4M3 codes (low 16 bits of w) -> packed fp16 pair (exact)
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t w) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
 }
 
-template <int QDT, int KVDT, int D, int G>
-__global__ void __launch_bounds__(DecodeCfg<QDT, KVDT, D, G>::THREADS)
+// Packed fp32 pairs: one 64-bit register pair holds (x, y); fma/mul on both
+// halves is one instruction (fma.rn.f32x2 / mul.rn.f32x2).
+__device__ __forceinline__ uint64_t pk2(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ uint64_t pk2u(uint32_t x, uint32_t y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(x), "r"(y));
+    return r;
+}
+__device__ __forceinline__ float2 up2(uint64_t r) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// packed 16-bit pair -> fp32 pair
+template <int DT>
+__device__ __forceinline__ uint64_t pair_of(uint32_t w);
+template <>
+__device__ __forceinline__ uint64_t pair_of<PA_BF16>(uint32_t w) { return pk2u(w << 16, w & 0xffff0000u); }
+template <>
+__device__ __forceinline__ uint64_t pair_of<PA_F16>(uint32_t w) {
+    const float2 f = f16x2_to_f2(w);
+    return pk2(f.x, f.y);
+}
+
+template <int QDT, int KVDT, int D, int G, int BS>
+__global__ void __maxnreg__((DecodeCfg<QDT, KVDT, D, G, BS>::MAX_REGS))
 paged_decode_kernel(const DecodeParams p) {
-    using C = DecodeCfg<QDT, KVDT, D, G>;
+    using C = DecodeCfg<QDT, KVDT, D, G, BS>;
+    // the 16-bit type the QK products are taken in: the cache's, or fp16
+    // (exact for E4M3 codes) with power-of-two scaled queries for E4M3 caches
+    constexpr int KT = C::KB == 2 ? KVDT : PA_F16;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const int page_bytes = p.block_size * C::ROWB;
-    const DecodeSmem L = DecodeSmem::make(p.stages, page_bytes, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
+    const DecodeSmem L = DecodeSmem::make(p.stages, C::STAGE_BYTES, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
     uint8_t* ring = smem_raw + L.ring;
     uint8_t* qbuf = smem_raw + L.qbuf;
     float* merge = reinterpret_cast<float*>(smem_raw + L.merge);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem_raw + L.prefix);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + L.flags);
-    volatile int* page_ok = abort_flag + 1;
+    volatile int* stage_mask = abort_flag + 1;  // bit k: page k of the stage is present
     const int S = p.stages;
     const uint32_t full0 = smem_addr(bars), empty0 = full0 + 8u * S;
     const uint32_t qfull0 = full0 + 16u * S, qempty0 = qfull0 + 16u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr uint32_t QSLOT = (C::QBYTES + 127) & ~127;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -260,10 +316,10 @@ paged_decode_kernel(const DecodeParams p) {
     if (warp == C::NCW) {
         // ------------------------------ producer ------------------------------
         const uint64_t policy = policy_evict_first();
-        uint32_t fill = 0;    // ring slots used so far by this CTA
+        uint32_t fill = 0;    // ring stages used so far by this CTA
         uint32_t stage = 0;   // fill % S
         uint32_t phase = 0;   // (fill / S) & 1
-        uint32_t issued = 0;  // fills that started copies (all but bad pages)
+        uint32_t issued = 0;  // fills that started copies
         uint32_t qn = 0;      // items issued so far
         bool ok = true;
         for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++qn) {
@@ -275,36 +331,52 @@ paged_decode_kernel(const DecodeParams p) {
                     const uint8_t* src = static_cast<const uint8_t*>(p.q) +
                                          (static_cast<int64_t>(it.b) * p.num_heads + it.kvh * G) * D * C::QB;
                     mbar_expect_tx(qfull0 + 8u * slot, C::QBYTES);
-                    bulk_g2s(smem_addr(qbuf + slot * ((C::QBYTES + 127) & ~127)), src, C::QBYTES,
-                             qfull0 + 8u * slot);
+                    bulk_g2s(smem_addr(qbuf + slot * QSLOT), src, C::QBYTES, qfull0 + 8u * slot);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             const int32_t* row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
-            const int64_t head_off = static_cast<int64_t>(it.kvh) * page_bytes;
-            const int64_t blk_stride = static_cast<int64_t>(p.num_kv_heads) * page_bytes;
+            const int64_t head_off = static_cast<int64_t>(it.kvh) * C::PAGE;
+            const int64_t blk_stride = static_cast<int64_t>(p.num_kv_heads) * C::PAGE;
             for (int jb = it.j0; jb < it.j1 && ok; jb += 32) {
                 const int j = jb + lane;
-                const int32_t id = j < it.j1 ? __ldg(row + j) : 0;
+                const int32_t id = j < it.j1 ? __ldg(row + j) : -1;
                 const int cnt = min(32, it.j1 - jb);
-                for (int k = 0; k < cnt; ++k) {
-                    const int32_t idk = __shfl_sync(0xffffffffu, id, k);
+                for (int k0 = 0; k0 < cnt; k0 += C::SPAGES) {
+                    int32_t ids[C::SPAGES];
+#pragma unroll
+                    for (int k = 0; k < C::SPAGES; ++k) ids[k] = __shfl_sync(0xffffffffu, id, k0 + k);
                     if (lane == 0) {
                         if (fill >= static_cast<uint32_t>(S))
                             ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status, abort_flag);
                         if (ok) {
-                            const bool good = idk >= 0 && idk < p.num_blocks;
-                            page_ok[stage] = good ? 1 : 0;
                             const uint32_t bar = full0 + 8u * stage;
-                            if (good) {
-                                const int64_t off = idk * blk_stride + head_off;
-                                const uint32_t dst = smem_addr(ring) + stage * 2u * page_bytes;
-                                mbar_expect_tx(bar, 2u * page_bytes);
-                                bulk_g2s_hint(dst, p.k_cache + off, page_bytes, bar, policy);
-                                bulk_g2s_hint(dst + page_bytes, p.v_cache + off, page_bytes, bar, policy);
+                            const uint32_t dst = smem_addr(ring) + stage * C::STAGE_BYTES;
+                            int mask = 0;
+                            uint32_t bytes = 0;
+#pragma unroll
+                            for (int k = 0; k < C::SPAGES; ++k) {
+                                if (k0 + k >= cnt) continue;  // past the item's pages
+                                if (ids[k] >= 0 && ids[k] < p.num_blocks) {
+                                    mask |= 1 << k;
+                                    bytes += 2u * C::PAGE;
+                                } else {
+                                    report(p.status, PA_ERR_BAD_BLOCK);
+                                }
+                            }
+                            stage_mask[stage] = mask;
+                            if (bytes) {
+                                mbar_expect_tx(bar, bytes);
+#pragma unroll
+                                for (int k = 0; k < C::SPAGES; ++k) {
+                                    if (!(mask & (1 << k))) continue;
+                                    const int64_t off = ids[k] * blk_stride + head_off;
+                                    bulk_g2s_hint(dst + k * C::PAGE, p.k_cache + off, C::PAGE, bar, policy);
+                                    bulk_g2s_hint(dst + (C::SPAGES + k) * C::PAGE, p.v_cache + off, C::PAGE, bar,
+                                                  policy);
+                                }
                                 issued = fill + 1;
                             } else {
-                                report(p.status, PA_ERR_BAD_BLOCK);
                                 mbar_arrive(bar);
                             }
                         }
@@ -335,122 +407,157 @@ paged_decode_kernel(const DecodeParams p) {
     }
 
     // ------------------------------- consumers ------------------------------
-    // A warp is TG token groups of LPT lanes.  In every step of TPI tokens of a
-    // page, group tg takes token st + warp*TG + tg; lane c of the group owns
-    // the row chunks {v*LPT + c} (VB bytes each) of that token's key row (its
-    // share of the dot product) and of its value row (its share of the
-    // output).  Each group keeps its own online-softmax state, so a step needs
-    // no exchange between groups; groups and warps are merged once per item.
+    // Consumer warp w works for head group hg = w / TW (query heads hg*GW ..
+    // hg*GW+GW-1 of the KV head) as token warp tw = w % TW.  A warp is TG token
+    // groups of LPT lanes; in every TPI-token step of a stage, group tg takes
+    // token u*TPI + tw*TG + tg, and lane c of the group owns the row chunks
+    // {v*LPT + c} (VB bytes each) of that token's key row (its share of the
+    // dot products) and value row (its share of the outputs).  Every group
+    // keeps its own online-softmax state, so a step needs no exchange between
+    // groups; groups, then warps, are merged once per work item.
+    const int hg = warp / C::TW, tw = warp % C::TW;
     const int tg = lane / C::LPT, c = lane % C::LPT;
-    constexpr int EV = C::VB / C::KB;          // elements per row chunk
-    constexpr bool kMixed = C::KB == 2;        // 16-bit KV: mixed-precision FMA on packed pairs
-    constexpr float kTau = 8.f;                // lazy-rescale threshold (log2 units)
-    uint32_t stage = 0, phase = 0;             // ring position
+    constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
+    const uint32_t lane_off = (tw * C::TG + tg) * C::ROWB + c * C::VB;
+    uint32_t stage = 0, phase = 0;
     uint32_t qn = 0;
     for (int i = blockIdx.x; i < n_items; i += gridDim.x, ++qn) {
         const Item it = decode_item(p, prefix, i);
         const uint32_t slot = qn & 1u;
         bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8u * slot, (qn >> 1) & 1u, p.status, abort_flag));
-        // queries of this KV head's group, in the lane's chunk order
-        uint32_t qw[G][kMixed ? C::EPL / 2 : 1];  // packed pairs (16-bit KV)
-        float qf[G][kMixed ? 1 : C::EPL];         // floats (E4M3 KV)
+        // this warp's queries as packed 16-bit pairs in the lane's chunk order
+        uint32_t qw[C::GW][C::PL];
+        float qk_scale = p.qk_scale;
         {
-            const uint8_t* qs = qbuf + slot * ((C::QBYTES + 127) & ~127);
+            const uint8_t* qs = qbuf + slot * QSLOT;
+            if constexpr (C::KB == 2) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < C::GW; ++g)
 #pragma unroll
-                for (int v = 0; v < C::NV; ++v) {
-                    const int e0 = (v * C::LPT + c) * EV;
+                    for (int v = 0; v < C::NV; ++v)
 #pragma unroll
-                    for (int e = 0; e < EV; e += 2) {
-                        const uint32_t w = *reinterpret_cast<const uint32_t*>(qs + (g * D + e0 + e) * C::QB);
-                        if constexpr (kMixed) {
-                            qw[g][(v * EV + e) / 2] = w;
-                        } else {
-                            const float2 f = kv_pair<QDT>(w);
-                            qf[g][v * EV + e] = f.x;
-                            qf[g][v * EV + e + 1] = f.y;
+                        for (int e = 0; e < C::EV; e += 2)
+                            qw[g][(v * C::EV + e) / 2] = *reinterpret_cast<const uint32_t*>(
+                                qs + ((hg * C::GW + g) * D + (v * C::LPT + c) * C::EV + e) * C::QB);
+            } else {
+                // E4M3 cache: queries to fp16, scaled by a power of two so that
+                // the largest lands in [2^14, 2^15) (exact but for components
+                // 2^28 times smaller than the largest); the scale is folded
+                // back into the score scale
+                float qv[C::GW][C::EPL];
+                float mx = 0.f;
+#pragma unroll
+                for (int g = 0; g < C::GW; ++g)
+#pragma unroll
+                    for (int v = 0; v < C::NV; ++v)
+#pragma unroll
+                        for (int e = 0; e < C::EV; e += 2) {
+                            const float2 f = kv_pair<QDT>(*reinterpret_cast<const uint32_t*>(
+                                qs + ((hg * C::GW + g) * D + (v * C::LPT + c) * C::EV + e) * C::QB));
+                            qv[g][v * C::EV + e] = f.x;
+                            qv[g][v * C::EV + e + 1] = f.y;
+                            mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
                         }
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                int ex = mx > 0.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14 : 0;
+                ex = max(-100, min(100, ex));
+                const float down = __int_as_float((127 - ex) << 23), up = __int_as_float((127 + ex) << 23);
+                qk_scale *= up;
+#pragma unroll
+                for (int g = 0; g < C::GW; ++g)
+#pragma unroll
+                    for (int x = 0; x < C::PL; ++x) {
+                        const __half2 h = __floats2half2_rn(qv[g][2 * x] * down, qv[g][2 * x + 1] * down);
+                        qw[g][x] = *reinterpret_cast<const uint32_t*>(&h);
                     }
-                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(qempty0 + 8u * slot);
 
-        float m[G], l[G], acc[G][C::EPL];
+        float m[C::GW], l[C::GW];
+        uint64_t acc[C::GW][C::PL];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < C::GW; ++g) {
             m[g] = -INFINITY;
             l[g] = 0.f;
 #pragma unroll
-            for (int e = 0; e < C::EPL; ++e) acc[g][e] = 0.f;
+            for (int x = 0; x < C::PL; ++x) acc[g][x] = 0ull;
         }
 
-        for (int j = it.j0; j < it.j1 && ok; ++j) {
+        for (int js = it.j0; js < it.j1 && ok; js += C::SPAGES) {
             if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8u * stage, phase, p.status, abort_flag))) {
                 ok = false;
                 break;
             }
-            const bool page_good = page_ok[stage] != 0;
-            const uint8_t* Kp = ring + stage * 2u * page_bytes;
-            const uint8_t* Vp = Kp + page_bytes;
-            for (int st = 0; st < p.block_size; st += C::TPI) {
-                const int tok = st + warp * C::TG + tg;
-                const bool valid = page_good && j * p.block_size + tok < it.t1;
-                const uint8_t* krow = Kp + tok * C::ROWB + c * C::VB;
-                const uint8_t* vrow = Vp + tok * C::ROWB + c * C::VB;
-                // ---- QK: this lane's chunks, then a butterfly over the group ----
-                float sc[G];
-                {
-                    float s0[G], s1[G];
+            const int mask = stage_mask[stage];
+            const uint8_t* Kp = ring + stage * C::STAGE_BYTES + lane_off;
+            const uint8_t* Vp = Kp + C::SPAGES * C::PAGE;
+            const int tok0 = js * BS + tw * C::TG + tg;  // this group's first position
 #pragma unroll
-                    for (int g = 0; g < G; ++g) s0[g] = s1[g] = 0.f;
+            for (int u = 0; u < C::SUB; ++u) {
+                const int tis = u * C::TPI;  // step offset inside the stage
+                const bool valid = ((mask >> ((tis + tw * C::TG + tg) / BS)) & 1) && tok0 + tis < it.t1;
+                const uint8_t* krow = Kp + tis * C::ROWB;
+                const uint8_t* vrow = Vp + tis * C::ROWB;
+                // ---- QK: this lane's chunks, then a butterfly over the group ----
+                float sc[C::GW];
+                {
+                    float s0[C::GW], s1[C::GW];
+#pragma unroll
+                    for (int g = 0; g < C::GW; ++g) s0[g] = s1[g] = 0.f;
 #pragma unroll
                     for (int v = 0; v < C::NV; ++v) {
                         uint32_t w[4];
                         load_chunk<C::VB>(krow + v * C::LPT * C::VB, w);
-                        constexpr int NW = C::VB / 4;
 #pragma unroll
-                        for (int x = 0; x < NW; ++x) {
-                            if constexpr (kMixed) {
+                        for (int x = 0; x < C::VB / 4; ++x) {
+                            if constexpr (C::KB == 2) {
+                                const int pi = (v * C::EV) / 2 + x;
 #pragma unroll
-                                for (int g = 0; g < G; ++g) fma_mixed2<KVDT>(s0[g], s1[g], qw[g][(v * EV) / 2 + x], w[x]);
+                                for (int g = 0; g < C::GW; ++g) fma_mixed2<KT>(s0[g], s1[g], qw[g][pi], w[x]);
                             } else {
-                                const float2 f0 = e4m3x2_to_f2(w[x]);
-                                const float2 f1 = e4m3x2_to_f2(w[x] >> 16);
-                                const int e = v * EV + 4 * x;
+                                const uint32_t h0 = e4m3x2_to_h2(w[x]), h1 = e4m3x2_to_h2(w[x] >> 16);
+                                const int pi = (v * C::EV) / 2 + 2 * x;
 #pragma unroll
-                                for (int g = 0; g < G; ++g) {
-                                    s0[g] = fmaf(qf[g][e], f0.x, s0[g]);
-                                    s1[g] = fmaf(qf[g][e + 1], f0.y, s1[g]);
-                                    s0[g] = fmaf(qf[g][e + 2], f1.x, s0[g]);
-                                    s1[g] = fmaf(qf[g][e + 3], f1.y, s1[g]);
+                                for (int g = 0; g < C::GW; ++g) {
+                                    fma_mixed2<KT>(s0[g], s1[g], qw[g][pi], h0);
+                                    fma_mixed2<KT>(s0[g], s1[g], qw[g][pi + 1], h1);
                                 }
                             }
                         }
                     }
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int g = 0; g < C::GW; ++g) {
                         float t = s0[g] + s1[g];
 #pragma unroll
                         for (int o = 1; o < C::LPT; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                        sc[g] = valid ? t * p.qk_scale : -INFINITY;
+                        sc[g] = valid ? t * qk_scale : -INFINITY;
                     }
                 }
-                // ---- online softmax of this group (lazy rescale) ----
-                float pr[G];
+                // ---- online softmax of this group, lazy rescale (warp-uniform test) ----
+                bool need = false;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    if (sc[g] > m[g] + kTau) {
-                        const float a = fast_exp2(m[g] - sc[g]);  // 0 when m = -inf
+                for (int g = 0; g < C::GW; ++g) need |= sc[g] > m[g] + kTau;
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+                    for (int g = 0; g < C::GW; ++g) {
+                        const bool r = sc[g] > m[g] + kTau;
+                        const float a = r ? fast_exp2(m[g] - sc[g]) : 1.f;  // 0 when m = -inf
+                        m[g] = r ? sc[g] : m[g];
                         l[g] *= a;
+                        const uint64_t aa = pk2(a, a);
 #pragma unroll
-                        for (int e = 0; e < C::EPL; ++e) acc[g][e] *= a;
-                        m[g] = sc[g];
+                        for (int x = 0; x < C::PL; ++x) acc[g][x] = fmul2(acc[g][x], aa);
                     }
-                    pr[g] = valid ? fast_exp2(sc[g] - m[g]) : 0.f;
-                    l[g] += pr[g];
+                }
+                uint64_t pp[C::GW];
+#pragma unroll
+                for (int g = 0; g < C::GW; ++g) {
+                    const float pr = valid ? fast_exp2(sc[g] - m[g]) : 0.f;
+                    l[g] += pr;
+                    pp[g] = pk2(pr, pr);
                 }
                 // ---- PV over this lane's value chunks (masked rows are not read) ----
                 if (valid) {
@@ -458,22 +565,21 @@ paged_decode_kernel(const DecodeParams p) {
                     for (int v = 0; v < C::NV; ++v) {
                         uint32_t w[4];
                         load_chunk<C::VB>(vrow + v * C::LPT * C::VB, w);
-                        constexpr int NW = C::VB / 4;
 #pragma unroll
-                        for (int x = 0; x < NW; ++x) {
-                            if constexpr (kMixed) {
-                                const float2 f = kv_pair<KVDT>(w[x]);
-                                const int e = v * EV + 2 * x;
+                        for (int x = 0; x < C::VB / 4; ++x) {
+                            if constexpr (C::KB == 2) {
+                                const uint64_t v2 = pair_of<KVDT>(w[x]);
+                                const int pi = (v * C::EV) / 2 + x;
 #pragma unroll
-                                for (int g = 0; g < G; ++g) ffma2(acc[g][e], acc[g][e + 1], pr[g], f.x, f.y);
+                                for (int g = 0; g < C::GW; ++g) acc[g][pi] = ffma2(pp[g], v2, acc[g][pi]);
                             } else {
-                                const float2 f0 = e4m3x2_to_f2(w[x]);
-                                const float2 f1 = e4m3x2_to_f2(w[x] >> 16);
-                                const int e = v * EV + 4 * x;
+                                const uint64_t v0 = pair_of<PA_F16>(e4m3x2_to_h2(w[x]));
+                                const uint64_t v1 = pair_of<PA_F16>(e4m3x2_to_h2(w[x] >> 16));
+                                const int pi = (v * C::EV) / 2 + 2 * x;
 #pragma unroll
-                                for (int g = 0; g < G; ++g) {
-                                    ffma2(acc[g][e], acc[g][e + 1], pr[g], f0.x, f0.y);
-                                    ffma2(acc[g][e + 2], acc[g][e + 3], pr[g], f1.x, f1.y);
+                                for (int g = 0; g < C::GW; ++g) {
+                                    acc[g][pi] = ffma2(pp[g], v0, acc[g][pi]);
+                                    acc[g][pi + 1] = ffma2(pp[g], v1, acc[g][pi + 1]);
                                 }
                             }
                         }
@@ -488,11 +594,11 @@ paged_decode_kernel(const DecodeParams p) {
             }
         }
 
-        // ---- merge the token groups of this warp, then the warps ----
+        // ---- merge the token groups of this warp, then the token warps ----
         {
-            float* mw = merge + warp * G * (D + 2);
+            float* mw = merge + warp * C::GW * (D + 2);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < C::GW; ++g) {
                 float M = m[g];
 #pragma unroll
                 for (int o = C::LPT; o < 32; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -501,18 +607,21 @@ paged_decode_kernel(const DecodeParams p) {
 #pragma unroll
                 for (int o = C::LPT; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
 #pragma unroll
-                for (int e = 0; e < C::EPL; ++e) {
-                    float a = acc[g][e] * f;
+                for (int x = 0; x < C::PL; ++x) {
+                    float2 a = up2(acc[g][x]);
+                    a.x *= f;
+                    a.y *= f;
 #pragma unroll
-                    for (int o = C::LPT; o < 32; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                    acc[g][e] = a;
-                }
-                if (tg == 0) {
-#pragma unroll
-                    for (int v = 0; v < C::NV; ++v)
-#pragma unroll
-                        for (int e = 0; e < EV; ++e)
-                            mw[g * (D + 2) + (v * C::LPT + c) * EV + e] = acc[g][v * EV + e];
+                    for (int o = C::LPT; o < 32; o <<= 1) {
+                        a.x += __shfl_xor_sync(0xffffffffu, a.x, o);
+                        a.y += __shfl_xor_sync(0xffffffffu, a.y, o);
+                    }
+                    if (tg == 0) {
+                        const int k = 2 * x;  // lane-local element index
+                        const int e = ((k / C::EV) * C::LPT + c) * C::EV + k % C::EV;
+                        mw[g * (D + 2) + e] = a.x;
+                        mw[g * (D + 2) + e + 1] = a.y;
+                    }
                 }
                 if (lane == 0) {
                     mw[g * (D + 2) + D] = M;
@@ -526,14 +635,15 @@ paged_decode_kernel(const DecodeParams p) {
             const bool direct = it.nparts == 1;
             for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
                 const int g = (2 * e) / D, d = (2 * e) % D;
+                const int ghg = g / C::GW, gw = g % C::GW;
                 float M = -INFINITY;
 #pragma unroll
-                for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, merge[(w * G + g) * (D + 2) + D]);
+                for (int t = 0; t < C::TW; ++t) M = fmaxf(M, merge[((ghg * C::TW + t) * C::GW + gw) * (D + 2) + D]);
                 float o0 = 0.f, o1 = 0.f, lsum = 0.f;
                 if (M != -INFINITY) {
 #pragma unroll
-                    for (int w = 0; w < C::NCW; ++w) {
-                        const float* mw = merge + (w * G + g) * (D + 2);
+                    for (int t = 0; t < C::TW; ++t) {
+                        const float* mw = merge + ((ghg * C::TW + t) * C::GW + gw) * (D + 2);
                         const float a = fast_exp2(mw[D] - M);
                         lsum = fmaf(a, mw[D + 1], lsum);
                         o0 = fmaf(a, mw[d], o0);

@@ -1,29 +1,26 @@
-// Host-side launch of the paged decode kernels for one (q dtype, KV dtype)
-// pair; included by the per-dtype translation units.
+// Host-side launch of the paged decode kernels for one (q dtype, KV dtype,
+// block size); included by the per-configuration translation units.
 #pragma once
-
-#include <cmath>
 
 #include "decode_impl.cuh"
 #include "launch.h"
 
 namespace pa {
 
-// ring depth: as many (K, V) page pairs as fit in about 64 KB, at least 2
-inline int decode_stages(int page_bytes) {
-    int s = (64 * 1024) / (2 * page_bytes);
+// ring depth: as many stages as fit in about 64 KB, between 2 and 8
+inline int decode_stages(int stage_bytes) {
+    int s = (64 * 1024) / stage_bytes;
     return s < 2 ? 2 : (s > 8 ? 8 : s);
 }
 
-template <int QDT, int KVDT, int D, int G>
+template <int QDT, int KVDT, int D, int G, int BS>
 pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
-    using C = DecodeCfg<QDT, KVDT, D, G>;
-    const int page_bytes = p.block_size * C::ROWB;
-    p.stages = decode_stages(page_bytes);
-    const DecodeSmem L = DecodeSmem::make(p.stages, page_bytes, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
+    using C = DecodeCfg<QDT, KVDT, D, G, BS>;
+    p.stages = decode_stages(C::STAGE_BYTES);
+    const DecodeSmem L = DecodeSmem::make(p.stages, C::STAGE_BYTES, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
     const int smem = static_cast<int>(L.total) + 1024;  // slack for the 1 KB base alignment
     if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
-    auto kern = paged_decode_kernel<QDT, KVDT, D, G>;
+    auto kern = paged_decode_kernel<QDT, KVDT, D, G, BS>;
     static LaunchCache cache;
     const int per_sm = blocks_per_sm(kern, C::THREADS, smem, cache);
     if (per_sm <= 0) return PA_ERR_CUDA;
@@ -43,20 +40,28 @@ pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     return PA_OK;
 }
 
-template <int QDT, int KVDT>
-pa_status launch_decode_dtype(const DecodeParams& p, int head_size, int group, cudaStream_t s) {
+template <int QDT, int KVDT, int BS>
+pa_status launch_decode_bs(const DecodeParams& p, int head_size, int group, cudaStream_t s) {
 #define PA_CASE(D, G) \
-    if (head_size == D && group == G) return launch_decode_t<QDT, KVDT, D, G>(p, s);
+    if (head_size == D && group == G) return launch_decode_t<QDT, KVDT, D, G, BS>(p, s);
     PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
     PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
 #undef PA_CASE
     return PA_ERR_UNSUPPORTED;
 }
 
-// one per translation unit
-pa_status launch_decode_f16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
-pa_status launch_decode_bf16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
-pa_status launch_decode_fp8_qf16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
-pa_status launch_decode_fp8_qbf16(const DecodeParams& p, int head_size, int group, cudaStream_t s);
+// one per translation unit: (KV dtype, block size); E4M3 units take both q dtypes
+#define PA_DECLARE_DECODE(NAME) \
+    pa_status NAME(const DecodeParams& p, int q_dtype, int head_size, int group, cudaStream_t s);
+PA_DECLARE_DECODE(launch_decode_f16_bs16)
+PA_DECLARE_DECODE(launch_decode_f16_bs32)
+PA_DECLARE_DECODE(launch_decode_f16_bs64)
+PA_DECLARE_DECODE(launch_decode_bf16_bs16)
+PA_DECLARE_DECODE(launch_decode_bf16_bs32)
+PA_DECLARE_DECODE(launch_decode_bf16_bs64)
+PA_DECLARE_DECODE(launch_decode_fp8_bs16)
+PA_DECLARE_DECODE(launch_decode_fp8_bs32)
+PA_DECLARE_DECODE(launch_decode_fp8_bs64)
+#undef PA_DECLARE_DECODE
 
 }  // namespace pa
