@@ -232,8 +232,10 @@ __device__ __forceinline__ void fma_mixed2(float& a0, float& a1, uint32_t q, uin
 
 // two E4M3 codes (low 16 bits of w) -> packed fp16 pair (exact)
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t w) {
-    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
+    uint32_t h;
+    const uint16_t b = static_cast<uint16_t>(w & 0xffffu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(b));
+    return h;
 }
 
 // Packed fp32 pairs: one 64-bit register pair holds (x, y); fma/mul on both
@@ -501,6 +503,11 @@ paged_decode_kernel(const DecodeParams p) {
                 const bool valid = ((mask >> ((tis + tw * C::TG + tg) / BS)) & 1) && tok0 + tis < it.t1;
                 const uint8_t* krow = Kp + tis * C::ROWB;
                 const uint8_t* vrow = Vp + tis * C::ROWB;
+                // value chunks are loaded up front (unconditionally: the
+                // rows are in shared memory) so the loads overlap the QK math
+                uint32_t vw[C::NV][4];
+#pragma unroll
+                for (int v = 0; v < C::NV; ++v) load_chunk<C::VB>(vrow + v * C::LPT * C::VB, vw[v]);
                 // ---- QK: this lane's chunks, then a butterfly over the group ----
                 float sc[C::GW];
                 {
@@ -563,8 +570,7 @@ paged_decode_kernel(const DecodeParams p) {
                 if (valid) {
 #pragma unroll
                     for (int v = 0; v < C::NV; ++v) {
-                        uint32_t w[4];
-                        load_chunk<C::VB>(vrow + v * C::LPT * C::VB, w);
+                        const uint32_t (&w)[4] = vw[v];
 #pragma unroll
                         for (int x = 0; x < C::VB / 4; ++x) {
                             if constexpr (C::KB == 2) {

@@ -7,16 +7,22 @@
 
 namespace pa {
 
-// ring depth: as many stages as fit in about 64 KB, between 2 and 8
-inline int decode_stages(int stage_bytes) {
-    int s = (64 * 1024) / stage_bytes;
+// ring depth: as many stages as fit next to the rest of the block's shared
+// memory when `ctas` blocks share an SM (228 KB, 1 KB reserved per block),
+// at most 64 KB and 8 stages, at least 2
+inline int decode_stages(int stage_bytes, int other_bytes, int ctas) {
+    int room = (228 * 1024) / ctas - 1024 - 1024 - other_bytes;
+    if (room > 64 * 1024) room = 64 * 1024;
+    int s = room / stage_bytes;
     return s < 2 ? 2 : (s > 8 ? 8 : s);
 }
 
 template <int QDT, int KVDT, int D, int G, int BS>
 pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     using C = DecodeCfg<QDT, KVDT, D, G, BS>;
-    p.stages = decode_stages(C::STAGE_BYTES);
+    const int other = static_cast<int>(DecodeSmem::make(0, C::STAGE_BYTES, C::QBYTES, C::MERGE_FLOATS,
+                                                        p.num_seqs).total) + 2 * 8 * 8 + 64;
+    p.stages = decode_stages(C::STAGE_BYTES, other, C::MAX_REGS <= 112 ? 3 : 2);
     const DecodeSmem L = DecodeSmem::make(p.stages, C::STAGE_BYTES, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
     const int smem = static_cast<int>(L.total) + 1024;  // slack for the 1 KB base alignment
     if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
