@@ -221,6 +221,56 @@ class DecodeStep:
                           self.case.scale, self.P, self.ws, self.status)
 
 
+class PrefillStep:
+    """Inputs of one mixed varlen step (new tokens' K/V written through their
+    slots, then one varlen prefill call over all sequences), on the device."""
+
+    def __init__(self, case: W.PagedCase, device, name=""):
+        import paged_kv_cache_75_gb300 as pk
+        self.pk = pk
+        self.name = name
+        self.case = case
+        self.device = device
+        lq = np.asarray(case.meta["query_lens"], np.int64)
+        lk = np.asarray(case.meta["key_lens"], np.int64)
+        self.lq, self.lk = lq, lk
+        self.B = len(lq)
+        bt = case.block_table.cpu().numpy()
+        # a1: slots of each sequence's new tokens, positions Lk-Lq .. Lk-1
+        seq_idx = np.repeat(np.arange(self.B, dtype=np.int32), lq)
+        pos = np.concatenate([np.arange(k - q, k) for q, k in zip(lq, lk)]).astype(np.int64)
+        self.slots = torch.from_numpy(pk.pa_slot_mapping(bt, case.block_size, seq_idx, pos)).to(device)
+        T = int(lq.sum())
+        g = torch.Generator(device=device)
+        g.manual_seed(54321)
+        self.k_new = W.random_values(g, (T, case.num_kv_heads, case.head_size), case.q_dtype, device)
+        self.v_new = W.random_values(g, (T, case.num_kv_heads, case.head_size), case.q_dtype, device)
+        self.cache = pk.KVCache(case.k_cache, case.v_cache)
+        self.q = case.q
+        self.bt = case.block_table.to(device)
+        self.cu_q = case.cu_seq_lens_q.to(device)
+        self.cu_k = case.cu_seq_lens_k.to(device)
+        self.max_q, self.max_k = int(lq.max()), int(lk.max())
+        self.out = torch.empty_like(self.q)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        # algorithmic FLOPs: 4 * D * H per visible (query, key) pair, causal
+        pairs = 0
+        for q, k in zip(lq, lk):
+            i = np.arange(q)
+            pairs += int(np.minimum(k, k - q + i + 1).clip(min=0).sum())
+        self.flops = 4 * case.head_size * case.num_heads * pairs
+        self.pairs = pairs
+        self.launches_per_step = 2
+
+    def write(self):
+        self.pk.pa_kv_cache_write(self.cache, self.k_new, self.v_new, self.slots, self.status)
+
+    def main(self, q=None, out=None):
+        self.pk.pa_prefill_varlen(self.out if out is None else out, self.q if q is None else q, self.cache,
+                                  self.bt, self.cu_q, self.cu_k, self.max_q, self.max_k, self.case.scale, True,
+                                  self.status)
+
+
 def build_workload(name, device, num_seqs=None, pool_blocks=None):
     if name == "mha":
         B = num_seqs or 64
@@ -234,6 +284,8 @@ def build_workload(name, device, num_seqs=None, pool_blocks=None):
     if name == "long":
         B = num_seqs or 8
         return W.long_fp8_decode(device=device, B=B), "long_decode_%dseq_64q8kv_d128_bs32_e4m3_len_u32k_128k_p512" % B
+    if name == "mixed":
+        return W.mixed_varlen(device=device), "mixed_varlen_8prefill_120decode_32q8kv_d128_bs16_bf16_causal"
     if name == "tiny":
         case = W.tiny_decode(device=device)
         case.seq_lens = torch.tensor([31, 33, 71], dtype=torch.int32, device=device)
@@ -267,6 +319,106 @@ def timed_decode(step: DecodeStep, steps, warmup, world):
     if st != 0:
         raise RuntimeError("device status %d during the benchmark" % st)
     return total_ms, decode_ms, clk.summary()
+
+
+def timed_prefill(step: PrefillStep, steps, warmup, world):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.write()
+        step.main()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        start.record(stream)
+        for i in range(steps):
+            step.write()
+            evs[i][0].record(stream)
+            step.main()
+            evs[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    st = int(step.status.item())
+    if st != 0:
+        raise RuntimeError("device status %d during the benchmark" % st)
+    return start.elapsed_time(end), sum(a.elapsed_time(b) for a, b in evs) / steps, clk.summary()
+
+
+def timed_prefill_e2e(step: PrefillStep, steps, warmup, world):
+    host = {n: t.cpu().pin_memory() for n, t in (("q", step.q), ("k", step.k_new), ("v", step.v_new),
+                                                 ("slots", step.slots), ("cu_q", step.cu_q), ("cu_k", step.cu_k),
+                                                 ("bt", step.bt))}
+    dev = {n: torch.empty_like(t, device=step.device) for n, t in host.items()}
+    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    pk = step.pk
+
+    def one():
+        for n, t in host.items():
+            dev[n].copy_(t, non_blocking=True)
+        pk.pa_kv_cache_write(step.cache, dev["k"], dev["v"], dev["slots"], step.status)
+        pk.pa_prefill_varlen(step.out, dev["q"], step.cache, dev["bt"], dev["cu_q"], dev["cu_k"], step.max_q,
+                             step.max_k, step.case.scale, True, step.status)
+        out_host.copy_(step.out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(warmup):
+        one()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end), h2d, d2h
+
+
+def run_prefill(args, case, wname, dev, rank, world):
+    step = PrefillStep(case, dev, wname)
+    total_ms, main_ms, clocks = timed_prefill(step, args.steps, args.warmup, world)
+    total_ms, flops_sum = aggregate(total_ms, float(step.flops) * args.steps, world)
+    e2e_ms, h2d, d2h = timed_prefill_e2e(step, args.steps, args.warmup, world)
+    e2e_ms, flops_e2e = aggregate(e2e_ms, float(step.flops) * args.steps, world)
+    _, tflops_peak, tflops_sustained, peak_kind = measured_peaks()
+    achieved = step.flops / (main_ms / 1e3) / 1e12
+    line = {
+        "metric": "paged-attn varlen prefill TFLOP/s (causal, % of GB300 bf16 tensor peak)",
+        "value": round(flops_sum / (total_ms / 1e3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16->f32",
+        "data": "synthetic",
+        "config": {"workload": wname, "num_seqs": step.B, "num_heads": case.num_heads,
+                   "num_kv_heads": case.num_kv_heads, "head_size": case.head_size, "block_size": case.block_size,
+                   "total_q": int(step.lq.sum()), "visible_pairs": step.pairs, "flops_per_step": step.flops,
+                   "l2": "inputs larger than L2 (%.2f GB of K/V cache)" % (
+                       2 * case.k_cache.numel() * case.k_cache.element_size() / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "clocks": clocks,
+        "e2e": {"value": round(flops_e2e / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "roofline": {"bound": "tensor", "kernel": "pa_prefill_varlen", "achieved": round(achieved, 2),
+                     "peak": tflops_sustained, "unit": "TFLOP/s", "frac": round(achieved / tflops_sustained, 4),
+                     "peak_kind": "of %s (bf16 dense, sustained)" % peak_kind, "traffic": None,
+                     "prefill_ms": round(main_ms, 5)},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def timed_e2e(step: DecodeStep, steps, warmup, world):
@@ -352,6 +504,12 @@ def run_ours(args):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     case, wname = build_workload(args.workload, dev, args.num_seqs, args.pool_blocks)
+    if args.workload == "mixed":
+        run_prefill(args, case, wname, dev, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     step = DecodeStep(case, dev, args.partition_size, wname)
     total_ms, decode_ms, clocks = timed_decode(step, args.steps, args.warmup, world)
     total_ms, kv_sum = aggregate(total_ms, float(step.kv_bytes) * args.steps, world)
@@ -442,7 +600,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny"], default="mha")
+    ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny", "mixed"], default="mha")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="sequences (smaller profiling cases)")

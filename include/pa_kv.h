@@ -209,11 +209,15 @@ pa_status pa_decode_static_ws(void* out, const void* q, pa_dtype q_dtype, const 
  * (bottom-right alignment), otherwise all Lk keys.  A row that sees no key
  * outputs 0.
  * q, out: device [total_q][num_heads][head_size] of q_dtype (BF16 or F16,
- *   equal to kv_dtype), total_q = cu_seq_lens_q[num_seqs].
+ *   equal to kv_dtype), total_q = cu_seq_lens_q[num_seqs], 16-byte aligned.
  * cu_seq_lens_q, cu_seq_lens_k: device int32 [num_seqs + 1], non-decreasing,
- *   starting at 0.  max_seqlen_q / max_seqlen_k must bound the lengths
- *   (a longer sequence is reported as PA_ERR_INVALID_ARG and left at 0).
- * Supported: head_size 128; block_size 16, 32 or 64; 16-bit caches.
+ *   starting at 0.  max_seqlen_q / max_seqlen_k must bound the lengths (a
+ *   sequence that breaks them is reported as PA_ERR_INVALID_ARG and its rows
+ *   are not written).  A block id outside [0, num_blocks) among the entries
+ *   a sequence needs is reported as PA_ERR_BAD_BLOCK; that sequence's rows are
+ *   then unspecified.
+ * Supported: head_size 128; block_size 16, 32 or 64;
+ *   num_heads / num_kv_heads in {1, 2, 4, 8}; 16-bit caches.
  * ------------------------------------------------------------------------- */
 pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
                             const int32_t* block_table, int32_t max_blocks_per_seq,

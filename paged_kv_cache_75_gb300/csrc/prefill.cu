@@ -1,4 +1,5 @@
-// Varlen (prefill / mixed) attention over the paged KV cache.
+// Varlen (prefill / mixed) attention over the paged KV cache on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // "Paged 어텐션" (data-sketchers.com transformers paged-attention wiki),
 // Varlen 경로: a batch of sequences of different lengths is indexed by the
@@ -10,31 +11,55 @@
 // Softmax by max subtraction as in the vLLM PagedAttention design doc
 // (section Softmax), kept online across key tiles.
 //
-// This translation unit is the tensor-core path built on mma.sync
-// (m16n8k16, fp32 accumulate): 4 warps x 16 query rows per CTA, 64-key tiles
-// gathered page by page with 16-byte cp.async into XOR-swizzled shared
-// memory, double-buffered.  Causal alignment is bottom-right: query i of a
-// sequence with Lq queries and Lk keys sits at position Lk - Lq + i.
+// Work item = (sequence, tile of TQ = 128/G query tokens, KV head): its 128
+// rows are the G query heads of the KV head for TQ tokens (row = t*G + g), so
+// one key/value tile serves the whole GQA group.  Per item, key tiles of 64
+// keys stream through a 3-stage shared-memory ring:
+//   warp 0      loads pages with TMA tensor copies (128B swizzle), through the
+//               block table;
+//   warp 1      allocates tensor memory and issues the MMAs (one thread):
+//               S = Q K^T into one of two S buffers, then O += P V;
+//   warps 4..7  softmax: one row per thread, online max / sum in fp32 (exp2
+//               domain, lazy rescale of O in tensor memory), P to shared
+//               memory as 16-bit (bf16: a hi + lo pair, so the weights keep
+//               ~16 bits), then the epilogue O / l.
+// Causal alignment is bottom-right: query i of a sequence with Lq queries and
+// Lk keys sits at position Lk - Lq + i.  Every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
 namespace pa {
 namespace {
 
-constexpr int kD = 128;        // head size
-constexpr int kBM = 64;        // query rows per tile
-constexpr int kBN = 64;        // keys per tile
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRowBytes = kD * 2;
-constexpr int kTileBytes = kBN * kRowBytes;  // 16 KB
-constexpr int kQBytes = kBM * kRowBytes;     // 16 KB
+constexpr int kD = 128;              // head size
+constexpr int kBN = 64;              // keys per tile
+constexpr int kRows = 128;           // MMA M: query rows per item
+constexpr int kStages = 3;           // K/V ring depth
+constexpr int kThreads = 256;        // 8 warps
+constexpr int kSoftWarp0 = 4;        // softmax warpgroup = warps 4..7
+constexpr uint32_t kTmemCols = 256;  // S[2] x 64 + O 128
+
+// shared memory layout (bytes from the 1 KB-aligned base)
+constexpr int kQBytes = kRows * kD * 2;        // 32 KB: two 64-column blocks of 16 KB
+constexpr int kKVTileBytes = kBN * kD * 2;     // 16 KB: two 64-column blocks of 8 KB
+constexpr int kStageBytes = 2 * kKVTileBytes;  // K then V
+constexpr int kPBytes = kRows * kBN * 2;       // 16 KB per 16-bit P tile
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + kStages * kStageBytes;  // P[2] x (hi, lo)
+constexpr int kOffBar = kOffP + 2 * 2 * kPBytes;
+constexpr int kNumBars = 2 * kStages + 4 * 2 + 2;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 64;
 
 struct PrefillParams {
     void* out;
     const uint16_t* q;
-    const uint16_t* k_cache;
-    const uint16_t* v_cache;
     const int32_t* block_table;
     const int32_t* cu_q;
     const int32_t* cu_k;
@@ -43,6 +68,8 @@ struct PrefillParams {
     int32_t block_size;
     int32_t num_kv_heads;
     int32_t num_heads;
+    int32_t group;  // num_heads / num_kv_heads
+    int32_t tq;     // query tokens per item (128 / group)
     int32_t num_seqs;
     int32_t max_blocks;
     int32_t max_q;
@@ -51,47 +78,95 @@ struct PrefillParams {
     float scale_log2;  // scale * log2(e)
 };
 
-// byte offset of (row, 16-byte chunk) inside a swizzled [rows][128] b16 tile
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-    return static_cast<uint32_t>(row * kRowBytes + ((chunk ^ (row & 7)) << 4));
+// ---------------------------------------------------------------------------
+// PTX wrappers (tcgen05, TMA)
+// ---------------------------------------------------------------------------
+// shared-memory matrix descriptor, 128-byte swizzle
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = static_cast<uint64_t>((addr >> 4) & 0x3FFF);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFF) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFF) << 32;
+    d |= 1ull << 46;  // descriptor version
+    d |= 2ull << 61;  // SWIZZLE_128B
+    return d;
+}
+// instruction descriptor, kind::f16, fp32 accumulate; fmt 0 = f16, 1 = bf16
+__host__ __device__ constexpr uint32_t mma_idesc(int fmt, int M, int N, int b_mn_major) {
+    return (1u << 4) | (static_cast<uint32_t>(fmt) << 7) | (static_cast<uint32_t>(fmt) << 10) |
+           (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(addr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(addr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2-D tiled TMA load into shared memory, completion counted on `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     const int n = valid ? 16 : 0;  // 0 source bytes: zero-fill
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
-}
-
-template <int DT>
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    if constexpr (DT == PA_BF16) {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    } else {
-        asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-            "{%8,%9}, {%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-    }
+// byte offset of (row, 16-byte chunk) in a [rows][128 B] region with 128B swizzle
+__device__ __forceinline__ uint32_t sw128(int row, int chunk) {
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
 template <int DT>
@@ -105,26 +180,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-// (lo, hi) weights -> packed 16-bit pair, plus (bf16 only) the packed
-// residual pair that the first rounding dropped
-template <int DT>
-__device__ __forceinline__ void split_pair(float lo, float hi, uint32_t& main, uint32_t& rest) {
-    main = pack2<DT>(lo, hi);
-    if constexpr (DT == PA_BF16) {
-        const float lo_r = __uint_as_float(main << 16), hi_r = __uint_as_float(main & 0xffff0000u);
-        rest = pack2<DT>(lo - lo_r, hi - hi_r);
-    } else {
-        rest = 0u;
-    }
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// per-sequence lengths, or -1 if they break the stated bounds
+// lengths of sequence b; false if they break the stated bounds
 __device__ __forceinline__ bool seq_lens_ok(const PrefillParams& p, int b, int& lq, int& lk) {
     const int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
     const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
@@ -134,40 +190,103 @@ __device__ __forceinline__ bool seq_lens_ok(const PrefillParams& p, int b, int& 
            static_cast<int64_t>(lk) <= static_cast<int64_t>(p.max_blocks) * p.block_size;
 }
 
+struct Work {
+    int b, i0, kvh, lq, lk, kend, ntiles;
+};
+
+__device__ __forceinline__ Work work_item(const PrefillParams& p, const int32_t* prefix, int item) {
+    Work w;
+    const int tile_id = item / p.num_kv_heads;
+    w.kvh = item - tile_id * p.num_kv_heads;
+    int lo = 0, hi = p.num_seqs - 1;  // largest b with prefix[b] <= tile_id
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tile_id) lo = mid;
+        else hi = mid - 1;
+    }
+    w.b = lo;
+    seq_lens_ok(p, lo, w.lq, w.lk);
+    w.i0 = (tile_id - prefix[lo]) * p.tq;
+    const int shift = w.lk - w.lq;
+    w.kend = w.lk;
+    if (p.causal) w.kend = min(w.lk, shift + min(w.i0 + p.tq, w.lq));
+    w.ntiles = w.kend > 0 ? (w.kend + kBN - 1) / kBN : 0;
+    return w;
+}
+
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) paged_prefill_mma_kernel(const PrefillParams p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* sQ = smem;
-    uint8_t* sK[2] = {smem + kQBytes, smem + kQBytes + kTileBytes};
-    uint8_t* sV[2] = {smem + kQBytes + 2 * kTileBytes, smem + kQBytes + 3 * kTileBytes};
-    int32_t* prefix = reinterpret_cast<int32_t*>(smem + kQBytes + 4 * kTileBytes);
-    __shared__ int32_t scan_scratch[kWarps];
+__global__ void __launch_bounds__(kThreads, 1)
+paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                        const PrefillParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 128B-swizzled tiles need 1 KB alignment; the launch adds 1 KB of slack
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem + kOffQ;
+    uint8_t* sKV = smem + kOffKV;
+    uint8_t* sP = smem + kOffP;
+    const uint32_t bar0 = smem_addr(smem + kOffBar);
+    const uint32_t kv_full = bar0;                 // [kStages] TMA bytes
+    const uint32_t kv_empty = bar0 + 8 * kStages;  // [kStages] MMA commit after PV
+    const uint32_t s_full = bar0 + 16 * kStages;   // [2] MMA commit after QK
+    const uint32_t s_empty = s_full + 16;          // [2] 4 softmax warps: S read
+    const uint32_t p_full = s_empty + 16;          // [2] 4 softmax warps: P written
+    const uint32_t p_empty = p_full + 16;          // [2] MMA commit after PV
+    const uint32_t q_full = p_empty + 16;          // 4 softmax warps: Q in place
+    const uint32_t mma_done = q_full + 8;          // MMA commit at the very end
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSmemBytes);  // B + 1 ints past the fixed layout
+    __shared__ int32_t scan_scratch[kThreads / 32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.num_seqs;
 
-    // ---- per-sequence tile prefix: tiles(b) = ceil(Lq_b / 64) ----
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(kv_full + 8 * s, 1);
+            mbar_init(kv_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(s_full + 8 * s, 1);
+            mbar_init(s_empty + 8 * s, 4);
+            mbar_init(p_full + 8 * s, 4);
+            mbar_init(p_empty + 8 * s, 1);
+        }
+        mbar_init(q_full, 4);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+
+    // ---- per-sequence prefix of query tiles ----
     {
         const int chunk = (B + kThreads - 1) / kThreads;
         const int b0 = tid * chunk, b1 = min(B, b0 + chunk);
         int local = 0;
         for (int b = b0; b < b1; ++b) {
             int lq, lk;
-            if (seq_lens_ok(p, b, lq, lk)) local += (lq + kBM - 1) / kBM;
+            if (seq_lens_ok(p, b, lq, lk)) local += (lq + p.tq - 1) / p.tq;
             else report(p.status, PA_ERR_INVALID_ARG);
         }
         int v = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, v, o);
+            const int n = __shfl_up_sync(0xffffffffu, v, o);
             if (lane >= o) v += n;
         }
         if (lane == 31) scan_scratch[warp] = v;
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
         if (tid == 0) {
             int run = 0;
-            for (int w = 0; w < kWarps; ++w) {
-                int x = scan_scratch[w];
+            for (int w = 0; w < kThreads / 32; ++w) {
+                const int x = scan_scratch[w];
                 scan_scratch[w] = run;
                 run += x;
             }
@@ -178,208 +297,355 @@ __global__ void __launch_bounds__(kThreads, 2) paged_prefill_mma_kernel(const Pr
         for (int b = b0; b < b1; ++b) {
             prefix[b] = run;
             int lq, lk;
-            if (seq_lens_ok(p, b, lq, lk)) run += (lq + kBM - 1) / kBM;
+            if (seq_lens_ok(p, b, lq, lk)) run += (lq + p.tq - 1) / p.tq;
         }
         __syncthreads();
     }
-    const int n_items = prefix[B] * p.num_heads;
-    const int group = p.num_heads / p.num_kv_heads;
+    const uint32_t tmem = *tmem_slot;
+    const int n_items = prefix[B] * p.num_kv_heads;
     const int64_t hstride = static_cast<int64_t>(p.num_heads) * kD;  // elements per q/out row
 
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int tile_id = item / p.num_heads;
-        const int h = item - tile_id * p.num_heads;
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (prefix[mid] <= tile_id) lo = mid;
-            else hi = mid - 1;
-        }
-        const int b = lo;
-        int lq, lk;
-        seq_lens_ok(p, b, lq, lk);
-        const int i0 = (tile_id - prefix[b]) * kBM;
-        const int qrow0 = __ldg(p.cu_q + b) + i0;
-        const int shift = lk - lq;
-        const int kvh = h / group;
-        int kend = lk;  // exclusive bound on the keys this tile can see
-        if (p.causal) kend = min(lk, shift + min(i0 + kBM, lq));
-        const int n_tiles = kend > 0 ? (kend + kBN - 1) / kBN : 0;
-        const int32_t* bt_row = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
-
-        // ---- Q tile (rows past Lq are zero-filled) ----
-        for (int ci = tid; ci < kBM * 16; ci += kThreads) {
-            const int r = ci >> 4, c = ci & 15;
-            const bool ok = i0 + r < lq;
-            const uint16_t* src = p.q + (static_cast<int64_t>(ok ? qrow0 + r : 0) * hstride + h * kD + c * 8);
-            cp_async16(smem_addr(sQ) + swz(r, c), src, ok);
-        }
-        cp_async_commit();
-
-        auto load_kv = [&](int t, int buf) {
-            const int key0 = t * kBN;
-            for (int ci = tid; ci < kBN * 16; ci += kThreads) {
-                const int r = ci >> 4, c = ci & 15;
-                const int key = key0 + r;
-                bool ok = key < lk;
-                int64_t off = 0;
-                if (ok) {
-                    const int32_t blk = __ldg(bt_row + key / p.block_size);
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        report(p.status, PA_ERR_BAD_BLOCK);
-                        ok = false;
-                    } else {
-                        off = ((static_cast<int64_t>(blk) * p.num_kv_heads + kvh) * p.block_size +
-                               key % p.block_size) * kD + c * 8;
+    if (warp == 0) {
+        // ------------------------------- loader -------------------------------
+        uint32_t fill = 0, stage = 0, phase = 0;
+        bool ok = true;
+        const int ppt = kBN / p.block_size;  // pages per tile (<= 4)
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Work w = work_item(p, prefix, item);
+            const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
+            for (int t = 0; t < w.ntiles && ok; ++t) {
+                // page ids of this tile, one per lane (-1: past Lk, -2: bad id)
+                int32_t id = -1;
+                if (lane < ppt) {
+                    const int key = t * kBN + lane * p.block_size;
+                    if (key < w.lk) {
+                        id = __ldg(bt_row + key / p.block_size);
+                        if (id < 0 || id >= p.num_blocks) {
+                            report(p.status, PA_ERR_BAD_BLOCK);
+                            id = -2;
+                        }
                     }
                 }
-                cp_async16(smem_addr(sK[buf]) + swz(r, c), p.k_cache + off, ok);
-                cp_async16(smem_addr(sV[buf]) + swz(r, c), p.v_cache + off, ok);
-            }
-        };
-        if (n_tiles > 0) load_kv(0, 0);
-        cp_async_commit();
-
-        // ---- per-warp state: 16 rows; lane holds rows g and g+8 ----
-        const int g = lane >> 2, t4 = lane & 3;
-        const int row_a = i0 + warp * 16 + g;  // query index within the sequence
-        const int row_b = row_a + 8;
-        float o[16][4];
+                int32_t ids[4];
+                uint32_t bytes = 0;
 #pragma unroll
-        for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-        float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-        uint32_t qa[8][4];
-
-        for (int t = 0; t < n_tiles; ++t) {
-            const int buf = t & 1;
-            if (t + 1 < n_tiles) load_kv(t + 1, buf ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-            __syncthreads();
-            if (t == 0) {
-                // Q fragments for this warp's 16 rows, all 8 k-steps
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const int mi = lane >> 3, r = warp * 16 + (lane & 7) + (mi & 1) * 8;
-                    ldsm_x4(qa[kk], smem_addr(sQ) + swz(r, kk * 2 + (mi >> 1)));
+                for (int k = 0; k < 4; ++k) {
+                    ids[k] = __shfl_sync(0xffffffffu, id, k);
+                    if (k < ppt && ids[k] >= 0) bytes += 4u * p.block_size * kD;
+                }
+                if (lane == 0) ok = mbar_wait(kv_empty + 8 * stage, phase ^ 1u, p.status, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (lane == 0 && ok) {
+                    const uint32_t bar = kv_full + 8 * stage;
+                    const uint32_t kdst = smem_addr(sKV + stage * kStageBytes);
+                    const uint32_t vdst = kdst + kKVTileBytes;
+                    if (bytes) mbar_expect_tx(bar, bytes);
+                    else mbar_arrive(bar);
+                    for (int k = 0; k < ppt; ++k) {
+                        if (ids[k] < 0) continue;
+                        const int row = (ids[k] * p.num_kv_heads + w.kvh) * p.block_size;
+                        const uint32_t off = k * p.block_size * 128;  // rows offset inside a column block
+                        tma_load_2d(kdst + off, &map_k, 0, row, bar);
+                        tma_load_2d(kdst + kKVTileBytes / 2 + off, &map_k, 64, row, bar);
+                        tma_load_2d(vdst + off, &map_v, 0, row, bar);
+                        tma_load_2d(vdst + kKVTileBytes / 2 + off, &map_v, 64, row, bar);
+                    }
+                }
+                ++fill;
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            // ---- S = Q K^T (16 x 64 per warp) ----
-            float s[8][4];
+        }
+        // after an abort, wait (bounded) for the copies still landing
+        if (lane == 0 && *abort_flag) {
+            const uint64_t t0 = global_timer_ns();
+            const uint32_t first = fill > kStages ? fill - kStages : 0u;
+            for (uint32_t f = first; f < fill; ++f)
+                while (!mbar_try_wait(kv_full + 8 * (f % kStages), (f / kStages) & 1u))
+                    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+        }
+    } else if (warp == 1) {
+        // -------------------------------- MMA ---------------------------------
+        const uint32_t id_qk = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kBN, 0);
+        const uint32_t id_pv = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kD, 1);
+        const uint32_t tmem_o = tmem + 128;
+        uint32_t stage = 0, phase = 0;  // K/V ring position
+        uint32_t s_cnt = 0;             // S tiles produced
+        uint32_t p_cnt = 0;             // P tiles consumed
+        uint32_t q_cnt = 0;             // items with tiles
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Work w = work_item(p, prefix, item);
+            if (w.ntiles == 0) continue;
+            ok = mbar_wait(q_full, q_cnt & 1u, p.status, abort_flag);
+            ++q_cnt;
+            uint32_t prev_stage = 0;
+            for (int t = 0; t <= w.ntiles && ok; ++t) {
+                if (t < w.ntiles) {
+                    const uint32_t sb = s_cnt & 1u;
+                    ok = mbar_wait(kv_full + 8 * stage, phase, p.status, abort_flag) &&
+                         mbar_wait(s_empty + 8 * sb, ((s_cnt >> 1) & 1u) ^ 1u, p.status, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t kb = smem_addr(sKV + stage * kStageBytes);
 #pragma unroll
-            for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-                for (int np = 0; np < 4; ++np) {  // pairs of 8-key blocks
-                    uint32_t kb[4];
-                    const int mi = lane >> 3;
-                    const int key = np * 16 + (lane & 7) + (mi >> 1) * 8;
-                    ldsm_x4(kb, smem_addr(sK[buf]) + swz(key, kk * 2 + (mi & 1)));
-                    mma16816<DT>(s[2 * np], qa[kk], kb[0], kb[1]);
-                    mma16816<DT>(s[2 * np + 1], qa[kk], kb[2], kb[3]);
+                        for (int k = 0; k < kD / 16; ++k) {
+                            const uint32_t blk = (k / 4) * 16384, ko = (k % 4) * 32;
+                            const uint64_t da = smem_desc(smem_addr(sQ) + blk + ko, 16, 1024);
+                            const uint64_t db = smem_desc(kb + (k / 4) * (kKVTileBytes / 2) + ko, 16, 1024);
+                            mma_f16(tmem + sb * kBN, da, db, id_qk, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(s_full + 8 * sb);
+                    }
+                    __syncwarp();
+                    ++s_cnt;
                 }
-            }
-            // ---- mask + online softmax ----
-            const int key0 = t * kBN;
-            float mx_a = -INFINITY, mx_b = -INFINITY;
+                if (t > 0) {
+                    // O += P(t-1) V(t-1)
+                    const uint32_t pb = p_cnt & 1u;
+                    ok = mbar_wait(p_full + 8 * pb, (p_cnt >> 1) & 1u, p.status, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t vb = smem_addr(sKV + prev_stage * kStageBytes + kKVTileBytes);
+                        const uint32_t pbase = smem_addr(sP + pb * 2 * kPBytes);
+                        constexpr int kParts = DT == PA_BF16 ? 2 : 1;  // bf16: hi and lo weights
 #pragma unroll
-            for (int n = 0; n < 8; ++n) {
+                        for (int part = 0; part < kParts; ++part) {
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int key = key0 + n * 8 + t4 * 2 + e;
-                    const bool va = key < lk && (!p.causal || key <= shift + row_a);
-                    const bool vb = key < lk && (!p.causal || key <= shift + row_b);
-                    s[n][e] = va ? s[n][e] * p.scale_log2 : -INFINITY;
-                    s[n][2 + e] = vb ? s[n][2 + e] * p.scale_log2 : -INFINITY;
-                    mx_a = fmaxf(mx_a, s[n][e]);
-                    mx_b = fmaxf(mx_b, s[n][2 + e]);
+                            for (int k = 0; k < kBN / 16; ++k) {
+                                const uint64_t da = smem_desc(pbase + part * kPBytes + k * 32, 16, 1024);
+                                const uint64_t db = smem_desc(vb + k * 2048, kKVTileBytes / 2, 1024);
+                                mma_f16(tmem_o, da, db, id_pv, (t > 1 || part > 0 || k > 0) ? 1u : 0u);
+                            }
+                        }
+                        mma_commit(kv_empty + 8 * prev_stage);
+                        mma_commit(p_empty + 8 * pb);
+                    }
+                    __syncwarp();
+                    ++p_cnt;
                 }
-            }
-#pragma unroll
-            for (int off = 1; off < 4; off <<= 1) {
-                mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, off));
-                mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, off));
-            }
-            const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-            const float base_a = mn_a == -INFINITY ? 0.f : mn_a;
-            const float base_b = mn_b == -INFINITY ? 0.f : mn_b;
-            const float al_a = ex2(m_a - base_a), al_b = ex2(m_b - base_b);
-            m_a = mn_a;
-            m_b = mn_b;
-            float rs_a = 0.f, rs_b = 0.f;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                s[n][0] = ex2(s[n][0] - base_a);
-                s[n][1] = ex2(s[n][1] - base_a);
-                s[n][2] = ex2(s[n][2] - base_b);
-                s[n][3] = ex2(s[n][3] - base_b);
-                rs_a += s[n][0] + s[n][1];
-                rs_b += s[n][2] + s[n][3];
-            }
-            l_a = l_a * al_a + rs_a;
-            l_b = l_b * al_b + rs_b;
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                o[n][0] *= al_a;
-                o[n][1] *= al_a;
-                o[n][2] *= al_b;
-                o[n][3] *= al_b;
-            }
-            // ---- O += P V ----
-            // P goes to the tensor cores in V's 16-bit type.  fp16 keeps 11
-            // significant bits of each weight; bf16 keeps only 8, so for bf16
-            // P is carried as hi + lo (two bf16 terms, ~16 bits) and the
-            // product is taken twice.
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {  // 16 keys per k-step
-                uint32_t pa[4], pl[4];
-                split_pair<DT>(s[2 * kk][0], s[2 * kk][1], pa[0], pl[0]);
-                split_pair<DT>(s[2 * kk][2], s[2 * kk][3], pa[1], pl[1]);
-                split_pair<DT>(s[2 * kk + 1][0], s[2 * kk + 1][1], pa[2], pl[2]);
-                split_pair<DT>(s[2 * kk + 1][2], s[2 * kk + 1][3], pa[3], pl[3]);
-#pragma unroll
-                for (int np = 0; np < 8; ++np) {  // pairs of 8-column blocks of D
-                    uint32_t vb[4];
-                    const int mi = lane >> 3;
-                    const int key = kk * 16 + (lane & 7) + (mi & 1) * 8;
-                    ldsm_x4_t(vb, smem_addr(sV[buf]) + swz(key, np * 2 + (mi >> 1)));
-                    mma16816<DT>(o[2 * np], pa, vb[0], vb[1]);
-                    mma16816<DT>(o[2 * np + 1], pa, vb[2], vb[3]);
-                    if constexpr (DT == PA_BF16) {
-                        mma16816<DT>(o[2 * np], pl, vb[0], vb[1]);
-                        mma16816<DT>(o[2 * np + 1], pl, vb[2], vb[3]);
+                if (t < w.ntiles) {
+                    prev_stage = stage;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
                 }
             }
-            __syncthreads();  // the buffer is refilled next iteration
         }
-        cp_async_wait<0>();
-        __syncthreads();
-
-        // ---- finish rows: O / l (rows without keys stay 0) ----
-        float la = l_a, lb = l_b;  // per-lane partial sums -> row sums
+        // every MMA this warp issued is complete before tensor memory is freed
+        if (lane == 0) mma_commit(mma_done);
+        __syncwarp();
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(mma_done, 0u))
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                report(p.status, PA_ERR_TIMEOUT);
+                break;
+            }
+    } else if (warp >= kSoftWarp0) {
+        // ------------------------------ softmax -------------------------------
+        const int r = tid - kSoftWarp0 * 32;  // row of the tile = tensor-memory lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp - kSoftWarp0) * 32) << 16;
+        const uint32_t tmem_o = tmem + 128 + lane_base;
+        uint32_t s_cnt = 0, p_cnt = 0;
+        uint32_t ring = 0;  // K/V ring fills before the current item
+        constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+            const Work w = work_item(p, prefix, item);
+            const int shift = w.lk - w.lq;
+            const int t_row = r / p.group, g_row = r - t_row * p.group;
+            const int qi = w.i0 + t_row;  // query index of this row in its sequence
+            const bool row_valid = qi < w.lq;
+            const int lim = p.causal ? min(w.lk, shift + qi + 1) : w.lk;  // keys [0, lim) visible
+            uint16_t* dst = static_cast<uint16_t*>(p.out) +
+                            (static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * hstride + (w.kvh * p.group + g_row) * kD;
+            if (w.ntiles == 0) {
+                // no visible key for any row of the item: output 0
+                if (row_valid)
+                    for (int c = 0; c < kD; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
+                continue;
+            }
+            // ---- Q tile: 128 rows x 128 d, K-major with 128B swizzle, zero past Lq ----
+            {
+                const int64_t qrow0 = static_cast<int64_t>(__ldg(p.cu_q + w.b)) + w.i0;
+                for (int ci = r; ci < kRows * 16; ci += 128) {
+                    const int rr = ci >> 4, c = ci & 15;
+                    const int tt = rr / p.group, gg = rr - tt * p.group;
+                    const bool valid = w.i0 + tt < w.lq;
+                    const uint16_t* src =
+                        p.q + (valid ? (qrow0 + tt) * hstride + (w.kvh * p.group + gg) * kD + c * 8 : 0);
+                    cp_async16(smem_addr(sQ) + (c >> 3) * 16384 + sw128(rr, c & 7), src, valid);
+                }
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(q_full);
+            }
+            float m = -INFINITY, l = 0.f;
+            for (int t = 0; t < w.ntiles && ok; ++t) {
+                const uint32_t sb = s_cnt & 1u;
+                const int key0 = t * kBN;
+                ok = mbar_wait(s_full + 8 * sb, (s_cnt >> 1) & 1u, p.status, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                float s[kBN];
+                {
+                    float v[32];
+                    tmem_ld32(tmem + sb * kBN + lane_base, v);
 #pragma unroll
-        for (int off = 1; off < 4; off <<= 1) {
-            la += __shfl_xor_sync(0xffffffffu, la, off);
-            lb += __shfl_xor_sync(0xffffffffu, lb, off);
-        }
-        const float inv_a = la > 0.f ? 1.f / la : 0.f;
-        const float inv_b = lb > 0.f ? 1.f / lb : 0.f;
-        uint16_t* out = static_cast<uint16_t*>(p.out);
-        if (row_a < lq) {
-            uint16_t* dst = out + static_cast<int64_t>(__ldg(p.cu_q + b) + row_a) * hstride + h * kD;
+                    for (int i = 0; i < 32; ++i) s[i] = v[i];
+                    tmem_ld32(tmem + sb * kBN + 32 + lane_base, v);
 #pragma unroll
-            for (int n = 0; n < 16; ++n)
-                *reinterpret_cast<uint32_t*>(dst + n * 8 + t4 * 2) = pack2<DT>(o[n][0] * inv_a, o[n][1] * inv_a);
-        }
-        if (row_b < lq) {
-            uint16_t* dst = out + static_cast<int64_t>(__ldg(p.cu_q + b) + row_b) * hstride + h * kD;
+                    for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_empty + 8 * sb);  // S buffer may be rewritten
+                ++s_cnt;
+                // mask + scale (exp2 domain); rows past Lq see nothing
+                const int vis = row_valid ? lim - key0 : 0;  // visible keys of this tile: [0, vis)
+                float mx = -INFINITY;
 #pragma unroll
-            for (int n = 0; n < 16; ++n)
-                *reinterpret_cast<uint32_t*>(dst + n * 8 + t4 * 2) = pack2<DT>(o[n][2] * inv_b, o[n][3] * inv_b);
+                for (int i = 0; i < kBN; ++i) {
+                    s[i] = i < vis ? s[i] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, s[i]);
+                }
+                // this P buffer is free once PV(t-2) is done
+                const uint32_t pb = p_cnt & 1u;
+                ok = mbar_wait(p_empty + 8 * pb, ((p_cnt >> 1) & 1u) ^ 1u, p.status, abort_flag);
+                if (!ok) break;
+                // lazy rescale: move the reference max only when it grows by > tau
+                if (mx > m + kTau) {
+                    const float a = ex2(m - mx);  // 0 when m = -inf
+                    if (t > 0 && m != -INFINITY) {
+                        // O holds tiles 0..t-1: wait for PV(t-1), then scale the row
+                        const uint32_t lp = p_cnt - 1;
+                        ok = mbar_wait(p_empty + 8 * (lp & 1u), (lp >> 1) & 1u, p.status, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        for (int c0 = 0; c0 < kD; c0 += 32) {
+                            float o[32];
+                            tmem_ld32(tmem_o + c0, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= a;
+                            tmem_st32(tmem_o + c0, o);
+                        }
+                    }
+                    l *= a;
+                    m = mx;
+                }
+                const float base = m == -INFINITY ? 0.f : m;
+                float rs = 0.f;
+#pragma unroll
+                for (int i = 0; i < kBN; ++i) {
+                    s[i] = ex2(s[i] - base);  // masked: exp2(-inf) = 0
+                    rs += s[i];
+                }
+                l += rs;
+                // values past Lk in the last tile may hold anything: zero those
+                // V rows (after the tile landed) so zero weights never meet NaN
+                if (key0 + kBN > w.lk) {
+                    const uint32_t f = ring + t;
+                    ok = mbar_wait(kv_full + 8 * (f % kStages), (f / kStages) & 1u, p.status, abort_flag);
+                    if (!ok) break;
+                    uint8_t* vt = sKV + (f % kStages) * kStageBytes + kKVTileBytes;
+                    const int first = max(0, w.lk - key0);
+                    for (int ci = r; ci < (kBN - first) * 16; ci += 128) {
+                        const int rr = first + (ci >> 4), c = ci & 15;
+                        *reinterpret_cast<uint4*>(vt + (c >> 3) * (kKVTileBytes / 2) + sw128(rr, c & 7)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                uint8_t* ph = sP + pb * 2 * kPBytes;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 keys
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float a = s[c * 8 + 2 * j], b = s[c * 8 + 2 * j + 1];
+                        hw[j] = pack2<DT>(a, b);
+                        if constexpr (DT == PA_BF16) {
+                            const float ar = __uint_as_float(hw[j] << 16), br = __uint_as_float(hw[j] & 0xffff0000u);
+                            lw[j] = pack2<DT>(a - ar, b - br);
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(ph + sw128(r, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    if constexpr (DT == PA_BF16)
+                        *reinterpret_cast<uint4*>(ph + kPBytes + sw128(r, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full + 8 * pb);
+                ++p_cnt;
+            }
+            ring += w.ntiles;
+            if (!ok) break;
+            // ---- epilogue: wait for the last PV, then O / l for valid rows ----
+            const uint32_t lp = p_cnt - 1;
+            ok = mbar_wait(p_empty + 8 * (lp & 1u), (lp >> 1) & 1u, p.status, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                float o[32];
+                tmem_ld32(tmem_o + c0, o);
+                if (row_valid) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint4 u;
+                        u.x = pack2<DT>(o[8 * j] * inv, o[8 * j + 1] * inv);
+                        u.y = pack2<DT>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
+                        u.z = pack2<DT>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
+                        u.w = pack2<DT>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
+                        *reinterpret_cast<uint4*>(dst + c0 + 8 * j) = u;
+                    }
+                }
+            }
+            tc_fence_before();
         }
     }
+    // ---- teardown: every role is done; free tensor memory ----
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+// ---------------------------------------------------------------------------
+// host: tensor maps (driver entry point, no link-time dependency on libcuda)
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// the cache as a 2-D tensor of rows (num_blocks * kv_heads * block_size) x head_size
+bool make_cache_map(CUtensorMap* map, const void* base, int64_t rows, int dtype, int block_size) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(block_size)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -406,18 +672,20 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
     if ((reinterpret_cast<uintptr_t>(out) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u))
         return PA_ERR_INVALID_ARG;
     if (num_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int group = num_heads / cache->num_kv_heads;
     if (cache->head_size != kD) return PA_ERR_UNSUPPORTED;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
     if (q_dtype != PA_F16 && q_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     if (cache->kv_dtype != q_dtype) return PA_ERR_UNSUPPORTED;
     const int bs = cache->block_size;
     if (bs != 16 && bs != 32 && bs != 64) return PA_ERR_UNSUPPORTED;
     if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
+    const int64_t rows = cache->num_blocks * cache->num_kv_heads * bs;
+    if (rows > INT32_MAX) return PA_ERR_UNSUPPORTED;
 
     PrefillParams p{};
     p.out = out;
     p.q = static_cast<const uint16_t*>(q);
-    p.k_cache = static_cast<const uint16_t*>(cache->k_cache);
-    p.v_cache = static_cast<const uint16_t*>(cache->v_cache);
     p.block_table = block_table;
     p.cu_q = cu_seq_lens_q;
     p.cu_k = cu_seq_lens_k;
@@ -426,6 +694,8 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
     p.block_size = bs;
     p.num_kv_heads = cache->num_kv_heads;
     p.num_heads = num_heads;
+    p.group = group;
+    p.tq = kRows / group;
     p.num_seqs = num_seqs;
     p.max_blocks = max_blocks_per_seq;
     p.max_q = max_seqlen_q;
@@ -433,16 +703,22 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
     p.causal = causal ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
 
-    const int smem = kQBytes + 4 * kTileBytes + (num_seqs + 1) * 4;
+    CUtensorMap map_k, map_v;
+    if (!make_cache_map(&map_k, cache->k_cache, rows, q_dtype, bs) ||
+        !make_cache_map(&map_v, cache->v_cache, rows, q_dtype, bs))
+        return PA_ERR_CUDA;
+
+    const int smem = kSmemBytes + (num_seqs + 1) * 4 + 1024;
     if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
     static LaunchCache cache_bf16, cache_f16;
-    auto kern = q_dtype == PA_BF16 ? paged_prefill_mma_kernel<PA_BF16> : paged_prefill_mma_kernel<PA_F16>;
+    auto kern = q_dtype == PA_BF16 ? paged_prefill_tc_kernel<PA_BF16> : paged_prefill_tc_kernel<PA_F16>;
     const int per_sm = blocks_per_sm(kern, kThreads, smem, q_dtype == PA_BF16 ? cache_bf16 : cache_f16);
     if (per_sm <= 0) return PA_ERR_CUDA;
-    const int64_t max_items = static_cast<int64_t>(num_seqs) * ((max_seqlen_q + kBM - 1) / kBM) * num_heads;
+    const int64_t max_items =
+        static_cast<int64_t>(num_seqs) * ((max_seqlen_q + p.tq - 1) / p.tq) * cache->num_kv_heads;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);
     if (grid <= 0) return PA_OK;
-    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(map_k, map_v, p);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
