@@ -18,11 +18,17 @@
 //   warp 0      loads pages with TMA tensor copies (128B swizzle), through the
 //               block table;
 //   warp 1      allocates tensor memory and issues the MMAs (one thread):
-//               S = Q K^T into one of two S buffers, then O += P V;
-//   warps 4..7  softmax: one row per thread, online max / sum in fp32 (exp2
-//               domain, lazy rescale of O in tensor memory), P to shared
-//               memory as 16-bit (bf16: a hi + lo pair, so the weights keep
-//               ~16 bits), then the epilogue O / l.
+//               S = Q K^T into S[t & 1], then O[t & 1] += P[t & 1] V;
+//   warps 4..7, two softmax warpgroups; warpgroup x takes the key tiles
+//   8..11       t = x, x+2, ... of the item with its own S buffer, P buffer
+//               and O accumulator: one row per thread, online max / sum in
+//               fp32 (exp2 domain, lazy rescale of its O in tensor memory), P
+//               to shared memory as 16-bit (bf16: a hi + lo pair, so the
+//               weights keep ~16 bits).  The two partial results are merged
+//               by their log-sum-exp in the epilogue, O / l.
+// Scores are streamed from tensor memory in halves of 32 columns (a max pass,
+// then an exp / sum / store pass), which keeps a softmax thread's registers
+// low enough for 12 warps.
 // Causal alignment is bottom-right: query i of a sequence with Lq queries and
 // Lk keys sits at position Lk - Lq + i.  Every wait is bounded.
 #include <cuda.h>
@@ -40,9 +46,9 @@ constexpr int kD = 128;              // head size
 constexpr int kBN = 64;              // keys per tile
 constexpr int kRows = 128;           // MMA M: query rows per item
 constexpr int kStages = 3;           // K/V ring depth
-constexpr int kThreads = 256;        // 8 warps
-constexpr int kSoftWarp0 = 4;        // softmax warpgroup = warps 4..7
-constexpr uint32_t kTmemCols = 256;  // S[2] x 64 + O 128
+constexpr int kThreads = 384;        // 12 warps
+constexpr int kSoftWarp0 = 4;        // softmax warpgroups = warps 4..7 and 8..11
+constexpr uint32_t kTmemCols = 512;  // S[2] x 64 (cols 0..127), O[2] x 128 (cols 128..383)
 
 // shared memory layout (bytes from the 1 KB-aligned base)
 constexpr int kQBytes = kRows * kD * 2;        // 32 KB: two 64-column blocks of 16 KB
@@ -55,7 +61,8 @@ constexpr int kOffP = kOffKV + kStages * kStageBytes;  // P[2] x (hi, lo)
 constexpr int kOffBar = kOffP + 2 * 2 * kPBytes;
 constexpr int kNumBars = 2 * kStages + 4 * 2 + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 64;
+constexpr int kOffStats = kOffMisc + 64;                 // [128 rows] x (m, l) of warpgroup 1
+constexpr int kSmemBytes = kOffStats + kRows * 8;
 
 struct PrefillParams {
     void* out;
@@ -228,13 +235,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     const uint32_t kv_full = bar0;                 // [kStages] TMA bytes
     const uint32_t kv_empty = bar0 + 8 * kStages;  // [kStages] MMA commit after PV
     const uint32_t s_full = bar0 + 16 * kStages;   // [2] MMA commit after QK
-    const uint32_t s_empty = s_full + 16;          // [2] 4 softmax warps: S read
-    const uint32_t p_full = s_empty + 16;          // [2] 4 softmax warps: P written
-    const uint32_t p_empty = p_full + 16;          // [2] MMA commit after PV
-    const uint32_t q_full = p_empty + 16;          // 4 softmax warps: Q in place
+    const uint32_t s_empty = s_full + 16;          // [2] the 4 warps of softmax group x: S[x] read
+    const uint32_t p_full = s_empty + 16;          // [2] the 4 warps of softmax group x: P[x] written
+    const uint32_t p_empty = p_full + 16;          // [2] MMA commit after PV into O[x]
+    const uint32_t q_full = p_empty + 16;          // 8 softmax warps: Q in place
     const uint32_t mma_done = q_full + 8;          // MMA commit at the very end
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+    volatile int* stop_word = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSmemBytes);  // B + 1 ints past the fixed layout
     __shared__ int32_t scan_scratch[kThreads / 32];
 
@@ -252,9 +260,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             mbar_init(p_full + 8 * s, 4);
             mbar_init(p_empty + 8 * s, 1);
         }
-        mbar_init(q_full, 4);
+        mbar_init(q_full, 8);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
+        *stop_word = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -304,7 +313,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     const uint32_t tmem = *tmem_slot;
     const int n_items = prefix[B] * p.num_kv_heads;
     const int64_t hstride = static_cast<int64_t>(p.num_heads) * kD;  // elements per q/out row
-
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
         uint32_t fill = 0, stage = 0, phase = 0;
@@ -313,13 +321,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Work w = work_item(p, prefix, item);
             const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
+            // page ids come in batches of 32 (one per lane, -1: past Lk, -2:
+            // bad id), so the table's latency is paid once per batch
+            const int pages = (w.ntiles * kBN + p.block_size - 1) / p.block_size;
+            int32_t id = -1;
             for (int t = 0; t < w.ntiles && ok; ++t) {
-                // page ids of this tile, one per lane (-1: past Lk, -2: bad id)
-                int32_t id = -1;
-                if (lane < ppt) {
-                    const int key = t * kBN + lane * p.block_size;
-                    if (key < w.lk) {
-                        id = __ldg(bt_row + key / p.block_size);
+                const int pg0 = t * ppt;  // first page of this tile
+                if ((pg0 & 31) == 0) {
+                    const int pg = pg0 + lane;
+                    id = -1;
+                    if (pg < pages && pg * p.block_size < w.lk) {
+                        id = __ldg(bt_row + pg);
                         if (id < 0 || id >= p.num_blocks) {
                             report(p.status, PA_ERR_BAD_BLOCK);
                             id = -2;
@@ -330,7 +342,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 uint32_t bytes = 0;
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    ids[k] = __shfl_sync(0xffffffffu, id, k);
+                    ids[k] = __shfl_sync(0xffffffffu, id, (pg0 + k) & 31);
                     if (k < ppt && ids[k] >= 0) bytes += 4u * p.block_size * kD;
                 }
                 if (lane == 0) ok = mbar_wait(kv_empty + 8 * stage, phase ^ 1u, p.status, abort_flag);
@@ -370,10 +382,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         // -------------------------------- MMA ---------------------------------
         const uint32_t id_qk = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kBN, 0);
         const uint32_t id_pv = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kD, 1);
-        const uint32_t tmem_o = tmem + 128;
+        // descriptors are built once; a k-step only adds a constant to the
+        // start-address field (bits 0..13, in 16-byte units), which keeps the
+        // single issuing thread from stalling the tensor core
+        const uint64_t dq = smem_desc(smem_addr(sQ), 16, 1024);
+        const uint64_t dk = smem_desc(smem_addr(sKV), 16, 1024);
+        const uint64_t dv = smem_desc(smem_addr(sKV + kKVTileBytes), kKVTileBytes / 2, 1024);
+        const uint64_t dp = smem_desc(smem_addr(sP), 16, 1024);
         uint32_t stage = 0, phase = 0;  // K/V ring position
-        uint32_t s_cnt = 0;             // S tiles produced
-        uint32_t p_cnt = 0;             // P tiles consumed
+        uint32_t s_use[2] = {0, 0};     // uses of S[x]
+        uint32_t p_use[2] = {0, 0};     // uses of P[x]
         uint32_t q_cnt = 0;             // items with tiles
         bool ok = true;
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -384,49 +402,51 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             uint32_t prev_stage = 0;
             for (int t = 0; t <= w.ntiles && ok; ++t) {
                 if (t < w.ntiles) {
-                    const uint32_t sb = s_cnt & 1u;
+                    const int x = t & 1;
                     ok = mbar_wait(kv_full + 8 * stage, phase, p.status, abort_flag) &&
-                         mbar_wait(s_empty + 8 * sb, ((s_cnt >> 1) & 1u) ^ 1u, p.status, abort_flag);
+                         mbar_wait(s_empty + 8 * x, (s_use[x] & 1u) ^ 1u, p.status, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t kb = smem_addr(sKV + stage * kStageBytes);
+                        const uint64_t dks = dk + stage * (kStageBytes >> 4);
 #pragma unroll
                         for (int k = 0; k < kD / 16; ++k) {
-                            const uint32_t blk = (k / 4) * 16384, ko = (k % 4) * 32;
-                            const uint64_t da = smem_desc(smem_addr(sQ) + blk + ko, 16, 1024);
-                            const uint64_t db = smem_desc(kb + (k / 4) * (kKVTileBytes / 2) + ko, 16, 1024);
-                            mma_f16(tmem + sb * kBN, da, db, id_qk, k > 0 ? 1u : 0u);
+                            constexpr int kQBlk = 16384 >> 4, kKBlk = (kKVTileBytes / 2) >> 4;
+                            const uint32_t step = (k % 4) * 2;  // 32 bytes per 16-element k-step
+                            mma_f16(tmem + x * kBN, dq + ((k / 4) * kQBlk + step), dks + ((k / 4) * kKBlk + step),
+                                    id_qk, k > 0 ? 1u : 0u);
                         }
-                        mma_commit(s_full + 8 * sb);
+                        mma_commit(s_full + 8 * x);
                     }
                     __syncwarp();
-                    ++s_cnt;
+                    ++s_use[x];
                 }
                 if (t > 0) {
-                    // O += P(t-1) V(t-1)
-                    const uint32_t pb = p_cnt & 1u;
-                    ok = mbar_wait(p_full + 8 * pb, (p_cnt >> 1) & 1u, p.status, abort_flag);
+                    // O[y] += P[y] V(t-1)
+                    const int y = (t - 1) & 1;
+                    ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t vb = smem_addr(sKV + prev_stage * kStageBytes + kKVTileBytes);
-                        const uint32_t pbase = smem_addr(sP + pb * 2 * kPBytes);
+                        const uint64_t dvs = dv + prev_stage * (kStageBytes >> 4);
+                        const uint64_t dps = dp + y * ((2 * kPBytes) >> 4);
+                        const uint32_t tmem_o = tmem + 128 + y * kD;
+                        const bool first = t - 1 < 2;  // this warpgroup's first tile of the item
                         constexpr int kParts = DT == PA_BF16 ? 2 : 1;  // bf16: hi and lo weights
 #pragma unroll
                         for (int part = 0; part < kParts; ++part) {
 #pragma unroll
                             for (int k = 0; k < kBN / 16; ++k) {
-                                const uint64_t da = smem_desc(pbase + part * kPBytes + k * 32, 16, 1024);
-                                const uint64_t db = smem_desc(vb + k * 2048, kKVTileBytes / 2, 1024);
-                                mma_f16(tmem_o, da, db, id_pv, (t > 1 || part > 0 || k > 0) ? 1u : 0u);
+                                // P: 32 bytes per k-step; V: 16 keys = 2048 bytes per k-step
+                                mma_f16(tmem_o, dps + (part * (kPBytes >> 4) + k * 2), dvs + k * (2048 >> 4), id_pv,
+                                        (!first || part > 0 || k > 0) ? 1u : 0u);
                             }
                         }
                         mma_commit(kv_empty + 8 * prev_stage);
-                        mma_commit(p_empty + 8 * pb);
+                        mma_commit(p_empty + 8 * y);
                     }
                     __syncwarp();
-                    ++p_cnt;
+                    ++p_use[y];
                 }
                 if (t < w.ntiles) {
                     prev_stage = stage;
@@ -448,14 +468,20 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             }
     } else if (warp >= kSoftWarp0) {
         // ------------------------------ softmax -------------------------------
-        const int r = tid - kSoftWarp0 * 32;  // row of the tile = tensor-memory lane
-        const uint32_t lane_base = static_cast<uint32_t>((warp - kSoftWarp0) * 32) << 16;
-        const uint32_t tmem_o = tmem + 128 + lane_base;
-        uint32_t s_cnt = 0, p_cnt = 0;
-        uint32_t ring = 0;  // K/V ring fills before the current item
+        const int x = (warp - kSoftWarp0) >> 2;   // softmax group: tiles t = x, x+2, ...
+        const int u = tid - kSoftWarp0 * 32;       // 0..255 over both groups
+        const int r = u & 127;                     // row of the tile = tensor-memory lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t sbuf = tmem + x * kBN + lane_base;
+        const uint32_t tmem_o = tmem + 128 + x * kD + lane_base;
+        const uint32_t tmem_o_other = tmem + 128 + (x ^ 1) * kD + lane_base;
+        float* stats = reinterpret_cast<float*>(smem + kOffStats);
+        uint8_t* ph = sP + x * 2 * kPBytes;
+        uint32_t s_use = 0, p_use = 0;
+        uint32_t ring = 0;           // K/V ring fills before the current item
         constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
-        bool ok = true;
-        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            bool ok = true;
             const Work w = work_item(p, prefix, item);
             const int shift = w.lk - w.lq;
             const int t_row = r / p.group, g_row = r - t_row * p.group;
@@ -466,14 +492,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                             (static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * hstride + (w.kvh * p.group + g_row) * kD;
             if (w.ntiles == 0) {
                 // no visible key for any row of the item: output 0
-                if (row_valid)
+                if (x == 0 && row_valid)
                     for (int c = 0; c < kD; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
                 continue;
             }
             // ---- Q tile: 128 rows x 128 d, K-major with 128B swizzle, zero past Lq ----
             {
                 const int64_t qrow0 = static_cast<int64_t>(__ldg(p.cu_q + w.b)) + w.i0;
-                for (int ci = r; ci < kRows * 16; ci += 128) {
+                for (int ci = u; ci < kRows * 16; ci += 256) {
                     const int rr = ci >> 4, c = ci & 15;
                     const int tt = rr / p.group, gg = rr - tt * p.group;
                     const bool valid = w.i0 + tt < w.lq;
@@ -487,46 +513,42 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 if (lane == 0) mbar_arrive(q_full);
             }
             float m = -INFINITY, l = 0.f;
-            for (int t = 0; t < w.ntiles && ok; ++t) {
-                const uint32_t sb = s_cnt & 1u;
+            int mine = 0;  // tiles this group took in the item
+            for (int t = x; t < w.ntiles && ok; t += 2) {
                 const int key0 = t * kBN;
-                ok = mbar_wait(s_full + 8 * sb, (s_cnt >> 1) & 1u, p.status, abort_flag);
+                ok = mbar_wait(s_full + 8 * x, s_use & 1u, p.status, abort_flag);
                 if (!ok) break;
+                ++s_use;
                 tc_fence_after();
-                float s[kBN];
-                {
-                    float v[32];
-                    tmem_ld32(tmem + sb * kBN + lane_base, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[i] = v[i];
-                    tmem_ld32(tmem + sb * kBN + 32 + lane_base, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_empty + 8 * sb);  // S buffer may be rewritten
-                ++s_cnt;
-                // mask + scale (exp2 domain); rows past Lq see nothing
+                // pass 1: row max of the raw scores, masked past this row's last
+                // visible key (only tiles that cross it); rows past Lq see nothing
                 const int vis = row_valid ? lim - key0 : 0;  // visible keys of this tile: [0, vis)
-                float mx = -INFINITY;
+                float mx;
+                {
+                    float m8[8];
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) {
-                    s[i] = i < vis ? s[i] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, s[i]);
+                    for (int j = 0; j < 8; ++j) m8[j] = -INFINITY;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        float v[32];
+                        tmem_ld32(sbuf + 32 * h, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float sv = (vis >= kBN || 32 * h + i < vis) ? v[i] : -INFINITY;
+                            m8[i & 7] = fmaxf(m8[i & 7], sv);
+                        }
+                    }
+                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    mx *= p.scale_log2;  // scale > 0: the max commutes with it
                 }
-                // this P buffer is free once PV(t-2) is done
-                const uint32_t pb = p_cnt & 1u;
-                ok = mbar_wait(p_empty + 8 * pb, ((p_cnt >> 1) & 1u) ^ 1u, p.status, abort_flag);
+                // P[x] is free and O[x] stable once this group's previous PV is done
+                ok = mbar_wait(p_empty + 8 * x, (p_use & 1u) ^ 1u, p.status, abort_flag);
                 if (!ok) break;
                 // lazy rescale: move the reference max only when it grows by > tau
                 if (mx > m + kTau) {
                     const float a = ex2(m - mx);  // 0 when m = -inf
-                    if (t > 0 && m != -INFINITY) {
-                        // O holds tiles 0..t-1: wait for PV(t-1), then scale the row
-                        const uint32_t lp = p_cnt - 1;
-                        ok = mbar_wait(p_empty + 8 * (lp & 1u), (lp >> 1) & 1u, p.status, abort_flag);
-                        if (!ok) break;
+                    if (mine > 0 && m != -INFINITY) {
                         tc_fence_after();
                         for (int c0 = 0; c0 < kD; c0 += 32) {
                             float o[32];
@@ -539,14 +561,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                     l *= a;
                     m = mx;
                 }
-                const float base = m == -INFINITY ? 0.f : m;
-                float rs = 0.f;
-#pragma unroll
-                for (int i = 0; i < kBN; ++i) {
-                    s[i] = ex2(s[i] - base);  // masked: exp2(-inf) = 0
-                    rs += s[i];
-                }
-                l += rs;
                 // values past Lk in the last tile may hold anything: zero those
                 // V rows (after the tile landed) so zero weights never meet NaN
                 if (key0 + kBN > w.lk) {
@@ -561,53 +575,104 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
-                uint8_t* ph = sP + pb * 2 * kPBytes;
+                // pass 2: p = 2^(s*scale - m) (one FFMA and one exp2 per score),
+                // the row sum, and P to shared memory
+                const float nb = m == -INFINITY ? 0.f : -m;
+                {
+                    float r8[8];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {  // 8 chunks of 8 keys
-                    uint32_t hw[4], lw[4];
+                    for (int j = 0; j < 8; ++j) r8[j] = 0.f;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float a = s[c * 8 + 2 * j], b = s[c * 8 + 2 * j + 1];
-                        hw[j] = pack2<DT>(a, b);
-                        if constexpr (DT == PA_BF16) {
-                            const float ar = __uint_as_float(hw[j] << 16), br = __uint_as_float(hw[j] & 0xffff0000u);
-                            lw[j] = pack2<DT>(a - ar, b - br);
+                    for (int h = 0; h < 2; ++h) {
+                        float v[32];
+                        tmem_ld32(sbuf + 32 * h, v);
+                        if (h == 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(s_empty + 8 * x);  // S[x] may be rewritten
+                        }
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const bool keep = vis >= kBN || 32 * h + i < vis;
+                            v[i] = keep ? ex2(fmaf(v[i], p.scale_log2, nb)) : 0.f;
+                            r8[i & 7] += v[i];
+                        }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {  // 4 chunks of 8 keys
+                            uint32_t hw[4], lw[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float a = v[c * 8 + 2 * j], b = v[c * 8 + 2 * j + 1];
+                                hw[j] = pack2<DT>(a, b);
+                                if constexpr (DT == PA_BF16) {
+                                    const float ar = __uint_as_float(hw[j] << 16), br = __uint_as_float(hw[j] & 0xffff0000u);
+                                    lw[j] = pack2<DT>(a - ar, b - br);
+                                }
+                            }
+                            *reinterpret_cast<uint4*>(ph + sw128(r, 4 * h + c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            if constexpr (DT == PA_BF16)
+                                *reinterpret_cast<uint4*>(ph + kPBytes + sw128(r, 4 * h + c)) =
+                                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
                         }
                     }
-                    *reinterpret_cast<uint4*>(ph + sw128(r, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    if constexpr (DT == PA_BF16)
-                        *reinterpret_cast<uint4*>(ph + kPBytes + sw128(r, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
                 }
                 fence_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full + 8 * pb);
-                ++p_cnt;
+                if (lane == 0) mbar_arrive(p_full + 8 * x);
+                ++p_use;
+                ++mine;
             }
             ring += w.ntiles;
-            if (!ok) break;
-            // ---- epilogue: wait for the last PV, then O / l for valid rows ----
-            const uint32_t lp = p_cnt - 1;
-            ok = mbar_wait(p_empty + 8 * (lp & 1u), (lp >> 1) & 1u, p.status, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                float o[32];
-                tmem_ld32(tmem_o + c0, o);
-                if (row_valid) {
+            // ---- epilogue: both groups' last PVs done, then merge by log-sum-exp ----
+            // (both groups always pass both barriers of an item, even after a
+            // failed wait, and decide together whether to go on)
+            if (ok && mine > 0) ok = mbar_wait(p_empty + 8 * x, (p_use - 1) & 1u, p.status, abort_flag);
+            if (x == 1) {
+                stats[2 * r] = mine > 0 ? m : -INFINITY;
+                stats[2 * r + 1] = mine > 0 ? l : 0.f;
+            }
+            named_bar_sync(2, 256);
+            if (u == 0) *stop_word = *abort_flag;  // every wait of this item is behind us
+            if (x == 0 && ok) {
+                tc_fence_after();
+                const float m1 = stats[2 * r], l1 = stats[2 * r + 1];
+                const bool has1 = w.ntiles > 1;
+                const float M = fmaxf(m, m1);
+                const float a0 = M == -INFINITY ? 0.f : ex2(m - M);
+                const float a1 = (M == -INFINITY || !has1) ? 0.f : ex2(m1 - M);
+                const float L = l * a0 + l1 * a1;
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                for (int c0 = 0; c0 < kD; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(tmem_o + c0, o);
+                    if (has1) {
+                        float o1[32];
+                        tmem_ld32(tmem_o_other + c0, o1);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint4 u;
-                        u.x = pack2<DT>(o[8 * j] * inv, o[8 * j + 1] * inv);
-                        u.y = pack2<DT>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
-                        u.z = pack2<DT>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
-                        u.w = pack2<DT>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
-                        *reinterpret_cast<uint4*>(dst + c0 + 8 * j) = u;
+                        for (int i = 0; i < 32; ++i) o[i] = o[i] * a0 + o1[i] * a1;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= a0;
+                    }
+                    if (row_valid) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 q4;
+                            q4.x = pack2<DT>(o[8 * j] * inv, o[8 * j + 1] * inv);
+                            q4.y = pack2<DT>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
+                            q4.z = pack2<DT>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
+                            q4.w = pack2<DT>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
+                            *reinterpret_cast<uint4*>(dst + c0 + 8 * j) = q4;
+                        }
                     }
                 }
+                tc_fence_before();
             }
-            tc_fence_before();
+            // the next item's first PVs overwrite both O accumulators
+            named_bar_sync(3, 256);
+            if (*stop_word) break;
         }
     }
     // ---- teardown: every role is done; free tensor memory ----
