@@ -45,21 +45,22 @@ namespace {
 constexpr int kD = 128;              // head size
 constexpr int kBN = 64;              // keys per tile
 constexpr int kRows = 128;           // MMA M: query rows per item
-constexpr int kStages = 3;           // K/V ring depth
+constexpr int kStages = 5;           // K/V ring depth
 constexpr int kThreads = 384;        // 12 warps
 constexpr int kSoftWarp0 = 4;        // softmax warpgroups = warps 4..7 and 8..11
-constexpr uint32_t kTmemCols = 512;  // S[2] x 64 (cols 0..127), O[2] x 128 (cols 128..383)
+constexpr uint32_t kTmemCols = 512;
+// tensor-memory columns: S[x] (fp32 scores, later overwritten by the 16-bit
+// weights P[x]), O[x] (fp32 accumulators), Q (16-bit, 2 per column)
+constexpr uint32_t kColS = 0;    // S[x] at x * kBN
+constexpr uint32_t kColO = 128;  // O[x] at 128 + x * kD
+constexpr uint32_t kColQ = 384;  // 64 columns
 
 // shared memory layout (bytes from the 1 KB-aligned base)
-constexpr int kQBytes = kRows * kD * 2;        // 32 KB: two 64-column blocks of 16 KB
 constexpr int kKVTileBytes = kBN * kD * 2;     // 16 KB: two 64-column blocks of 8 KB
 constexpr int kStageBytes = 2 * kKVTileBytes;  // K then V
-constexpr int kPBytes = kRows * kBN * 2;       // 16 KB per 16-bit P tile
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kStages * kStageBytes;  // P[2] x (hi, lo)
-constexpr int kOffBar = kOffP + 2 * 2 * kPBytes;
-constexpr int kNumBars = 2 * kStages + 4 * 2 + 2;
+constexpr int kOffKV = 0;
+constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+constexpr int kNumBars = 2 * kStages + 3 * 2 + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffStats = kOffMisc + 64;                 // [128 rows] x (m, l) of warpgroup 1
 constexpr int kSmemBytes = kOffStats + kRows * 8;
@@ -103,11 +104,13 @@ __host__ __device__ constexpr uint32_t mma_idesc(int fmt, int M, int N, int b_mn
            (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
            (static_cast<uint32_t>(M >> 4) << 24);
 }
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+// A from tensor memory (row per lane, two 16-bit elements per column), B from shared memory
+__device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t db, uint32_t idesc,
+                                           uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(da), "l"(db), "r"(idesc), "r"(acc));
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(db), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -151,6 +154,49 @@ __device__ __forceinline__ void tmem_st32(uint32_t addr, const float (&v)[32]) {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 64 consecutive fp32 columns of this thread's tensor-memory lane, one wait
+__device__ __forceinline__ void tmem_ld64(uint32_t addr, float (&v)[64]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,"
+        "%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(addr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 16 consecutive 32-bit columns of this thread's lane (completion: tmem_wait_st)
+__device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t (&w)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            addr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "r"(w[8]), "r"(w[9]),
+        "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]), "r"(w[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// two fp32 -> their upper halves (bf16 by truncation), x in the low half
+__device__ __forceinline__ uint32_t hi_halves(float x, float y) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(d) : "r"(__float_as_uint(x)), "r"(__float_as_uint(y)));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // 2-D tiled TMA load into shared memory, completion counted on `bar`
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
     asm volatile(
@@ -158,11 +204,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "[%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    const int n = valid ? 16 : 0;  // 0 source bytes: zero-fill
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -228,17 +269,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 128B-swizzled tiles need 1 KB alignment; the launch adds 1 KB of slack
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sQ = smem + kOffQ;
     uint8_t* sKV = smem + kOffKV;
-    uint8_t* sP = smem + kOffP;
     const uint32_t bar0 = smem_addr(smem + kOffBar);
     const uint32_t kv_full = bar0;                 // [kStages] TMA bytes
     const uint32_t kv_empty = bar0 + 8 * kStages;  // [kStages] MMA commit after PV
-    const uint32_t s_full = bar0 + 16 * kStages;   // [2] MMA commit after QK
-    const uint32_t s_empty = s_full + 16;          // [2] the 4 warps of softmax group x: S[x] read
-    const uint32_t p_full = s_empty + 16;          // [2] the 4 warps of softmax group x: P[x] written
-    const uint32_t p_empty = p_full + 16;          // [2] MMA commit after PV into O[x]
-    const uint32_t q_full = p_empty + 16;          // 8 softmax warps: Q in place
+    const uint32_t s_full = bar0 + 16 * kStages;   // [2] MMA commit after QK into S[x]
+    const uint32_t p_full = s_full + 16;           // [2] the 4 warps of softmax group x: P[x] written
+    const uint32_t o_done = p_full + 16;           // [2] MMA commit after PV into O[x]
+    const uint32_t q_full = o_done + 16;           // 8 softmax warps: Q in tensor memory
     const uint32_t mma_done = q_full + 8;          // MMA commit at the very end
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -256,9 +294,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(s_full + 8 * s, 1);
-            mbar_init(s_empty + 8 * s, 4);
             mbar_init(p_full + 8 * s, 4);
-            mbar_init(p_empty + 8 * s, 1);
+            mbar_init(o_done + 8 * s, 1);
         }
         mbar_init(q_full, 8);
         mbar_init(mma_done, 1);
@@ -353,8 +390,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                     const uint32_t vdst = kdst + kKVTileBytes;
                     if (bytes) mbar_expect_tx(bar, bytes);
                     else mbar_arrive(bar);
-                    for (int k = 0; k < ppt; ++k) {
-                        if (ids[k] < 0) continue;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        if (k >= ppt || ids[k] < 0) continue;
                         const int row = (ids[k] * p.num_kv_heads + w.kvh) * p.block_size;
                         const uint32_t off = k * p.block_size * 128;  // rows offset inside a column block
                         tma_load_2d(kdst + off, &map_k, 0, row, bar);
@@ -380,81 +418,74 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         }
     } else if (warp == 1) {
         // -------------------------------- MMA ---------------------------------
+        // per item: S[0] = Q K(0)^T, S[1] = Q K(1)^T, then for each tile t:
+        // O[t&1] (+)= P[t&1] V(t) once softmax group t&1 has written P over S,
+        // followed by S[t&1] = Q K(t+2)^T.  One thread issues everything, so
+        // the tensor pipe sees each PV before the QK that overwrites its P,
+        // and a commit after QK(t+2) also covers PV(t).
         const uint32_t id_qk = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kBN, 0);
         const uint32_t id_pv = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kD, 1);
         // descriptors are built once; a k-step only adds a constant to the
-        // start-address field (bits 0..13, in 16-byte units), which keeps the
-        // single issuing thread from stalling the tensor core
-        const uint64_t dq = smem_desc(smem_addr(sQ), 16, 1024);
+        // start-address field (bits 0..13, in 16-byte units)
         const uint64_t dk = smem_desc(smem_addr(sKV), 16, 1024);
         const uint64_t dv = smem_desc(smem_addr(sKV + kKVTileBytes), kKVTileBytes / 2, 1024);
-        const uint64_t dp = smem_desc(smem_addr(sP), 16, 1024);
-        uint32_t stage = 0, phase = 0;  // K/V ring position
-        uint32_t s_use[2] = {0, 0};     // uses of S[x]
-        uint32_t p_use[2] = {0, 0};     // uses of P[x]
-        uint32_t q_cnt = 0;             // items with tiles
+        uint32_t qk_stage = 0, qk_phase = 0;  // ring position of the next QK
+        uint32_t pv_stage = 0;                // ring position of the next PV
+        uint32_t p_use[2] = {0, 0};           // P[x] handed over so far
+        uint32_t q_cnt = 0;                   // items with tiles
         bool ok = true;
+        auto issue_qk = [&](int t) -> bool {
+            if (!mbar_wait(kv_full + 8 * qk_stage, qk_phase, p.status, abort_flag)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t dks = dk + qk_stage * (kStageBytes >> 4);
+#pragma unroll
+                for (int k = 0; k < kD / 16; ++k) {
+                    constexpr int kKBlk = (kKVTileBytes / 2) >> 4;
+                    // Q: 8 columns per 16-element k-step; K: 32 bytes per k-step in a 64-column block
+                    mma_f16_ts(tmem + kColS + (t & 1) * kBN, tmem + kColQ + k * 8,
+                               dks + ((k / 4) * kKBlk + (k % 4) * 2), id_qk, k > 0 ? 1u : 0u);
+                }
+                mma_commit(s_full + 8 * (t & 1));
+            }
+            __syncwarp();
+            if (++qk_stage == kStages) {
+                qk_stage = 0;
+                qk_phase ^= 1u;
+            }
+            return true;
+        };
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Work w = work_item(p, prefix, item);
             if (w.ntiles == 0) continue;
             ok = mbar_wait(q_full, q_cnt & 1u, p.status, abort_flag);
             ++q_cnt;
-            uint32_t prev_stage = 0;
-            for (int t = 0; t <= w.ntiles && ok; ++t) {
-                if (t < w.ntiles) {
-                    const int x = t & 1;
-                    ok = mbar_wait(kv_full + 8 * stage, phase, p.status, abort_flag) &&
-                         mbar_wait(s_empty + 8 * x, (s_use[x] & 1u) ^ 1u, p.status, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t dks = dk + stage * (kStageBytes >> 4);
+            if (ok) ok = issue_qk(0);
+            if (ok && w.ntiles > 1) ok = issue_qk(1);
+            for (int t = 0; t < w.ntiles && ok; ++t) {
+                const int y = t & 1;
+                ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag);
+                if (!ok) break;
+                ++p_use[y];
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t dvs = dv + pv_stage * (kStageBytes >> 4);
+                    constexpr int kParts = DT == PA_BF16 ? 2 : 1;  // bf16: hi and lo weights
 #pragma unroll
-                        for (int k = 0; k < kD / 16; ++k) {
-                            constexpr int kQBlk = 16384 >> 4, kKBlk = (kKVTileBytes / 2) >> 4;
-                            const uint32_t step = (k % 4) * 2;  // 32 bytes per 16-element k-step
-                            mma_f16(tmem + x * kBN, dq + ((k / 4) * kQBlk + step), dks + ((k / 4) * kKBlk + step),
-                                    id_qk, k > 0 ? 1u : 0u);
+                    for (int part = 0; part < kParts; ++part) {
+#pragma unroll
+                        for (int k = 0; k < kBN / 16; ++k) {
+                            // P: 8 columns per 16 keys (hi at 0..31, lo at 32..63); V: 2048 bytes per 16 keys
+                            mma_f16_ts(tmem + kColO + y * kD, tmem + kColS + y * kBN + part * 32 + k * 8,
+                                       dvs + k * (2048 >> 4), id_pv, (t >= 2 || part > 0 || k > 0) ? 1u : 0u);
                         }
-                        mma_commit(s_full + 8 * x);
                     }
-                    __syncwarp();
-                    ++s_use[x];
+                    mma_commit(kv_empty + 8 * pv_stage);
+                    mma_commit(o_done + 8 * y);
                 }
-                if (t > 0) {
-                    // O[y] += P[y] V(t-1)
-                    const int y = (t - 1) & 1;
-                    ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t dvs = dv + prev_stage * (kStageBytes >> 4);
-                        const uint64_t dps = dp + y * ((2 * kPBytes) >> 4);
-                        const uint32_t tmem_o = tmem + 128 + y * kD;
-                        const bool first = t - 1 < 2;  // this warpgroup's first tile of the item
-                        constexpr int kParts = DT == PA_BF16 ? 2 : 1;  // bf16: hi and lo weights
-#pragma unroll
-                        for (int part = 0; part < kParts; ++part) {
-#pragma unroll
-                            for (int k = 0; k < kBN / 16; ++k) {
-                                // P: 32 bytes per k-step; V: 16 keys = 2048 bytes per k-step
-                                mma_f16(tmem_o, dps + (part * (kPBytes >> 4) + k * 2), dvs + k * (2048 >> 4), id_pv,
-                                        (!first || part > 0 || k > 0) ? 1u : 0u);
-                            }
-                        }
-                        mma_commit(kv_empty + 8 * prev_stage);
-                        mma_commit(p_empty + 8 * y);
-                    }
-                    __syncwarp();
-                    ++p_use[y];
-                }
-                if (t < w.ntiles) {
-                    prev_stage = stage;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
+                __syncwarp();
+                if (++pv_stage == kStages) pv_stage = 0;
+                if (t + 2 < w.ntiles) ok = issue_qk(t + 2);
             }
         }
         // every MMA this warp issued is complete before tensor memory is freed
@@ -472,11 +503,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         const int u = tid - kSoftWarp0 * 32;       // 0..255 over both groups
         const int r = u & 127;                     // row of the tile = tensor-memory lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t sbuf = tmem + x * kBN + lane_base;
-        const uint32_t tmem_o = tmem + 128 + x * kD + lane_base;
-        const uint32_t tmem_o_other = tmem + 128 + (x ^ 1) * kD + lane_base;
+        const uint32_t sbuf = tmem + kColS + x * kBN + lane_base;
+        const uint32_t tmem_o = tmem + kColO + x * kD + lane_base;
+        const uint32_t tmem_o_other = tmem + kColO + (x ^ 1) * kD + lane_base;
         float* stats = reinterpret_cast<float*>(smem + kOffStats);
-        uint8_t* ph = sP + x * 2 * kPBytes;
         uint32_t s_use = 0, p_use = 0;
         uint32_t ring = 0;           // K/V ring fills before the current item
         constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
@@ -488,27 +518,32 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const int qi = w.i0 + t_row;  // query index of this row in its sequence
             const bool row_valid = qi < w.lq;
             const int lim = p.causal ? min(w.lk, shift + qi + 1) : w.lk;  // keys [0, lim) visible
-            uint16_t* dst = static_cast<uint16_t*>(p.out) +
-                            (static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * hstride + (w.kvh * p.group + g_row) * kD;
+            const int64_t row_off =
+                (static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * hstride + (w.kvh * p.group + g_row) * kD;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + row_off;
             if (w.ntiles == 0) {
                 // no visible key for any row of the item: output 0
                 if (x == 0 && row_valid)
                     for (int c = 0; c < kD; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
                 continue;
             }
-            // ---- Q tile: 128 rows x 128 d, K-major with 128B swizzle, zero past Lq ----
+            // ---- Q row -> tensor memory (group x: elements 64x .. 64x+63), zero past Lq ----
             {
-                const int64_t qrow0 = static_cast<int64_t>(__ldg(p.cu_q + w.b)) + w.i0;
-                for (int ci = u; ci < kRows * 16; ci += 256) {
-                    const int rr = ci >> 4, c = ci & 15;
-                    const int tt = rr / p.group, gg = rr - tt * p.group;
-                    const bool valid = w.i0 + tt < w.lq;
-                    const uint16_t* src =
-                        p.q + (valid ? (qrow0 + tt) * hstride + (w.kvh * p.group + gg) * kD + c * 8 : 0);
-                    cp_async16(smem_addr(sQ) + (c >> 3) * 16384 + sw128(rr, c & 7), src, valid);
+                uint32_t qw[32];
+                const uint4* src = reinterpret_cast<const uint4*>(p.q + row_off + 64 * x);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 v = row_valid ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
+                    qw[4 * j] = v.x;
+                    qw[4 * j + 1] = v.y;
+                    qw[4 * j + 2] = v.z;
+                    qw[4 * j + 3] = v.w;
                 }
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                fence_async_smem();
+                const uint32_t qcol = tmem + kColQ + 32 * x + lane_base;
+                tmem_st16(qcol, *reinterpret_cast<const uint32_t(*)[16]>(qw));
+                tmem_st16(qcol + 16, *reinterpret_cast<const uint32_t(*)[16]>(qw + 16));
+                tmem_wait_st();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(q_full);
             }
@@ -520,36 +555,36 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 if (!ok) break;
                 ++s_use;
                 tc_fence_after();
-                // pass 1: row max of the raw scores, masked past this row's last
-                // visible key (only tiles that cross it); rows past Lq see nothing
+                // the scores of this tile; masked past this row's last visible
+                // key (only tiles that cross it); rows past Lq see nothing
+                float sv[64];
+                tmem_ld64(sbuf, sv);
                 const int vis = row_valid ? lim - key0 : 0;  // visible keys of this tile: [0, vis)
+                if (vis < kBN) {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (i >= vis) sv[i] = -INFINITY;
+                }
                 float mx;
                 {
                     float m8[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) m8[j] = -INFINITY;
+                    for (int j = 0; j < 8; ++j) m8[j] = fmax3(sv[8 * j], sv[8 * j + 1], sv[8 * j + 2]);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float v[32];
-                        tmem_ld32(sbuf + 32 * h, v);
+                    for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], sv[8 * j + 3], sv[8 * j + 4]);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float sv = (vis >= kBN || 32 * h + i < vis) ? v[i] : -INFINITY;
-                            m8[i & 7] = fmaxf(m8[i & 7], sv);
-                        }
-                    }
-                    mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+                    for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], sv[8 * j + 5], sv[8 * j + 6]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], sv[8 * j + 7]);
+                    mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                     mx *= p.scale_log2;  // scale > 0: the max commutes with it
                 }
-                // P[x] is free and O[x] stable once this group's previous PV is done
-                ok = mbar_wait(p_empty + 8 * x, (p_use & 1u) ^ 1u, p.status, abort_flag);
-                if (!ok) break;
-                // lazy rescale: move the reference max only when it grows by > tau
+                // lazy rescale: move the reference max only when it grows by > tau.
+                // O[x] is stable: the commit behind this tile's QK covered this
+                // group's previous PV.
                 if (mx > m + kTau) {
                     const float a = ex2(m - mx);  // 0 when m = -inf
                     if (mine > 0 && m != -INFINITY) {
-                        tc_fence_after();
                         for (int c0 = 0; c0 < kD; c0 += 32) {
                             float o[32];
                             tmem_ld32(tmem_o + c0, o);
@@ -574,50 +609,40 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         *reinterpret_cast<uint4*>(vt + (c >> 3) * (kKVTileBytes / 2) + sw128(rr, c & 7)) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
+                    fence_async_smem();
                 }
-                // pass 2: p = 2^(s*scale - m) (one FFMA and one exp2 per score),
-                // the row sum, and P to shared memory
+                // p = 2^(s*scale - m): one FFMA and one exp2 per score (masked
+                // scores are -inf and give 0); the row sum; P over S in tensor
+                // memory as 16-bit pairs (bf16: hi at columns 0..31 and the
+                // remainder lo at 32..63, both truncated, ~16 bits together)
                 const float nb = m == -INFINITY ? 0.f : -m;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) sv[i] = ex2(fmaf(sv[i], p.scale_log2, nb));
                 {
                     float r8[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) r8[j] = 0.f;
+                    for (int j = 0; j < 8; ++j) r8[j] = (sv[j] + sv[j + 8]) + (sv[j + 16] + sv[j + 24]);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        float v[32];
-                        tmem_ld32(sbuf + 32 * h, v);
-                        if (h == 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(s_empty + 8 * x);  // S[x] may be rewritten
-                        }
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const bool keep = vis >= kBN || 32 * h + i < vis;
-                            v[i] = keep ? ex2(fmaf(v[i], p.scale_log2, nb)) : 0.f;
-                            r8[i & 7] += v[i];
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // 4 chunks of 8 keys
-                            uint32_t hw[4], lw[4];
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float a = v[c * 8 + 2 * j], b = v[c * 8 + 2 * j + 1];
-                                hw[j] = pack2<DT>(a, b);
-                                if constexpr (DT == PA_BF16) {
-                                    const float ar = __uint_as_float(hw[j] << 16), br = __uint_as_float(hw[j] & 0xffff0000u);
-                                    lw[j] = pack2<DT>(a - ar, b - br);
-                                }
-                            }
-                            *reinterpret_cast<uint4*>(ph + sw128(r, 4 * h + c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                            if constexpr (DT == PA_BF16)
-                                *reinterpret_cast<uint4*>(ph + kPBytes + sw128(r, 4 * h + c)) =
-                                    make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                        }
-                    }
+                    for (int j = 0; j < 8; ++j) r8[j] += (sv[j + 32] + sv[j + 40]) + (sv[j + 48] + sv[j + 56]);
                     l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
                 }
-                fence_async_smem();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // keys 32h .. 32h+31 = columns 16h .. 16h+15
+                    uint32_t hw[16], lw[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float a = sv[32 * h + 2 * j], b = sv[32 * h + 2 * j + 1];
+                        if constexpr (DT == PA_BF16) {
+                            hw[j] = hi_halves(a, b);
+                            lw[j] = hi_halves(a - __uint_as_float(hw[j] << 16), b - __uint_as_float(hw[j] & 0xffff0000u));
+                        } else {
+                            hw[j] = pack2<DT>(a, b);
+                        }
+                    }
+                    tmem_st16(sbuf + 16 * h, hw);
+                    if constexpr (DT == PA_BF16) tmem_st16(sbuf + 32 + 16 * h, lw);
+                }
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(p_full + 8 * x);
@@ -628,7 +653,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             // ---- epilogue: both groups' last PVs done, then merge by log-sum-exp ----
             // (both groups always pass both barriers of an item, even after a
             // failed wait, and decide together whether to go on)
-            if (ok && mine > 0) ok = mbar_wait(p_empty + 8 * x, (p_use - 1) & 1u, p.status, abort_flag);
+            if (ok && mine > 0) ok = mbar_wait(o_done + 8 * x, (p_use - 1) & 1u, p.status, abort_flag);
             if (x == 1) {
                 stats[2 * r] = mine > 0 ? m : -INFINITY;
                 stats[2 * r + 1] = mine > 0 ? l : 0.f;
@@ -668,10 +693,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         }
                     }
                 }
-                tc_fence_before();
             }
-            // the next item's first PVs overwrite both O accumulators
+            // the next item's Q store and first PVs overwrite tensor memory
+            // that this epilogue and the last QKs used
+            tc_fence_before();
             named_bar_sync(3, 256);
+            tc_fence_after();
             if (*stop_word) break;
         }
     }
