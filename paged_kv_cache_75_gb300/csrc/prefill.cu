@@ -43,27 +43,31 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;              // head size
-constexpr int kBN = 64;              // keys per tile
+constexpr int kBN = 128;             // keys per tile
 constexpr int kRows = 128;           // MMA M: query rows per item
-constexpr int kStages = 5;           // K/V ring depth
+constexpr int kStages = 3;           // K/V ring depth
 constexpr int kThreads = 384;        // 12 warps
 constexpr int kSoftWarp0 = 4;        // softmax warpgroups = warps 4..7 and 8..11
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns: S[x] (fp32 scores, later overwritten by the 16-bit
-// weights P[x]), O[x] (fp32 accumulators), Q (16-bit, 2 per column)
-constexpr uint32_t kColS = 0;    // S[x] at x * kBN
-constexpr uint32_t kColO = 128;  // O[x] at 128 + x * kD
+// tensor-memory columns: S[b] (fp32 scores of key tile b = t & 1, later
+// overwritten by the 16-bit weights P), O (fp32 accumulator), Q (16-bit, two
+// per column).  Softmax warpgroup x owns the key columns 64x .. 64x+63 of each
+// S and the value columns 64x .. 64x+63 of O.
+constexpr uint32_t kColS = 0;    // S[b] at b * kBN
+constexpr uint32_t kColO = 256;  // 128 columns
 constexpr uint32_t kColQ = 384;  // 64 columns
 
 // shared memory layout (bytes from the 1 KB-aligned base)
-constexpr int kKVTileBytes = kBN * kD * 2;     // 16 KB: two 64-column blocks of 8 KB
+constexpr int kBlkBytes = kBN * 128;           // 16 KB: one 64-column block of a K or V tile
+constexpr int kKVTileBytes = 2 * kBlkBytes;    // 32 KB
 constexpr int kStageBytes = 2 * kKVTileBytes;  // K then V
 constexpr int kOffKV = 0;
 constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 3 * 2 + 2;
+constexpr int kNumBars = 2 * kStages + 2 * 2 + 3;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffStats = kOffMisc + 64;                 // [128 rows] x (m, l) of warpgroup 1
-constexpr int kSmemBytes = kOffStats + kRows * 8;
+constexpr int kOffXch = kOffMisc + 64;                   // [2 slots][2 groups][128 rows] floats
+constexpr int kSmemBytes = kOffXch + 2 * 2 * kRows * 4;
+constexpr int kMaxSeqs = 6144;                           // prefix of query tiles: (B + 1) ints
 
 struct PrefillParams {
     void* out;
@@ -273,14 +277,15 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     const uint32_t bar0 = smem_addr(smem + kOffBar);
     const uint32_t kv_full = bar0;                 // [kStages] TMA bytes
     const uint32_t kv_empty = bar0 + 8 * kStages;  // [kStages] MMA commit after PV
-    const uint32_t s_full = bar0 + 16 * kStages;   // [2] MMA commit after QK into S[x]
-    const uint32_t p_full = s_full + 16;           // [2] the 4 warps of softmax group x: P[x] written
-    const uint32_t o_done = p_full + 16;           // [2] MMA commit after PV into O[x]
-    const uint32_t q_full = o_done + 16;           // 8 softmax warps: Q in tensor memory
+    const uint32_t s_full = bar0 + 16 * kStages;   // [2] MMA commit after QK into S[b]
+    const uint32_t p_full = s_full + 16;           // [2] the 8 softmax warps: P[b] written
+    const uint32_t o_done = p_full + 16;           // MMA commit after each PV
+    const uint32_t q_full = o_done + 8;            // 8 softmax warps: Q in tensor memory
     const uint32_t mma_done = q_full + 8;          // MMA commit at the very end
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-    volatile int* stop_word = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+    volatile int* snap = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);  // [2] abort snapshots
+    float* xch = reinterpret_cast<float*>(smem + kOffXch);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSmemBytes);  // B + 1 ints past the fixed layout
     __shared__ int32_t scan_scratch[kThreads / 32];
 
@@ -294,13 +299,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(s_full + 8 * s, 1);
-            mbar_init(p_full + 8 * s, 4);
-            mbar_init(o_done + 8 * s, 1);
+            mbar_init(p_full + 8 * s, 8);
         }
+        mbar_init(o_done, 1);
         mbar_init(q_full, 8);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
-        *stop_word = 0;
+        snap[0] = 0;
+        snap[1] = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -354,7 +360,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         // ------------------------------- loader -------------------------------
         uint32_t fill = 0, stage = 0, phase = 0;
         bool ok = true;
-        const int ppt = kBN / p.block_size;  // pages per tile (<= 4)
+        const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
         for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
             const Work w = work_item(p, prefix, item);
             const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
@@ -375,30 +381,29 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         }
                     }
                 }
-                int32_t ids[4];
-                uint32_t bytes = 0;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    ids[k] = __shfl_sync(0xffffffffu, id, (pg0 + k) & 31);
-                    if (k < ppt && ids[k] >= 0) bytes += 4u * p.block_size * kD;
-                }
+                // lane k < ppt holds the id of page k of this tile
+                const int my_id = __shfl_sync(0xffffffffu, id, (pg0 + (lane & 7)) & 31);
+                const bool have = lane < ppt && my_id >= 0;
+                const uint32_t bytes =
+                    static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, have))) * 4u * p.block_size * kD;
                 if (lane == 0) ok = mbar_wait(kv_empty + 8 * stage, phase ^ 1u, p.status, abort_flag);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (lane == 0 && ok) {
+                if (ok) {
                     const uint32_t bar = kv_full + 8 * stage;
-                    const uint32_t kdst = smem_addr(sKV + stage * kStageBytes);
-                    const uint32_t vdst = kdst + kKVTileBytes;
-                    if (bytes) mbar_expect_tx(bar, bytes);
-                    else mbar_arrive(bar);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        if (k >= ppt || ids[k] < 0) continue;
-                        const int row = (ids[k] * p.num_kv_heads + w.kvh) * p.block_size;
-                        const uint32_t off = k * p.block_size * 128;  // rows offset inside a column block
-                        tma_load_2d(kdst + off, &map_k, 0, row, bar);
-                        tma_load_2d(kdst + kKVTileBytes / 2 + off, &map_k, 64, row, bar);
-                        tma_load_2d(vdst + off, &map_v, 0, row, bar);
-                        tma_load_2d(vdst + kKVTileBytes / 2 + off, &map_v, 64, row, bar);
+                    if (lane == 0) {
+                        if (bytes) mbar_expect_tx(bar, bytes);
+                        else mbar_arrive(bar);
+                    }
+                    __syncwarp();
+                    if (have) {
+                        // one lane per page: 4 copies of bs rows x 64 columns
+                        const uint32_t kdst = smem_addr(sKV + stage * kStageBytes) + lane * p.block_size * 128;
+                        const uint32_t vdst = kdst + kKVTileBytes;
+                        const int row = (my_id * p.num_kv_heads + w.kvh) * p.block_size;
+                        tma_load_2d(kdst, &map_k, 0, row, bar);
+                        tma_load_2d(kdst + kBlkBytes, &map_k, 64, row, bar);
+                        tma_load_2d(vdst, &map_v, 0, row, bar);
+                        tma_load_2d(vdst + kBlkBytes, &map_v, 64, row, bar);
                     }
                 }
                 ++fill;
@@ -419,19 +424,19 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     } else if (warp == 1) {
         // -------------------------------- MMA ---------------------------------
         // per item: S[0] = Q K(0)^T, S[1] = Q K(1)^T, then for each tile t:
-        // O[t&1] (+)= P[t&1] V(t) once softmax group t&1 has written P over S,
-        // followed by S[t&1] = Q K(t+2)^T.  One thread issues everything, so
-        // the tensor pipe sees each PV before the QK that overwrites its P,
+        // O (+)= P[t&1] V(t) once both softmax warpgroups have written P over
+        // S, followed by S[t&1] = Q K(t+2)^T.  One thread issues everything,
+        // so the tensor pipe sees each PV before the QK that overwrites its P,
         // and a commit after QK(t+2) also covers PV(t).
         const uint32_t id_qk = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kBN, 0);
         const uint32_t id_pv = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kD, 1);
         // descriptors are built once; a k-step only adds a constant to the
         // start-address field (bits 0..13, in 16-byte units)
         const uint64_t dk = smem_desc(smem_addr(sKV), 16, 1024);
-        const uint64_t dv = smem_desc(smem_addr(sKV + kKVTileBytes), kKVTileBytes / 2, 1024);
+        const uint64_t dv = smem_desc(smem_addr(sKV + kKVTileBytes), kBlkBytes, 1024);
         uint32_t qk_stage = 0, qk_phase = 0;  // ring position of the next QK
         uint32_t pv_stage = 0;                // ring position of the next PV
-        uint32_t p_use[2] = {0, 0};           // P[x] handed over so far
+        uint32_t p_use[2] = {0, 0};           // P[b] handed over so far
         uint32_t q_cnt = 0;                   // items with tiles
         bool ok = true;
         auto issue_qk = [&](int t) -> bool {
@@ -441,10 +446,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 const uint64_t dks = dk + qk_stage * (kStageBytes >> 4);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
-                    constexpr int kKBlk = (kKVTileBytes / 2) >> 4;
                     // Q: 8 columns per 16-element k-step; K: 32 bytes per k-step in a 64-column block
                     mma_f16_ts(tmem + kColS + (t & 1) * kBN, tmem + kColQ + k * 8,
-                               dks + ((k / 4) * kKBlk + (k % 4) * 2), id_qk, k > 0 ? 1u : 0u);
+                               dks + ((k / 4) * (kBlkBytes >> 4) + (k % 4) * 2), id_qk, k > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full + 8 * (t & 1));
             }
@@ -474,14 +478,15 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
 #pragma unroll
                     for (int part = 0; part < kParts; ++part) {
 #pragma unroll
-                        for (int k = 0; k < kBN / 16; ++k) {
-                            // P: 8 columns per 16 keys (hi at 0..31, lo at 32..63); V: 2048 bytes per 16 keys
-                            mma_f16_ts(tmem + kColO + y * kD, tmem + kColS + y * kBN + part * 32 + k * 8,
-                                       dvs + k * (2048 >> 4), id_pv, (t >= 2 || part > 0 || k > 0) ? 1u : 0u);
+                        for (int j = 0; j < kBN / 16; ++j) {
+                            // keys 16j..16j+15: P of warpgroup j/4 at 8 columns (hi at +0, lo at +32);
+                            // V: 2048 bytes per 16 keys
+                            mma_f16_ts(tmem + kColO, tmem + kColS + y * kBN + (j / 4) * 64 + part * 32 + (j % 4) * 8,
+                                       dvs + j * (2048 >> 4), id_pv, (t > 0 || part > 0 || j > 0) ? 1u : 0u);
                         }
                     }
                     mma_commit(kv_empty + 8 * pv_stage);
-                    mma_commit(o_done + 8 * y);
+                    mma_commit(o_done);
                 }
                 __syncwarp();
                 if (++pv_stage == kStages) pv_stage = 0;
@@ -499,19 +504,34 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             }
     } else if (warp >= kSoftWarp0) {
         // ------------------------------ softmax -------------------------------
-        const int x = (warp - kSoftWarp0) >> 2;   // softmax group: tiles t = x, x+2, ...
-        const int u = tid - kSoftWarp0 * 32;       // 0..255 over both groups
+        // Both warpgroups work on every key tile: warpgroup x takes keys
+        // 64x .. 64x+63.  Per tile they swap their row maxima through shared
+        // memory (one named barrier), so both use the same reference max m
+        // and make the same lazy-rescale decision; each keeps its own partial
+        // row sum.  Every decision to stop is taken from an abort snapshot
+        // written right after the previous barrier, so all 256 threads pass
+        // the same sequence of named barriers.
+        const int x = (warp - kSoftWarp0) >> 2;   // warpgroup
+        const int u = tid - kSoftWarp0 * 32;       // 0..255 over both warpgroups
         const int r = u & 127;                     // row of the tile = tensor-memory lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t sbuf = tmem + kColS + x * kBN + lane_base;
-        const uint32_t tmem_o = tmem + kColO + x * kD + lane_base;
-        const uint32_t tmem_o_other = tmem + kColO + (x ^ 1) * kD + lane_base;
-        float* stats = reinterpret_cast<float*>(smem + kOffStats);
-        uint32_t s_use = 0, p_use = 0;
-        uint32_t ring = 0;           // K/V ring fills before the current item
+        const uint32_t sbuf = tmem + kColS + 64 * x + lane_base;   // + b * kBN
+        const uint32_t tmem_o = tmem + kColO + 64 * x + lane_base;
+        uint32_t s_use[2] = {0, 0};
+        uint32_t nbar = 0;     // named barriers passed (same count in all 256 threads)
+        uint32_t tiles = 0;    // key tiles (= PVs) before the current item
         constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-            bool ok = true;
+        // named barrier among the 256 softmax threads; returns the abort
+        // snapshot taken after the previous one (identical in all threads)
+        auto exchange = [&]() -> bool {
+            named_bar_sync(2, 256);
+            const int stop = snap[(nbar + 1) & 1];
+            if (u == 0) snap[nbar & 1] = *abort_flag;
+            ++nbar;
+            return stop != 0;
+        };
+        bool stop = false;
+        for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
             const Work w = work_item(p, prefix, item);
             const int shift = w.lk - w.lq;
             const int t_row = r / p.group, g_row = r - t_row * p.group;
@@ -520,14 +540,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const int lim = p.causal ? min(w.lk, shift + qi + 1) : w.lk;  // keys [0, lim) visible
             const int64_t row_off =
                 (static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * hstride + (w.kvh * p.group + g_row) * kD;
-            uint16_t* dst = static_cast<uint16_t*>(p.out) + row_off;
+            uint16_t* dst = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
             if (w.ntiles == 0) {
                 // no visible key for any row of the item: output 0
-                if (x == 0 && row_valid)
-                    for (int c = 0; c < kD; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
+                if (row_valid)
+                    for (int c = 0; c < 64; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
                 continue;
             }
-            // ---- Q row -> tensor memory (group x: elements 64x .. 64x+63), zero past Lq ----
+            // ---- Q row -> tensor memory (warpgroup x: elements 64x .. 64x+63), zero past Lq ----
             {
                 uint32_t qw[32];
                 const uint4* src = reinterpret_cast<const uint4*>(p.q + row_off + 64 * x);
@@ -547,26 +567,27 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(q_full);
             }
-            float m = -INFINITY, l = 0.f;
-            int mine = 0;  // tiles this group took in the item
-            for (int t = x; t < w.ntiles && ok; t += 2) {
-                const int key0 = t * kBN;
-                ok = mbar_wait(s_full + 8 * x, s_use & 1u, p.status, abort_flag);
-                if (!ok) break;
-                ++s_use;
-                tc_fence_after();
-                // the scores of this tile; masked past this row's last visible
-                // key (only tiles that cross it); rows past Lq see nothing
+            float m = -INFINITY, l = 0.f;  // reference max (shared by both warpgroups), own partial sum
+            bool ok = true;
+            for (int t = 0; t < w.ntiles; ++t) {
+                const int b = t & 1;
+                const int key0 = t * kBN + 64 * x;  // first key of this thread's 64 columns
+                ok = ok && mbar_wait(s_full + 8 * b, s_use[b] & 1u, p.status, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                ++s_use[b];
                 float sv[64];
-                tmem_ld64(sbuf, sv);
-                const int vis = row_valid ? lim - key0 : 0;  // visible keys of this tile: [0, vis)
-                if (vis < kBN) {
+                float mx = -INFINITY;
+                const int vis = row_valid ? lim - key0 : 0;  // visible keys of these columns: [0, vis)
+                if (ok) {
+                    tc_fence_after();
+                    // the scores of this thread's 64 keys; masked past this row's
+                    // last visible key (only tiles that cross it); rows past Lq see nothing
+                    tmem_ld64(sbuf + b * kBN, sv);
+                    if (vis < 64) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (i >= vis) sv[i] = -INFINITY;
-                }
-                float mx;
-                {
+                        for (int i = 0; i < 64; ++i)
+                            if (i >= vis) sv[i] = -INFINITY;
+                    }
                     float m8[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) m8[j] = fmax3(sv[8 * j], sv[8 * j + 1], sv[8 * j + 2]);
@@ -577,44 +598,63 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
 #pragma unroll
                     for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], sv[8 * j + 7]);
                     mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-                    mx *= p.scale_log2;  // scale > 0: the max commutes with it
                 }
-                // lazy rescale: move the reference max only when it grows by > tau.
-                // O[x] is stable: the commit behind this tile's QK covered this
-                // group's previous PV.
-                if (mx > m + kTau) {
-                    const float a = ex2(m - mx);  // 0 when m = -inf
-                    if (mine > 0 && m != -INFINITY) {
-                        for (int c0 = 0; c0 < kD; c0 += 32) {
-                            float o[32];
-                            tmem_ld32(tmem_o + c0, o);
+                xch[((nbar & 1) * 2 + x) * kRows + r] = mx;
+                if (exchange()) {
+                    stop = true;
+                    break;
+                }
+                // the tile's row max (raw scores); scale > 0 commutes with max
+                mx = fmaxf(mx, xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r]) * p.scale_log2;
+                if (!ok) continue;
+                // lazy rescale: move the reference max only when it grows by > tau
+                // (the two threads of a row decide alike: same inputs).  The
+                // tensor-memory accesses are warp-wide, so a warp with any such
+                // row rescales its O rows (factor 1 for the others) once O holds
+                // PV(t-1).
+                const bool grow = mx > m + kTau;
+                const float a = grow ? ex2(m - mx) : 1.f;  // 0 when m = -inf
+                if (__any_sync(0xffffffffu, grow) && t > 0) {
+                    // PV(t-2) is complete (it precedes QK(t) in the tensor pipe),
+                    // so the wait below cannot alias an older phase
+                    ok = mbar_wait(o_done, (tiles + t - 1) & 1u, p.status, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) continue;
+                    tc_fence_after();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] *= a;
-                            tmem_st32(tmem_o + c0, o);
-                        }
+                    for (int c0 = 0; c0 < 64; c0 += 32) {
+                        float o[32];
+                        tmem_ld32(tmem_o + c0, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= a;
+                        tmem_st32(tmem_o + c0, o);
                     }
+                }
+                if (grow) {
                     l *= a;
                     m = mx;
                 }
                 // values past Lk in the last tile may hold anything: zero those
                 // V rows (after the tile landed) so zero weights never meet NaN
-                if (key0 + kBN > w.lk) {
-                    const uint32_t f = ring + t;
+                if (t * kBN + kBN > w.lk) {
+                    const uint32_t f = tiles + t;
                     ok = mbar_wait(kv_full + 8 * (f % kStages), (f / kStages) & 1u, p.status, abort_flag);
-                    if (!ok) break;
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) continue;
                     uint8_t* vt = sKV + (f % kStages) * kStageBytes + kKVTileBytes;
-                    const int first = max(0, w.lk - key0);
-                    for (int ci = r; ci < (kBN - first) * 16; ci += 128) {
+                    const int first = max(0, w.lk - t * kBN);
+                    for (int ci = u; ci < (kBN - first) * 16; ci += 256) {
                         const int rr = first + (ci >> 4), c = ci & 15;
-                        *reinterpret_cast<uint4*>(vt + (c >> 3) * (kKVTileBytes / 2) + sw128(rr, c & 7)) =
+                        *reinterpret_cast<uint4*>(vt + (c >> 3) * kBlkBytes + sw128(rr, c & 7)) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     fence_async_smem();
                 }
                 // p = 2^(s*scale - m): one FFMA and one exp2 per score (masked
-                // scores are -inf and give 0); the row sum; P over S in tensor
-                // memory as 16-bit pairs (bf16: hi at columns 0..31 and the
-                // remainder lo at 32..63, both truncated, ~16 bits together)
+                // scores are -inf and give 0); the partial row sum; P over S in
+                // tensor memory as 16-bit pairs (bf16: hi at columns 0..31 of
+                // this warpgroup's 64 and the remainder lo at 32..63, both
+                // truncated, ~16 bits together)
                 const float nb = m == -INFINITY ? 0.f : -m;
 #pragma unroll
                 for (int i = 0; i < 64; ++i) sv[i] = ex2(fmaf(sv[i], p.scale_log2, nb));
@@ -631,56 +671,40 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                     uint32_t hw[16], lw[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float a = sv[32 * h + 2 * j], b = sv[32 * h + 2 * j + 1];
+                        const float a = sv[32 * h + 2 * j], c = sv[32 * h + 2 * j + 1];
                         if constexpr (DT == PA_BF16) {
-                            hw[j] = hi_halves(a, b);
-                            lw[j] = hi_halves(a - __uint_as_float(hw[j] << 16), b - __uint_as_float(hw[j] & 0xffff0000u));
+                            hw[j] = hi_halves(a, c);
+                            lw[j] = hi_halves(a - __uint_as_float(hw[j] << 16), c - __uint_as_float(hw[j] & 0xffff0000u));
                         } else {
-                            hw[j] = pack2<DT>(a, b);
+                            hw[j] = pack2<DT>(a, c);
                         }
                     }
-                    tmem_st16(sbuf + 16 * h, hw);
-                    if constexpr (DT == PA_BF16) tmem_st16(sbuf + 32 + 16 * h, lw);
+                    tmem_st16(sbuf + b * kBN + 16 * h, hw);
+                    if constexpr (DT == PA_BF16) tmem_st16(sbuf + b * kBN + 32 + 16 * h, lw);
                 }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full + 8 * x);
-                ++p_use;
-                ++mine;
+                if (lane == 0) mbar_arrive(p_full + 8 * b);
             }
-            ring += w.ntiles;
-            // ---- epilogue: both groups' last PVs done, then merge by log-sum-exp ----
-            // (both groups always pass both barriers of an item, even after a
-            // failed wait, and decide together whether to go on)
-            if (ok && mine > 0) ok = mbar_wait(o_done + 8 * x, (p_use - 1) & 1u, p.status, abort_flag);
-            if (x == 1) {
-                stats[2 * r] = mine > 0 ? m : -INFINITY;
-                stats[2 * r + 1] = mine > 0 ? l : 0.f;
-            }
-            named_bar_sync(2, 256);
-            if (u == 0) *stop_word = *abort_flag;  // every wait of this item is behind us
-            if (x == 0 && ok) {
+            if (stop) break;
+            tiles += w.ntiles;
+            // ---- epilogue: the last PV done, row sums combined, O / l ----
+            // PV(n-3) is known complete; wait for PV(n-2), then PV(n-1), so that
+            // no wait aliases a phase two behind
+            if (w.ntiles > 1) ok = ok && mbar_wait(o_done, (tiles - 2) & 1u, p.status, abort_flag);
+            ok = ok && mbar_wait(o_done, (tiles - 1) & 1u, p.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            xch[((nbar & 1) * 2 + x) * kRows + r] = l;
+            if (exchange()) break;
+            if (ok) {
                 tc_fence_after();
-                const float m1 = stats[2 * r], l1 = stats[2 * r + 1];
-                const bool has1 = w.ntiles > 1;
-                const float M = fmaxf(m, m1);
-                const float a0 = M == -INFINITY ? 0.f : ex2(m - M);
-                const float a1 = (M == -INFINITY || !has1) ? 0.f : ex2(m1 - M);
-                const float L = l * a0 + l1 * a1;
+                const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
                 const float inv = L > 0.f ? 1.f / L : 0.f;
-                for (int c0 = 0; c0 < kD; c0 += 32) {
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 32) {
                     float o[32];
                     tmem_ld32(tmem_o + c0, o);
-                    if (has1) {
-                        float o1[32];
-                        tmem_ld32(tmem_o_other + c0, o1);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = o[i] * a0 + o1[i] * a1;
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= a0;
-                    }
                     if (row_valid) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
@@ -693,13 +717,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         }
                     }
                 }
+                // the next item's Q store and first PV overwrite tensor memory
+                // read here; its q_full / p_full arrivals order them after this
+                tc_fence_before();
             }
-            // the next item's Q store and first PVs overwrite tensor memory
-            // that this epilogue and the last QKs used
-            tc_fence_before();
-            named_bar_sync(3, 256);
-            tc_fence_after();
-            if (*stop_word) break;
         }
     }
     // ---- teardown: every role is done; free tensor memory ----
@@ -771,7 +792,7 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
     if (cache->kv_dtype != q_dtype) return PA_ERR_UNSUPPORTED;
     const int bs = cache->block_size;
     if (bs != 16 && bs != 32 && bs != 64) return PA_ERR_UNSUPPORTED;
-    if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
     const int64_t rows = cache->num_blocks * cache->num_kv_heads * bs;
     if (rows > INT32_MAX) return PA_ERR_UNSUPPORTED;
 
