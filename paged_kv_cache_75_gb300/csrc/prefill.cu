@@ -45,27 +45,26 @@ namespace {
 constexpr int kD = 128;              // head size
 constexpr int kBN = 128;             // keys per tile
 constexpr int kRows = 128;           // MMA M: query rows per item
-constexpr int kStages = 3;           // K/V ring depth
+constexpr int kStages = 3;           // depth of the K ring and of the V ring
 constexpr int kThreads = 384;        // 12 warps
 constexpr int kSoftWarp0 = 4;        // softmax warpgroups = warps 4..7 and 8..11
 constexpr uint32_t kTmemCols = 512;
-// tensor-memory columns: S[b] (fp32 scores of key tile b = t & 1, later
-// overwritten by the 16-bit weights P), O (fp32 accumulator), Q (16-bit, two
-// per column).  Softmax warpgroup x owns the key columns 64x .. 64x+63 of each
-// S and the value columns 64x .. 64x+63 of O.
+// tensor-memory columns: S[b] (fp32 scores of the key tiles t with t & 1 = b,
+// later overwritten by the 16-bit weights P), O (fp32 accumulator), Q (16-bit,
+// two per column)
 constexpr uint32_t kColS = 0;    // S[b] at b * kBN
 constexpr uint32_t kColO = 256;  // 128 columns
 constexpr uint32_t kColQ = 384;  // 64 columns
 
 // shared memory layout (bytes from the 1 KB-aligned base)
 constexpr int kBlkBytes = kBN * 128;           // 16 KB: one 64-column block of a K or V tile
-constexpr int kKVTileBytes = 2 * kBlkBytes;    // 32 KB
-constexpr int kStageBytes = 2 * kKVTileBytes;  // K then V
-constexpr int kOffKV = 0;
-constexpr int kOffBar = kOffKV + kStages * kStageBytes;
-constexpr int kNumBars = 2 * kStages + 2 * 2 + 3;
+constexpr int kTileBytes = 2 * kBlkBytes;      // 32 KB: a K or a V tile
+constexpr int kOffK = 0;                       // K ring
+constexpr int kOffV = kOffK + kStages * kTileBytes;  // V ring
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kNumBars = 4 * kStages + 3 * 2 + 2;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kOffXch = kOffMisc + 64;                   // [2 slots][2 groups][128 rows] floats
+constexpr int kOffXch = kOffMisc + 64;                   // [2 slots][2 warpgroups][128 rows] floats
 constexpr int kSmemBytes = kOffXch + 2 * 2 * kRows * 4;
 constexpr int kMaxSeqs = 6144;                           // prefix of query tiles: (B + 1) ints
 
@@ -195,6 +194,38 @@ __device__ __forceinline__ uint32_t hi_halves(float x, float y) {
     asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(d) : "r"(__float_as_uint(x)), "r"(__float_as_uint(y)));
     return d;
 }
+// packed fp32 pairs: one instruction for both halves
+__device__ __forceinline__ uint64_t f2pack(float x, float y) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 f2unpack(uint64_t r) {
+    float2 f;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(f.x), "=f"(f.y) : "l"(r));
+    return f;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// named barrier over n threads that also ORs a predicate across them
+__device__ __forceinline__ bool bar_red_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(pred ? 1u : 0u), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -273,14 +304,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 128B-swizzled tiles need 1 KB alignment; the launch adds 1 KB of slack
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* sKV = smem + kOffKV;
+    uint8_t* sK = smem + kOffK;
+    uint8_t* sV = smem + kOffV;
     const uint32_t bar0 = smem_addr(smem + kOffBar);
-    const uint32_t kv_full = bar0;                 // [kStages] TMA bytes
-    const uint32_t kv_empty = bar0 + 8 * kStages;  // [kStages] MMA commit after PV
-    const uint32_t s_full = bar0 + 16 * kStages;   // [2] MMA commit after QK into S[b]
+    const uint32_t k_full = bar0;                  // [kStages] TMA bytes of a K tile
+    const uint32_t k_empty = bar0 + 8 * kStages;   // [kStages] MMA commit after QK
+    const uint32_t v_full = bar0 + 16 * kStages;   // [kStages] TMA bytes of a V tile
+    const uint32_t v_empty = bar0 + 24 * kStages;  // [kStages] MMA commit after PV
+    const uint32_t s_full = bar0 + 32 * kStages;   // [2] MMA commit after QK into S[b]
     const uint32_t p_full = s_full + 16;           // [2] the 8 softmax warps: P[b] written
-    const uint32_t o_done = p_full + 16;           // MMA commit after each PV
-    const uint32_t q_full = o_done + 8;            // 8 softmax warps: Q in tensor memory
+    const uint32_t o_done = p_full + 16;           // [2] MMA commit after PV number g, on o_done[g & 1]
+    const uint32_t q_full = o_done + 16;           // 8 softmax warps: Q in tensor memory
     const uint32_t mma_done = q_full + 8;          // MMA commit at the very end
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
@@ -294,14 +328,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(kv_full + 8 * s, 1);
-            mbar_init(kv_empty + 8 * s, 1);
+            mbar_init(k_full + 8 * s, 1);
+            mbar_init(k_empty + 8 * s, 1);
+            mbar_init(v_full + 8 * s, 1);
+            mbar_init(v_empty + 8 * s, 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(s_full + 8 * s, 1);
             mbar_init(p_full + 8 * s, 8);
+            mbar_init(o_done + 8 * s, 1);
         }
-        mbar_init(o_done, 1);
         mbar_init(q_full, 8);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
@@ -358,6 +394,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     const int64_t hstride = static_cast<int64_t>(p.num_heads) * kD;  // elements per q/out row
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
+        // K and V have rings of their own: a K stage is free again once its QK
+        // is done, long before the PV of the same tile has used V.
         uint32_t fill = 0, stage = 0, phase = 0;
         bool ok = true;
         const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
@@ -385,25 +423,26 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 const int my_id = __shfl_sync(0xffffffffu, id, (pg0 + (lane & 7)) & 31);
                 const bool have = lane < ppt && my_id >= 0;
                 const uint32_t bytes =
-                    static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, have))) * 4u * p.block_size * kD;
-                if (lane == 0) ok = mbar_wait(kv_empty + 8 * stage, phase ^ 1u, p.status, abort_flag);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (ok) {
-                    const uint32_t bar = kv_full + 8 * stage;
+                    static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, have))) * 2u * p.block_size * kD;
+                const int row = (my_id * p.num_kv_heads + w.kvh) * p.block_size;
+                const uint32_t off = lane * p.block_size * 128;  // page lane's rows in a 64-column block
+#pragma unroll
+                for (int kv = 0; kv < 2; ++kv) {
+                    const uint32_t full = (kv == 0 ? k_full : v_full) + 8 * stage;
+                    const uint32_t empty = (kv == 0 ? k_empty : v_empty) + 8 * stage;
+                    if (lane == 0) ok = ok && mbar_wait(empty, phase ^ 1u, p.status, abort_flag);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
                     if (lane == 0) {
-                        if (bytes) mbar_expect_tx(bar, bytes);
-                        else mbar_arrive(bar);
+                        if (bytes) mbar_expect_tx(full, bytes);
+                        else mbar_arrive(full);
                     }
                     __syncwarp();
                     if (have) {
-                        // one lane per page: 4 copies of bs rows x 64 columns
-                        const uint32_t kdst = smem_addr(sKV + stage * kStageBytes) + lane * p.block_size * 128;
-                        const uint32_t vdst = kdst + kKVTileBytes;
-                        const int row = (my_id * p.num_kv_heads + w.kvh) * p.block_size;
-                        tma_load_2d(kdst, &map_k, 0, row, bar);
-                        tma_load_2d(kdst + kBlkBytes, &map_k, 64, row, bar);
-                        tma_load_2d(vdst, &map_v, 0, row, bar);
-                        tma_load_2d(vdst + kBlkBytes, &map_v, 64, row, bar);
+                        const uint32_t dst = smem_addr((kv == 0 ? sK : sV) + stage * kTileBytes) + off;
+                        const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
+                        tma_load_2d(dst, map, 0, row, full);
+                        tma_load_2d(dst + kBlkBytes, map, 64, row, full);
                     }
                 }
                 ++fill;
@@ -418,32 +457,34 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const uint64_t t0 = global_timer_ns();
             const uint32_t first = fill > kStages ? fill - kStages : 0u;
             for (uint32_t f = first; f < fill; ++f)
-                while (!mbar_try_wait(kv_full + 8 * (f % kStages), (f / kStages) & 1u))
-                    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+                for (int kv = 0; kv < 2; ++kv)
+                    while (!mbar_try_wait((kv == 0 ? k_full : v_full) + 8 * (f % kStages), (f / kStages) & 1u))
+                        if (global_timer_ns() - t0 > kWaitLimitNs) break;
         }
     } else if (warp == 1) {
         // -------------------------------- MMA ---------------------------------
         // per item: S[0] = Q K(0)^T, S[1] = Q K(1)^T, then for each tile t:
-        // O (+)= P[t&1] V(t) once both softmax warpgroups have written P over
-        // S, followed by S[t&1] = Q K(t+2)^T.  One thread issues everything,
-        // so the tensor pipe sees each PV before the QK that overwrites its P,
-        // and a commit after QK(t+2) also covers PV(t).
+        // O (+)= P[t&1] V(t) once both softmax warpgroups have written P over S, followed
+        // by S[t&1] = Q K(t+2)^T.  One thread issues everything, so the tensor
+        // pipe sees each PV before the QK that overwrites its P, and a commit
+        // after QK(t+2) also covers PV(t).
         const uint32_t id_qk = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kBN, 0);
         const uint32_t id_pv = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kD, 1);
         // descriptors are built once; a k-step only adds a constant to the
         // start-address field (bits 0..13, in 16-byte units)
-        const uint64_t dk = smem_desc(smem_addr(sKV), 16, 1024);
-        const uint64_t dv = smem_desc(smem_addr(sKV + kKVTileBytes), kBlkBytes, 1024);
-        uint32_t qk_stage = 0, qk_phase = 0;  // ring position of the next QK
-        uint32_t pv_stage = 0;                // ring position of the next PV
-        uint32_t p_use[2] = {0, 0};           // P[b] handed over so far
-        uint32_t q_cnt = 0;                   // items with tiles
+        const uint64_t dk = smem_desc(smem_addr(sK), 16, 1024);
+        const uint64_t dv = smem_desc(smem_addr(sV), kBlkBytes, 1024);
+        uint32_t k_stage = 0, k_phase = 0;  // K ring position of the next QK
+        uint32_t v_stage = 0, v_phase = 0;  // V ring position of the next PV
+        uint32_t p_use[2] = {0, 0};         // P[b] handed over so far
+        uint32_t pv_count = 0;              // PVs issued so far (all items)
+        uint32_t q_cnt = 0;                 // items with tiles
         bool ok = true;
         auto issue_qk = [&](int t) -> bool {
-            if (!mbar_wait(kv_full + 8 * qk_stage, qk_phase, p.status, abort_flag)) return false;
+            if (!mbar_wait(k_full + 8 * k_stage, k_phase, p.status, abort_flag)) return false;
             tc_fence_after();
             if (lane == 0) {
-                const uint64_t dks = dk + qk_stage * (kStageBytes >> 4);
+                const uint64_t dks = dk + k_stage * (kTileBytes >> 4);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
                     // Q: 8 columns per 16-element k-step; K: 32 bytes per k-step in a 64-column block
@@ -451,11 +492,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                                dks + ((k / 4) * (kBlkBytes >> 4) + (k % 4) * 2), id_qk, k > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full + 8 * (t & 1));
+                mma_commit(k_empty + 8 * k_stage);
             }
             __syncwarp();
-            if (++qk_stage == kStages) {
-                qk_stage = 0;
-                qk_phase ^= 1u;
+            if (++k_stage == kStages) {
+                k_stage = 0;
+                k_phase ^= 1u;
             }
             return true;
         };
@@ -468,28 +510,33 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             if (ok && w.ntiles > 1) ok = issue_qk(1);
             for (int t = 0; t < w.ntiles && ok; ++t) {
                 const int y = t & 1;
-                ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag);
+                ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag) &&
+                     mbar_wait(v_full + 8 * v_stage, v_phase, p.status, abort_flag);
                 if (!ok) break;
                 ++p_use[y];
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint64_t dvs = dv + pv_stage * (kStageBytes >> 4);
+                    const uint64_t dvs = dv + v_stage * (kTileBytes >> 4);
                     constexpr int kParts = DT == PA_BF16 ? 2 : 1;  // bf16: hi and lo weights
 #pragma unroll
                     for (int part = 0; part < kParts; ++part) {
 #pragma unroll
                         for (int j = 0; j < kBN / 16; ++j) {
-                            // keys 16j..16j+15: P of warpgroup j/4 at 8 columns (hi at +0, lo at +32);
+                            // keys 16j..16j+15: P at 8 columns of half j/4 (hi at +0, lo at +32);
                             // V: 2048 bytes per 16 keys
                             mma_f16_ts(tmem + kColO, tmem + kColS + y * kBN + (j / 4) * 64 + part * 32 + (j % 4) * 8,
                                        dvs + j * (2048 >> 4), id_pv, (t > 0 || part > 0 || j > 0) ? 1u : 0u);
                         }
                     }
-                    mma_commit(kv_empty + 8 * pv_stage);
-                    mma_commit(o_done);
+                    mma_commit(v_empty + 8 * v_stage);
+                    mma_commit(o_done + 8 * (pv_count & 1u));
                 }
                 __syncwarp();
-                if (++pv_stage == kStages) pv_stage = 0;
+                ++pv_count;
+                if (++v_stage == kStages) {
+                    v_stage = 0;
+                    v_phase ^= 1u;
+                }
                 if (t + 2 < w.ntiles) ok = issue_qk(t + 2);
             }
         }
@@ -505,12 +552,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     } else if (warp >= kSoftWarp0) {
         // ------------------------------ softmax -------------------------------
         // Both warpgroups work on every key tile: warpgroup x takes keys
-        // 64x .. 64x+63.  Per tile they swap their row maxima through shared
-        // memory (one named barrier), so both use the same reference max m
-        // and make the same lazy-rescale decision; each keeps its own partial
-        // row sum.  Every decision to stop is taken from an abort snapshot
-        // written right after the previous barrier, so all 256 threads pass
-        // the same sequence of named barriers.
+        // 64x .. 64x+63 of S[t&1] and the value columns 64x .. 64x+63 of O, row
+        // r = its tensor-memory lane.  Both use one reference max m per row.
+        // Fast path: weights against the current m, and a barrier that ORs
+        // "this row's partial sum left the safe range" over all 256 threads;
+        // only then (and on an item's first tile, where m is -inf) do both
+        // warpgroups take the tile's true row max, swap it through shared
+        // memory, move m, rescale O and recompute.  Between such events the
+        // weights may grow up to 2^58 against m, well inside fp32 and bf16
+        // range, so no precision is lost.  Every thread of both warpgroups
+        // passes the same barriers whatever its waits returned, and stops only
+        // on an abort snapshot taken right after the previous barrier.
         const int x = (warp - kSoftWarp0) >> 2;   // warpgroup
         const int u = tid - kSoftWarp0 * 32;       // 0..255 over both warpgroups
         const int r = u & 127;                     // row of the tile = tensor-memory lane
@@ -518,13 +570,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         const uint32_t sbuf = tmem + kColS + 64 * x + lane_base;   // + b * kBN
         const uint32_t tmem_o = tmem + kColO + 64 * x + lane_base;
         uint32_t s_use[2] = {0, 0};
-        uint32_t nbar = 0;     // named barriers passed (same count in all 256 threads)
+        uint32_t nbar = 0;     // barriers passed (same count in all 256 threads)
         uint32_t tiles = 0;    // key tiles (= PVs) before the current item
-        constexpr float kTau = 8.f;  // lazy-rescale threshold (log2 units)
-        // named barrier among the 256 softmax threads; returns the abort
-        // snapshot taken after the previous one (identical in all threads)
-        auto exchange = [&]() -> bool {
-            named_bar_sync(2, 256);
+        constexpr float kSafe = 18446744073709551616.f;  // 2^64: partial sums below it need no new max
+        // after every barrier among the 256: the abort snapshot of the previous one
+        auto snapshot = [&]() -> bool {
             const int stop = snap[(nbar + 1) & 1];
             if (u == 0) snap[nbar & 1] = *abort_flag;
             ++nbar;
@@ -567,81 +617,143 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 __syncwarp();
                 if (lane == 0) mbar_arrive(q_full);
             }
-            float m = -INFINITY, l = 0.f;  // reference max (shared by both warpgroups), own partial sum
+            float m = -INFINITY, l = 0.f;  // reference max (same in both warpgroups), own partial sum
             bool ok = true;
+            const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
             for (int t = 0; t < w.ntiles; ++t) {
                 const int b = t & 1;
                 const int key0 = t * kBN + 64 * x;  // first key of this thread's 64 columns
+                const int vis = row_valid ? lim - key0 : 0;  // visible keys of these columns: [0, vis)
                 ok = ok && mbar_wait(s_full + 8 * b, s_use[b] & 1u, p.status, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 ++s_use[b];
-                float sv[64];
-                float mx = -INFINITY;
-                const int vis = row_valid ? lim - key0 : 0;  // visible keys of these columns: [0, vis)
+                float e[64];
+                float sum = 0.f;
+                bool over = false;
                 if (ok) {
                     tc_fence_after();
-                    // the scores of this thread's 64 keys; masked past this row's
-                    // last visible key (only tiles that cross it); rows past Lq see nothing
-                    tmem_ld64(sbuf + b * kBN, sv);
+                    tmem_ld64(sbuf + b * kBN, e);
                     if (vis < 64) {
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
-                            if (i >= vis) sv[i] = -INFINITY;
+                            if (i >= vis) e[i] = -INFINITY;
                     }
-                    float m8[8];
+                    if (m == -INFINITY) {
+                        // no reference yet: the slow path, unless these columns
+                        // are all masked for this row (weights 0)
+                        over = vis > 0;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) m8[j] = fmax3(sv[8 * j], sv[8 * j + 1], sv[8 * j + 2]);
+                        for (int i = 0; i < 64; ++i) e[i] = 0.f;
+                    } else {
+                        // p = 2^(s*scale - m): one packed FFMA per pair and one exp2
+                        // per score (masked scores are -inf and give 0)
+                        const uint64_t nb2 = f2pack(-m, -m);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], sv[8 * j + 3], sv[8 * j + 4]);
+                        for (int i = 0; i < 64; i += 2) {
+                            const float2 a = f2unpack(f2fma(f2pack(e[i], e[i + 1]), sc2, nb2));
+                            e[i] = ex2(a.x);
+                            e[i + 1] = ex2(a.y);
+                        }
+                        uint64_t s8[4];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], sv[8 * j + 5], sv[8 * j + 6]);
+                        for (int j = 0; j < 4; ++j)
+                            s8[j] = f2add(f2add(f2pack(e[2 * j], e[2 * j + 1]), f2pack(e[2 * j + 8], e[2 * j + 9])),
+                                          f2add(f2pack(e[2 * j + 16], e[2 * j + 17]), f2pack(e[2 * j + 24], e[2 * j + 25])));
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], sv[8 * j + 7]);
-                    mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+                        for (int j = 0; j < 4; ++j)
+                            s8[j] = f2add(s8[j], f2add(f2add(f2pack(e[2 * j + 32], e[2 * j + 33]), f2pack(e[2 * j + 40], e[2 * j + 41])),
+                                                       f2add(f2pack(e[2 * j + 48], e[2 * j + 49]), f2pack(e[2 * j + 56], e[2 * j + 57]))));
+                        const float2 s01 = f2unpack(f2add(f2add(s8[0], s8[1]), f2add(s8[2], s8[3])));
+                        sum = s01.x + s01.y;
+                        over = !(sum < kSafe);  // also catches inf and NaN
+                    }
                 }
-                xch[((nbar & 1) * 2 + x) * kRows + r] = mx;
-                if (exchange()) {
+                const bool any = bar_red_or(2, 256, over);
+                if (snapshot()) {
                     stop = true;
                     break;
                 }
-                // the tile's row max (raw scores); scale > 0 commutes with max
-                mx = fmaxf(mx, xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r]) * p.scale_log2;
-                if (!ok) continue;
-                // lazy rescale: move the reference max only when it grows by > tau
-                // (the two threads of a row decide alike: same inputs).  The
-                // tensor-memory accesses are warp-wide, so a warp with any such
-                // row rescales its O rows (factor 1 for the others) once O holds
-                // PV(t-1).
-                const bool grow = mx > m + kTau;
-                const float a = grow ? ex2(m - mx) : 1.f;  // 0 when m = -inf
-                if (__any_sync(0xffffffffu, grow) && t > 0) {
-                    // PV(t-2) is complete (it precedes QK(t) in the tensor pipe),
-                    // so the wait below cannot alias an older phase
-                    ok = mbar_wait(o_done, (tiles + t - 1) & 1u, p.status, abort_flag);
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) continue;
-                    tc_fence_after();
+                if (any) {
+                    // slow path (all 256 threads): the tile's true row max over both
+                    // halves, a new reference, O and l rescaled, weights recomputed
+                    float mx = -INFINITY;
+                    if (ok) {
+                        tmem_ld64(sbuf + b * kBN, e);
+                        if (vis < 64) {
 #pragma unroll
-                    for (int c0 = 0; c0 < 64; c0 += 32) {
-                        float o[32];
-                        tmem_ld32(tmem_o + c0, o);
+                            for (int i = 0; i < 64; ++i)
+                                if (i >= vis) e[i] = -INFINITY;
+                        }
+                        float m8[8];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= a;
-                        tmem_st32(tmem_o + c0, o);
+                        for (int j = 0; j < 8; ++j) m8[j] = fmax3(e[8 * j], e[8 * j + 1], e[8 * j + 2]);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], e[8 * j + 3], e[8 * j + 4]);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) m8[j] = fmax3(m8[j], e[8 * j + 5], e[8 * j + 6]);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) m8[j] = fmaxf(m8[j], e[8 * j + 7]);
+                        mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
                     }
+                    xch[((nbar & 1) * 2 + x) * kRows + r] = mx;
+                    named_bar_sync(3, 256);
+                    if (snapshot()) {
+                        stop = true;
+                        break;
+                    }
+                    if (!ok) continue;
+                    // scale > 0: the max commutes with it
+                    mx = fmaxf(mx, xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r]) * p.scale_log2;
+                    const bool grow = mx > m;
+                    const float a = grow ? ex2(m - mx) : 1.f;  // 0 when m = -inf
+                    // O holds PV(0..t-1) against m: rescale it (warp-wide accesses,
+                    // factor 1 for other rows) once PV(t-1) is complete.  PV number g
+                    // completes a phase of o_done[g & 1]; the previous phase of that
+                    // barrier belongs to PV(t-3), complete since it precedes QK(t).
+                    if (__any_sync(0xffffffffu, grow) && t > 0) {
+                        const uint32_t g = tiles + t - 1;
+                        ok = mbar_wait(o_done + 8 * (g & 1u), (g >> 1) & 1u, p.status, abort_flag);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) continue;
+                        tc_fence_after();
+#pragma unroll
+                        for (int c0 = 0; c0 < 64; c0 += 32) {
+                            float o[32];
+                            tmem_ld32(tmem_o + c0, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= a;
+                            tmem_st32(tmem_o + c0, o);
+                        }
+                    }
+                    if (grow) {
+                        l *= a;
+                        m = mx;
+                    }
+                    const float nb = m == -INFINITY ? 0.f : -m;
+                    const uint64_t nb2 = f2pack(nb, nb);
+#pragma unroll
+                    for (int i = 0; i < 64; i += 2) {
+                        const float2 q2 = f2unpack(f2fma(f2pack(e[i], e[i + 1]), sc2, nb2));
+                        e[i] = ex2(q2.x);
+                        e[i + 1] = ex2(q2.y);
+                    }
+                    float r8[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r8[j] = (e[j] + e[j + 8]) + (e[j + 16] + e[j + 24]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) r8[j] += (e[j + 32] + e[j + 40]) + (e[j + 48] + e[j + 56]);
+                    sum = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
                 }
-                if (grow) {
-                    l *= a;
-                    m = mx;
-                }
+                if (!ok) continue;
+                l += sum;
                 // values past Lk in the last tile may hold anything: zero those
                 // V rows (after the tile landed) so zero weights never meet NaN
                 if (t * kBN + kBN > w.lk) {
                     const uint32_t f = tiles + t;
-                    ok = mbar_wait(kv_full + 8 * (f % kStages), (f / kStages) & 1u, p.status, abort_flag);
+                    ok = mbar_wait(v_full + 8 * (f % kStages), (f / kStages) & 1u, p.status, abort_flag);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) continue;
-                    uint8_t* vt = sKV + (f % kStages) * kStageBytes + kKVTileBytes;
+                    uint8_t* vt = sV + (f % kStages) * kTileBytes;
                     const int first = max(0, w.lk - t * kBN);
                     for (int ci = u; ci < (kBN - first) * 16; ci += 256) {
                         const int rr = first + (ci >> 4), c = ci & 15;
@@ -650,31 +762,20 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                     }
                     fence_async_smem();
                 }
-                // p = 2^(s*scale - m): one FFMA and one exp2 per score (masked
-                // scores are -inf and give 0); the partial row sum; P over S in
-                // tensor memory as 16-bit pairs (bf16: hi at columns 0..31 of
-                // this warpgroup's 64 and the remainder lo at 32..63, both
+                // P over S in tensor memory as 16-bit pairs (bf16: hi at columns
+                // 0..31 of this warpgroup's 64 and the remainder lo at 32..63, both
                 // truncated, ~16 bits together)
-                const float nb = m == -INFINITY ? 0.f : -m;
-#pragma unroll
-                for (int i = 0; i < 64; ++i) sv[i] = ex2(fmaf(sv[i], p.scale_log2, nb));
-                {
-                    float r8[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) r8[j] = (sv[j] + sv[j + 8]) + (sv[j + 16] + sv[j + 24]);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) r8[j] += (sv[j + 32] + sv[j + 40]) + (sv[j + 48] + sv[j + 56]);
-                    l += ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
-                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {  // keys 32h .. 32h+31 = columns 16h .. 16h+15
                     uint32_t hw[16], lw[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float a = sv[32 * h + 2 * j], c = sv[32 * h + 2 * j + 1];
+                        const float a = e[32 * h + 2 * j], c = e[32 * h + 2 * j + 1];
                         if constexpr (DT == PA_BF16) {
                             hw[j] = hi_halves(a, c);
-                            lw[j] = hi_halves(a - __uint_as_float(hw[j] << 16), c - __uint_as_float(hw[j] & 0xffff0000u));
+                            const float2 lo = f2unpack(f2add(f2pack(a, c), f2pack(-__uint_as_float(hw[j] << 16),
+                                                                                -__uint_as_float(hw[j] & 0xffff0000u))));
+                            lw[j] = hi_halves(lo.x, lo.y);
                         } else {
                             hw[j] = pack2<DT>(a, c);
                         }
@@ -690,13 +791,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             if (stop) break;
             tiles += w.ntiles;
             // ---- epilogue: the last PV done, row sums combined, O / l ----
-            // PV(n-3) is known complete; wait for PV(n-2), then PV(n-1), so that
-            // no wait aliases a phase two behind
-            if (w.ntiles > 1) ok = ok && mbar_wait(o_done, (tiles - 2) & 1u, p.status, abort_flag);
-            ok = ok && mbar_wait(o_done, (tiles - 1) & 1u, p.status, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
+            // both warpgroups saw QK(n-1), so PV(n-3) -- the previous phase of
+            // the last PV's barrier -- is complete and the wait cannot alias
+            {
+                const uint32_t g = tiles - 1;
+                ok = ok && mbar_wait(o_done + 8 * (g & 1u), (g >> 1) & 1u, p.status, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+            }
             xch[((nbar & 1) * 2 + x) * kRows + r] = l;
-            if (exchange()) break;
+            named_bar_sync(3, 256);
+            if (snapshot()) break;
             if (ok) {
                 tc_fence_after();
                 const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
