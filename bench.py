@@ -46,17 +46,39 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture, keyed by workload, with the hash of the kernel source it was taken
-# on; reported only while the source is unchanged.
-NCU_TRAFFIC = {}
+# capture (`--set full`, one launch after 3 warm-up steps), keyed by workload
+# and the hash of the kernel source it was taken on; reported only while that
+# source is unchanged.
+NCU_TRAFFIC = {
+    ("mha", "07c6a73572c19639"): 945_729_792,
+    ("gqa", "07c6a73572c19639"): 1_003_785_472,
+    ("long", "07c6a73572c19639"): 1_748_673_610,
+    ("mixed", "0932f6a3353bb5b1"): 1_314_560_216,
+}
+L2_BYTES = 129 * 1024 * 1024
+DECODE_SOURCES = ("decode_impl.cuh", "decode_launch.cuh", "decode_api.cu", "common.cuh")
+PREFILL_SOURCES = ("prefill.cu", "common.cuh", "launch.h")
 
 
-def kernel_source_hash():
+def kernel_source_hash(files=DECODE_SOURCES):
     h = hashlib.sha256()
-    for f in ("decode_impl.cuh", "decode_launch.cuh", "decode_api.cu", "common.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "paged_kv_cache_75_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2 between timed iterations when the
+    inputs alone would fit in L2; the flush itself is outside every timed
+    interval."""
+
+    def __init__(self, device, needed):
+        self.buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=device) if needed else None
+
+    def __call__(self):
+        if self.buf is not None:
+            self.buf.fill_(1)
 
 
 def measured_peaks():
@@ -293,27 +315,34 @@ def build_workload(name, device, num_seqs=None, pool_blocks=None):
     raise ValueError(name)
 
 
-def timed_decode(step: DecodeStep, steps, warmup, world):
+def timed_decode(step: DecodeStep, steps, warmup, world, flush):
+    """Returns (total ms over the timed steps, mean decode-kernel ms, clocks).
+    With an L2 flush, every step is timed on its own (write + decode) and the
+    flush runs between the timed intervals."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         step.write()
         step.decode()
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    whole = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         start.record(stream)
         for i in range(steps):
+            flush()
+            whole[i][0].record(stream)
             step.write()
             evs[i][0].record(stream)
             step.decode()
             evs[i][1].record(stream)
+            whole[i][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
     barrier(world)
-    total_ms = start.elapsed_time(end)
+    total_ms = sum(a.elapsed_time(b) for a, b in whole) if flush.buf is not None else start.elapsed_time(end)
     decode_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
     st = int(step.status.item())
     if st != 0:
@@ -399,7 +428,8 @@ def run_prefill(args, case, wname, dev, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16->f32",
+        "dtype": {0: "f16", 1: "bf16"}[case.q_dtype],
+        "accumulate": "f32",
         "data": "synthetic",
         "config": {"workload": wname, "num_seqs": step.B, "num_heads": case.num_heads,
                    "num_kv_heads": case.num_kv_heads, "head_size": case.head_size, "block_size": case.block_size,
@@ -414,9 +444,12 @@ def run_prefill(args, case, wname, dev, rank, world):
         "gpu_launches": step.launches_per_step * args.steps,
         "roofline": {"bound": "tensor", "kernel": "pa_prefill_varlen", "achieved": round(achieved, 2),
                      "peak": tflops_sustained, "unit": "TFLOP/s", "frac": round(achieved / tflops_sustained, 4),
-                     "peak_kind": "of %s (bf16 dense, sustained)" % peak_kind, "traffic": None,
-                     "prefill_ms": round(main_ms, 5)},
+                     "peak_kind": "of %s (bf16 dense, sustained)" % peak_kind,
+                     "traffic": NCU_TRAFFIC.get(("mixed", kernel_source_hash(PREFILL_SOURCES))),
+                     "prefill_ms": round(main_ms, 5), "kernel_src": kernel_source_hash(PREFILL_SOURCES)},
     }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(case)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -495,6 +528,59 @@ def cpu_baseline(case, budget_s=10.0):
                       % (len(idx), case.num_seqs, sample_bytes / 1e6, reps, spent)}
 
 
+def prefill_sample(case, rows_per_prefill=16, decode_every=6):
+    """A valid sub-batch of a varlen case: the last rows of every prefill
+    sequence (bottom-right alignment keeps them exact) and every k-th decode
+    sequence.  Returns (q codes, table, cu_q, cu_k, visible pairs)."""
+    lq = np.asarray(case.meta["query_lens"], np.int64)
+    lk = np.asarray(case.meta["key_lens"], np.int64)
+    n_pre = int(case.meta["n_prefill"])
+    cu_q = case.cu_seq_lens_q.cpu().numpy()
+    q_bits = W.as_bits(case.q)
+    bt = case.block_table.cpu().numpy()
+    seqs = list(range(n_pre)) + list(range(n_pre, len(lq), decode_every))
+    rows, sq, sk, tab = [], [0], [0], []
+    pairs = 0
+    for b in seqs:
+        r = int(min(lq[b], rows_per_prefill))
+        rows.extend(range(int(cu_q[b + 1]) - r, int(cu_q[b + 1])))
+        sq.append(sq[-1] + r)
+        sk.append(sk[-1] + int(lk[b]))
+        tab.append(bt[b])
+        i = np.arange(lq[b] - r, lq[b])
+        pairs += int(np.minimum(lk[b], lk[b] - lq[b] + i + 1).clip(min=0).sum())
+    return (q_bits[np.asarray(rows)], np.stack(tab), np.asarray(sq, np.int32), np.asarray(sk, np.int32), pairs)
+
+
+def oracle_prefill_seconds(case, sample, nthreads, kc, vc):
+    import oracle
+    qs, tab, sq, sk, _ = sample
+    t0 = time.perf_counter()
+    _, _, rc = oracle.prefill(qs, case.q_dtype, kc, vc, case.kv_dtype, tab, sq, sk, case.scale, True,
+                              nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    assert rc == 0
+    return dt
+
+
+def cpu_baseline_prefill(case, budget_s=10.0):
+    """The oracle's varlen prefill, as it stands, on all host cores over a
+    bounded sub-batch of the same workload, in the metric's unit."""
+    import oracle
+    n = oracle.num_threads(os.cpu_count() or 1)
+    kc, vc = W.as_bits(case.k_cache), W.as_bits(case.v_cache)
+    sample = prefill_sample(case)
+    flops = 4 * case.head_size * case.num_heads * sample[4]
+    reps, spent = 0, 0.0
+    while spent < budget_s and reps < 50:
+        spent += oracle_prefill_seconds(case, sample, n, kc, vc)
+        reps += 1
+    return {"value": round(flops * reps / spent / 1e12, 6), "unit": "TFLOP/s", "cores": n, "kind": "oracle",
+            "sample": "oracle varlen prefill (fp64) over the last 16 query rows of each prefill sequence and "
+                      "every 6th decode sequence (%d rows, %.2f GFLOP), %d passes in %.1f s"
+                      % (int(sample[2][-1]), flops / 1e9, reps, spent)}
+
+
 # ---------------------------------------------------------------------------
 def run_ours(args):
     rank, local_rank, world = dist_env()
@@ -511,7 +597,10 @@ def run_ours(args):
             dist.destroy_process_group()
         return
     step = DecodeStep(case, dev, args.partition_size, wname)
-    total_ms, decode_ms, clocks = timed_decode(step, args.steps, args.warmup, world)
+    # the K/V a step reads, plus everything else it touches
+    small = step.kv_bytes + case.q.numel() * case.q.element_size() * 2 < L2_BYTES
+    flush = L2Flush(dev, small)
+    total_ms, decode_ms, clocks = timed_decode(step, args.steps, args.warmup, world, flush)
     total_ms, kv_sum = aggregate(total_ms, float(step.kv_bytes) * args.steps, world)
     seqs_sum = aggregate(0.0, float(step.B) * args.steps, world)[1]
     ms_per_step = total_ms / args.steps
@@ -540,7 +629,9 @@ def run_ours(args):
                    "num_kv_heads": case.num_kv_heads, "head_size": case.head_size, "block_size": case.block_size,
                    "num_blocks": case.num_blocks, "kv_bytes_per_step": step.kv_bytes,
                    "partition_size": args.partition_size or 512,
-                   "l2": "inputs larger than L2 (%.2f GB of K/V read per step > 129 MB L2)" % (step.kv_bytes / 1e9),
+                   "l2": ("L2 flushed between timed steps (%.3f MB of K/V per step < 129 MB L2; each step "
+                          "timed on its own)" % (step.kv_bytes / 1e6)) if small else
+                         "inputs larger than L2 (%.2f GB of K/V read per step > 129 MB L2)" % (step.kv_bytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
         "seqs_per_s_per_layer": round(seqs_sum / (total_ms / 1e3), 1),
         "hbm_frac_of_8000": round(value / world / 8000.0, 4),
@@ -572,6 +663,29 @@ def run_reference(args):
     case, wname = build_workload(args.workload, "cpu")
     cores = os.cpu_count() or 1
     n = oracle.num_threads(cores)
+    if args.workload == "mixed":
+        kc, vc = W.as_bits(case.k_cache), W.as_bits(case.v_cache)
+        sample = prefill_sample(case, rows_per_prefill=1, decode_every=12)
+        flops = 4 * case.head_size * case.num_heads * sample[4]
+        for _ in range(args.warmup):
+            oracle_prefill_seconds(case, sample, n, kc, vc)
+        spent = 0.0
+        for _ in range(args.steps):
+            spent += oracle_prefill_seconds(case, sample, n, kc, vc)
+        value = flops * args.steps / spent / 1e12
+        desc = ("oracle varlen prefill (fp64) over the last query row of each prefill sequence and every "
+                "12th decode sequence (%.2f GFLOP) per step" % (flops / 1e9))
+        print(json.dumps({
+            "impl": "reference", "metric": "paged-attn varlen prefill TFLOP/s (causal, % of GB300 bf16 tensor peak)",
+            "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(spent / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wname, "num_seqs": case.num_seqs, "sampled_rows": int(sample[2][-1])},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": n, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
     q_bits, kc, vc = W.as_bits(case.q), W.as_bits(case.k_cache), W.as_bits(case.v_cache)
     bt = case.block_table.numpy()
     lens = case.seq_lens.numpy()
