@@ -59,7 +59,10 @@ struct DecodeParams {
 
 template <int QDT, int KVDT, int D, int G, int BS>
 struct DecodeCfg {
-    static constexpr int GW = G < 4 ? G : 4;          // query heads per consumer warp
+    // query heads per consumer warp: two for G = 4 (fewer registers, three
+    // CTAs per SM hide more latency), four for G = 8, where E4M3 conversions
+    // are shared by more heads
+    static constexpr int GW = G == 8 ? 4 : (G < 2 ? G : 2);
     static constexpr int HG = G / GW;                 // head groups (warp sets)
     static constexpr int TW = 4 / HG;                 // token warps per head group
     static constexpr int NCW = TW * HG;               // consumer warps (4)
