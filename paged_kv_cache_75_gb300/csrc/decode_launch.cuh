@@ -22,7 +22,10 @@ pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     using C = DecodeCfg<QDT, KVDT, D, G, BS>;
     const int other = static_cast<int>(DecodeSmem::make(0, C::STAGE_BYTES, C::QBYTES, C::MERGE_FLOATS,
                                                         p.num_seqs).total) + 2 * 8 * 8 + 64;
-    p.stages = decode_stages(C::STAGE_BYTES, other, C::MAX_REGS <= 112 ? 3 : 2);
+    // CTAs an SM holds under the register cap (65536 registers per SM)
+    constexpr int kCtas = 65536 / (C::THREADS * C::MAX_REGS) < 1 ? 1
+                          : (65536 / (C::THREADS * C::MAX_REGS) > 4 ? 4 : 65536 / (C::THREADS * C::MAX_REGS));
+    p.stages = decode_stages(C::STAGE_BYTES, other, kCtas);
     const DecodeSmem L = DecodeSmem::make(p.stages, C::STAGE_BYTES, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
     const int smem = static_cast<int>(L.total) + 1024;  // slack for the 1 KB base alignment
     if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
