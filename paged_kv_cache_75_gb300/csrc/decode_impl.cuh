@@ -29,6 +29,8 @@
 //  * every mbarrier wait is bounded (PA_ERR_TIMEOUT, no hang).
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace pa {
@@ -504,135 +506,143 @@ paged_decode_kernel(const DecodeParams p) {
             const uint8_t* Kp = ring + stage * C::STAGE_BYTES + lane_off;
             const uint8_t* Vp = Kp + C::SPAGES * C::PAGE;
             const int tok0 = js * BS + tw * C::TG + tg;  // this group's first position
-            // with several heads per warp, steps go in pairs (NB = 2): both
-            // steps' dot products and shuffle reductions interleave (twice the
-            // independent chains), and the softmax takes one lazy-rescale
-            // decision per pair
-#pragma unroll
-            for (int u0 = 0; u0 < C::SUB; u0 += C::NB) {
-                bool valid[C::NB];
-                uint32_t vw[C::NB][C::NV][4];
-                float sc[C::NB][C::GW];
-#pragma unroll
-                for (int h = 0; h < C::NB; ++h) {
-                    const int tis = (u0 + h) * C::TPI;  // step offset inside the stage
-                    valid[h] = ((mask >> ((tis + tw * C::TG + tg) / BS)) & 1) && tok0 + tis < it.t1;
-                    // value chunks are loaded up front (unconditionally: the
-                    // rows are in shared memory) so the loads overlap the QK math
-#pragma unroll
-                    for (int v = 0; v < C::NV; ++v) load_chunk<C::VB>(Vp + tis * C::ROWB + v * C::LPT * C::VB, vw[h][v]);
-                }
-                // ---- QK: this lane's chunks of both steps, then butterflies over the group ----
-                {
-                    float s0[C::NB][C::GW], s1[C::NB][C::GW];
-#pragma unroll
-                    for (int h = 0; h < C::NB; ++h)
-#pragma unroll
-                        for (int g = 0; g < C::GW; ++g) s0[h][g] = s1[h][g] = 0.f;
-#pragma unroll
+            // a stage whose pages are all present and whose tokens all lie
+            // before the item's end takes a path without per-token masks
+            const bool full_stage = mask == (1 << C::SPAGES) - 1 && js * BS + C::STOK <= it.t1;
+            auto stage_steps = [&](auto full_tag) {
+                constexpr bool FULL = decltype(full_tag)::value;
+                // with several heads per warp, steps go in pairs (NB = 2): both
+                // steps' dot products and shuffle reductions interleave (twice the
+                // independent chains), and the softmax takes one lazy-rescale
+                // decision per pair
+    #pragma unroll
+                for (int u0 = 0; u0 < C::SUB; u0 += C::NB) {
+                    bool valid[C::NB];
+                    uint32_t vw[C::NB][C::NV][4];
+                    float sc[C::NB][C::GW];
+    #pragma unroll
                     for (int h = 0; h < C::NB; ++h) {
-                        const uint8_t* krow = Kp + (u0 + h) * C::TPI * C::ROWB;
-#pragma unroll
-                        for (int v = 0; v < C::NV; ++v) {
-                            uint32_t w[4];
-                            load_chunk<C::VB>(krow + v * C::LPT * C::VB, w);
-#pragma unroll
-                            for (int x = 0; x < C::VB / 4; ++x) {
-                                if constexpr (C::KB == 2) {
-                                    const int pi = (v * C::EV) / 2 + x;
-#pragma unroll
-                                    for (int g = 0; g < C::GW; ++g)
-                                        fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi], w[x]);
-                                } else {
-                                    const uint32_t h0 = e4m3x2_to_h2(w[x]), h1 = e4m3x2_to_h2(w[x] >> 16);
-                                    const int pi = (v * C::EV) / 2 + 2 * x;
-#pragma unroll
-                                    for (int g = 0; g < C::GW; ++g) {
-                                        fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi], h0);
-                                        fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi + 1], h1);
-                                    }
-                                }
-                            }
-                        }
+                        const int tis = (u0 + h) * C::TPI;  // step offset inside the stage
+                        valid[h] = FULL || (((mask >> ((tis + tw * C::TG + tg) / BS)) & 1) && tok0 + tis < it.t1);
+                        // value chunks are loaded up front (unconditionally: the
+                        // rows are in shared memory) so the loads overlap the QK math
+    #pragma unroll
+                        for (int v = 0; v < C::NV; ++v) load_chunk<C::VB>(Vp + tis * C::ROWB + v * C::LPT * C::VB, vw[h][v]);
                     }
-                    float t[C::NB][C::GW];
-#pragma unroll
-                    for (int h = 0; h < C::NB; ++h)
-#pragma unroll
-                        for (int g = 0; g < C::GW; ++g) t[h][g] = s0[h][g] + s1[h][g];
-#pragma unroll
-                    for (int o = 1; o < C::LPT; o <<= 1)
-#pragma unroll
+                    // ---- QK: this lane's chunks of both steps, then butterflies over the group ----
+                    {
+                        float s0[C::NB][C::GW], s1[C::NB][C::GW];
+    #pragma unroll
                         for (int h = 0; h < C::NB; ++h)
-#pragma unroll
-                            for (int g = 0; g < C::GW; ++g) t[h][g] += __shfl_xor_sync(0xffffffffu, t[h][g], o);
-#pragma unroll
+    #pragma unroll
+                            for (int g = 0; g < C::GW; ++g) s0[h][g] = s1[h][g] = 0.f;
+    #pragma unroll
+                        for (int h = 0; h < C::NB; ++h) {
+                            const uint8_t* krow = Kp + (u0 + h) * C::TPI * C::ROWB;
+    #pragma unroll
+                            for (int v = 0; v < C::NV; ++v) {
+                                uint32_t w[4];
+                                load_chunk<C::VB>(krow + v * C::LPT * C::VB, w);
+    #pragma unroll
+                                for (int x = 0; x < C::VB / 4; ++x) {
+                                    if constexpr (C::KB == 2) {
+                                        const int pi = (v * C::EV) / 2 + x;
+    #pragma unroll
+                                        for (int g = 0; g < C::GW; ++g)
+                                            fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi], w[x]);
+                                    } else {
+                                        const uint32_t h0 = e4m3x2_to_h2(w[x]), h1 = e4m3x2_to_h2(w[x] >> 16);
+                                        const int pi = (v * C::EV) / 2 + 2 * x;
+    #pragma unroll
+                                        for (int g = 0; g < C::GW; ++g) {
+                                            fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi], h0);
+                                            fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi + 1], h1);
+                                        }
+                                    }
+                                }
+                            }
+                        }
+                        float t[C::NB][C::GW];
+    #pragma unroll
+                        for (int h = 0; h < C::NB; ++h)
+    #pragma unroll
+                            for (int g = 0; g < C::GW; ++g) t[h][g] = s0[h][g] + s1[h][g];
+    #pragma unroll
+                        for (int o = 1; o < C::LPT; o <<= 1)
+    #pragma unroll
+                            for (int h = 0; h < C::NB; ++h)
+    #pragma unroll
+                                for (int g = 0; g < C::GW; ++g) t[h][g] += __shfl_xor_sync(0xffffffffu, t[h][g], o);
+    #pragma unroll
+                        for (int h = 0; h < C::NB; ++h)
+    #pragma unroll
+                            for (int g = 0; g < C::GW; ++g) sc[h][g] = (FULL || valid[h]) ? t[h][g] * qk_scale : -INFINITY;
+                    }
+                    // ---- online softmax of this group over the NB steps, lazy rescale (warp-uniform test) ----
+                    float smax[C::GW];
+    #pragma unroll
+                    for (int g = 0; g < C::GW; ++g) {
+                        smax[g] = sc[0][g];
+    #pragma unroll
+                        for (int h = 1; h < C::NB; ++h) smax[g] = fmaxf(smax[g], sc[h][g]);
+                    }
+                    bool need = false;
+    #pragma unroll
+                    for (int g = 0; g < C::GW; ++g) need |= smax[g] > m[g] + kTau;
+                    if (__any_sync(0xffffffffu, need)) {
+    #pragma unroll
+                        for (int g = 0; g < C::GW; ++g) {
+                            const float mx = smax[g];
+                            const bool r = mx > m[g] + kTau;
+                            const float a = r ? fast_exp2(m[g] - mx) : 1.f;  // 0 when m = -inf
+                            m[g] = r ? mx : m[g];
+                            l[g] *= a;
+                            const uint64_t aa = pk2(a, a);
+    #pragma unroll
+                            for (int x = 0; x < C::PL; ++x) acc[g][x] = fmul2(acc[g][x], aa);
+                        }
+                    }
+                    uint64_t pp[C::NB][C::GW];
+    #pragma unroll
                     for (int h = 0; h < C::NB; ++h)
-#pragma unroll
-                        for (int g = 0; g < C::GW; ++g) sc[h][g] = valid[h] ? t[h][g] * qk_scale : -INFINITY;
-                }
-                // ---- online softmax of this group over the NB steps, lazy rescale (warp-uniform test) ----
-                float smax[C::GW];
-#pragma unroll
-                for (int g = 0; g < C::GW; ++g) {
-                    smax[g] = sc[0][g];
-#pragma unroll
-                    for (int h = 1; h < C::NB; ++h) smax[g] = fmaxf(smax[g], sc[h][g]);
-                }
-                bool need = false;
-#pragma unroll
-                for (int g = 0; g < C::GW; ++g) need |= smax[g] > m[g] + kTau;
-                if (__any_sync(0xffffffffu, need)) {
-#pragma unroll
-                    for (int g = 0; g < C::GW; ++g) {
-                        const float mx = smax[g];
-                        const bool r = mx > m[g] + kTau;
-                        const float a = r ? fast_exp2(m[g] - mx) : 1.f;  // 0 when m = -inf
-                        m[g] = r ? mx : m[g];
-                        l[g] *= a;
-                        const uint64_t aa = pk2(a, a);
-#pragma unroll
-                        for (int x = 0; x < C::PL; ++x) acc[g][x] = fmul2(acc[g][x], aa);
-                    }
-                }
-                uint64_t pp[C::NB][C::GW];
-#pragma unroll
-                for (int h = 0; h < C::NB; ++h)
-#pragma unroll
-                    for (int g = 0; g < C::GW; ++g) {
-                        const float pr = valid[h] ? fast_exp2(sc[h][g] - m[g]) : 0.f;
-                        l[g] += pr;
-                        pp[h][g] = pk2(pr, pr);
-                    }
-                // ---- PV over this lane's value chunks (masked rows are not read) ----
-#pragma unroll
-                for (int h = 0; h < C::NB; ++h) {
-                    if (valid[h]) {
-#pragma unroll
-                        for (int v = 0; v < C::NV; ++v) {
-                            const uint32_t (&w)[4] = vw[h][v];
-#pragma unroll
-                            for (int x = 0; x < C::VB / 4; ++x) {
-                                if constexpr (C::KB == 2) {
-                                    const uint64_t v2 = pair_of<KVDT>(w[x]);
-                                    const int pi = (v * C::EV) / 2 + x;
-#pragma unroll
-                                    for (int g = 0; g < C::GW; ++g) acc[g][pi] = ffma2(pp[h][g], v2, acc[g][pi]);
-                                } else {
-                                    const uint64_t v0 = pair_of<PA_F16>(e4m3x2_to_h2(w[x]));
-                                    const uint64_t v1 = pair_of<PA_F16>(e4m3x2_to_h2(w[x] >> 16));
-                                    const int pi = (v * C::EV) / 2 + 2 * x;
-#pragma unroll
-                                    for (int g = 0; g < C::GW; ++g) {
-                                        acc[g][pi] = ffma2(pp[h][g], v0, acc[g][pi]);
-                                        acc[g][pi + 1] = ffma2(pp[h][g], v1, acc[g][pi + 1]);
+    #pragma unroll
+                        for (int g = 0; g < C::GW; ++g) {
+                            const float pr = (FULL || valid[h]) ? fast_exp2(sc[h][g] - m[g]) : 0.f;
+                            l[g] += pr;
+                            pp[h][g] = pk2(pr, pr);
+                        }
+                    // ---- PV over this lane's value chunks (masked rows are not read) ----
+    #pragma unroll
+                    for (int h = 0; h < C::NB; ++h) {
+                        if (FULL || valid[h]) {
+    #pragma unroll
+                            for (int v = 0; v < C::NV; ++v) {
+                                const uint32_t (&w)[4] = vw[h][v];
+    #pragma unroll
+                                for (int x = 0; x < C::VB / 4; ++x) {
+                                    if constexpr (C::KB == 2) {
+                                        const uint64_t v2 = pair_of<KVDT>(w[x]);
+                                        const int pi = (v * C::EV) / 2 + x;
+    #pragma unroll
+                                        for (int g = 0; g < C::GW; ++g) acc[g][pi] = ffma2(pp[h][g], v2, acc[g][pi]);
+                                    } else {
+                                        const uint64_t v0 = pair_of<PA_F16>(e4m3x2_to_h2(w[x]));
+                                        const uint64_t v1 = pair_of<PA_F16>(e4m3x2_to_h2(w[x] >> 16));
+                                        const int pi = (v * C::EV) / 2 + 2 * x;
+    #pragma unroll
+                                        for (int g = 0; g < C::GW; ++g) {
+                                            acc[g][pi] = ffma2(pp[h][g], v0, acc[g][pi]);
+                                            acc[g][pi + 1] = ffma2(pp[h][g], v1, acc[g][pi + 1]);
+                                        }
                                     }
                                 }
                             }
                         }
                     }
                 }
-            }
+            };
+            if (full_stage) stage_steps(std::true_type{});
+            else stage_steps(std::false_type{});
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8u * stage);
             if (++stage == static_cast<uint32_t>(S)) {
