@@ -229,7 +229,8 @@ class DecodeStep:
                                          partition_size)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         self.kv_bytes = case.kv_bytes()
-        P = partition_size or 512
+        P = partition_size or (1024 if case.num_heads // case.num_kv_heads >= 4 else 512)
+        self.P_eff = P
         self.split = self.max_len > P
         self.launches_per_step = 2 + (1 if self.split else 0)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -618,7 +619,9 @@ def run_ours(args):
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    step = DecodeStep(case, dev, args.partition_size, wname)
+    # the long-context configuration states its partition (512 tokens)
+    partition = args.partition_size or (512 if args.workload == "long" else 0)
+    step = DecodeStep(case, dev, partition, wname)
     # the K/V a step reads, plus everything else it touches
     small = step.kv_bytes + case.q.numel() * case.q.element_size() * 2 < L2_BYTES
     flush = L2Flush(dev, small)
@@ -651,7 +654,7 @@ def run_ours(args):
         "config": {"workload": wname, "num_seqs": step.B, "num_heads": case.num_heads,
                    "num_kv_heads": case.num_kv_heads, "head_size": case.head_size, "block_size": case.block_size,
                    "num_blocks": case.num_blocks, "kv_bytes_per_step": step.kv_bytes,
-                   "partition_size": args.partition_size or 512,
+                   "partition_size": step.P_eff,
                    "l2": ("L2 flushed between timed steps (%.3f MB of K/V per step < 129 MB L2; each step "
                           "timed on its own)" % (step.kv_bytes / 1e6)) if small else
                          "inputs larger than L2 (%.2f GB of K/V read per step > 129 MB L2)" % (step.kv_bytes / 1e9),

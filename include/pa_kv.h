@@ -147,7 +147,9 @@ pa_status pa_copy_blocks(const pa_kv_cache* cache, const int32_t* src_dst_pairs,
  *   <= max_blocks_per_seq*block_size, otherwise PA_ERR_INVALID_ARG is
  *   reported and the sequence's output is 0.
  * partition_size: tokens per context partition (a multiple of block_size),
- *   0 = automatic.  A sequence longer than one partition is split; the
+ *   0 = automatic (512, or 1024 when num_heads / num_kv_heads >= 4; the
+ *   workspace size query answers for 512, which covers both).  A sequence
+ *   longer than one partition is split; the
  *   partitions' partial results go to `workspace` and a second kernel merges
  *   them by their log-sum-exp.
  * workspace: device scratch of at least pa_decode_workspace_size(...) bytes,

@@ -6,11 +6,13 @@
 namespace pa {
 namespace {
 
-constexpr int kAutoPartition = 512;
-
-int resolve_partition(int partition_size, int block_size) {
+// Automatic partition: 512 tokens, or 1024 when a KV head serves 4 or more
+// query heads -- an item's fixed work (query load, merge and partial write of
+// every head) grows with the group, so longer items pay it less often.  A
+// workspace sized with group 1 (512) covers both.
+int resolve_partition(int partition_size, int block_size, int group) {
     if (partition_size == 0) {
-        int p = kAutoPartition;
+        const int p = group >= 4 ? 1024 : 512;
         return p % block_size == 0 ? p : block_size * ((p + block_size - 1) / block_size);
     }
     return partition_size;
@@ -45,7 +47,7 @@ extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, 
     if (num_seqs <= 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0 || block_size <= 0 ||
         partition_size < 0)
         return 0;
-    const int P = resolve_partition(partition_size, block_size);
+    const int P = resolve_partition(partition_size, block_size, 1);
     return ws_layout(num_seqs, num_heads, head_size, max_parts_of(max_seq_len, P)).bytes;
 }
 
@@ -77,7 +79,7 @@ extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const
         !(cache->k_scale > 0.f && std::isfinite(cache->k_scale) && cache->v_scale > 0.f &&
           std::isfinite(cache->v_scale)))
         return PA_ERR_INVALID_ARG;
-    const int P = resolve_partition(partition_size, bs);
+    const int P = resolve_partition(partition_size, bs, group);
     if (P % bs != 0) return PA_ERR_INVALID_ARG;
     if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
     const int max_parts = max_parts_of(max_seq_len, P);
