@@ -604,6 +604,91 @@ def cpu_baseline_prefill(case, budget_s=10.0):
                       % (int(sample[2][-1]), flops / 1e9, reps, spent)}
 
 
+def run_swap(args, dev, rank, world):
+    """Swap-based preemption's data move: whole blocks of an MHA-shaped cache
+    (32 KV heads x 16 tokens x 128 fp16, K and V: 256 KiB a block) out to
+    page-locked host memory and back in one pa_swap_blocks call each way.
+    Roofline: a single contiguous copy of the same bytes between the same
+    memories (cudaMemcpyAsync through torch), measured in the same run."""
+    import paged_kv_cache_75_gb300 as pk
+    nb, hkv, bs, d, n = 10_000, 32, 16, 128, 4096
+    g = torch.Generator(device=dev)
+    g.manual_seed(777)
+    k = torch.empty((nb, hkv, bs, d), dtype=torch.float16, device=dev).normal_(generator=g)
+    v = torch.empty_like(k).normal_(generator=g)
+    cache = pk.KVCache(k, v)
+    hk = torch.empty((n, hkv, bs, d), dtype=torch.float16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    rng = np.random.default_rng(778)
+    dev_ids = rng.permutation(nb)[:n].astype(np.int32)
+    pairs = torch.from_numpy(np.stack([dev_ids, np.arange(n, dtype=np.int32)], 1).copy()).to(dev)
+    back = torch.from_numpy(np.stack([rng.permutation(nb)[:n].astype(np.int32),
+                                      np.arange(n, dtype=np.int32)], 1).copy()).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bytes_one_way = 2 * n * hkv * bs * d * 2
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, steps):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+    out = lambda: pk.pa_swap_blocks(cache, hk, hv, pairs, True, status)
+    inn = lambda: pk.pa_swap_blocks(cache, hk, hv, back, False, status)
+    flat_d = torch.empty(bytes_one_way, dtype=torch.uint8, device=dev)
+    flat_h = torch.empty(bytes_one_way, dtype=torch.uint8).pin_memory()
+    d2h = lambda: flat_h.copy_(flat_d, non_blocking=True)
+    h2d = lambda: flat_d.copy_(flat_h, non_blocking=True)
+    for f in (out, inn, d2h, h2d):
+        for _ in range(args.warmup):
+            f()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 50))
+    barrier(world)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t_out, t_in = timed(out, steps), timed(inn, steps)
+    t_d2h, t_h2d = timed(d2h, steps), timed(h2d, steps)
+    barrier(world)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d during the swap benchmark" % int(status.item()))
+    total_ms, moved = aggregate(t_out + t_in, 2.0 * bytes_one_way, world)
+    gbs = lambda ms: bytes_one_way / (ms / 1e3) / 1e9
+    # CPU baseline: the same block gather done on the host (numpy fancy indexing)
+    hsrc = np.empty((2048, hkv * bs * d), dtype=np.float16)
+    idx = rng.permutation(2048)[:1024]
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < 3.0:
+        _ = hsrc[idx].copy()
+        reps += 1
+    cpu_gbs = reps * 1024 * hkv * bs * d * 2 / (time.perf_counter() - t0) / 1e9
+    line = {
+        "metric": "block swap GB/s (device cache <-> page-locked host, out + in)",
+        "value": round(moved / (total_ms / 1e3) / 1e9, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "swap_4096_blocks_of_10000_32kvh_bs16_d128_fp16", "blocks": n,
+                   "bytes_each_way": bytes_one_way, "l2": "inputs larger than L2 (1.07 GB each way)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "clocks": clk.summary(),
+        "swap_out_gbs": round(gbs(t_out), 2), "swap_in_gbs": round(gbs(t_in), 2),
+        "gpu_launches": 2 * steps,
+        "roofline": {"bound": "link", "kernel": "swap_blocks_kernel", "achieved": round(gbs(t_out), 2),
+                     "peak": round(gbs(t_d2h), 2), "unit": "GB/s", "frac": round(t_d2h / t_out, 4),
+                     "peak_kind": "of a contiguous device->host copy of the same bytes, measured live",
+                     "swap_in_frac": round(t_h2d / t_in, 4), "h2d_copy_gbs": round(gbs(t_h2d), 2),
+                     "traffic": None},
+        "cpu_baseline": {"value": round(cpu_gbs, 2), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "numpy gather of 1024 of 2048 host blocks of 256 KiB, %d passes" % reps},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------------------
 def run_ours(args):
     rank, local_rank, world = dist_env()
@@ -612,6 +697,12 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    if args.workload == "swap":
+        run_swap(args, dev, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     case, wname = build_workload(args.workload, dev, args.num_seqs, args.pool_blocks)
     if args.workload == "mixed":
         run_prefill(args, case, wname, dev, rank, world)
@@ -688,6 +779,31 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
+    if args.workload == "swap":
+        # a block swap is a copy: the host-side reference gathers the same
+        # blocks with numpy, host memory to host memory
+        hkv, bs, d = 32, 16, 128
+        rng = np.random.default_rng(778)
+        src = np.empty((2048, hkv * bs * d), dtype=np.float16)
+        idx = rng.permutation(2048)[:1024]
+        for _ in range(args.warmup):
+            src[idx].copy()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            src[idx].copy()
+        dt = time.perf_counter() - t0
+        value = args.steps * 1024 * hkv * bs * d * 2 / dt / 1e9
+        print(json.dumps({
+            "impl": "reference", "metric": "block swap GB/s (device cache <-> page-locked host, out + in)",
+            "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": "swap_4096_blocks_of_10000_32kvh_bs16_d128_fp16"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "numpy gather of 1024 of 2048 host blocks of 256 KiB per step"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        return
     import oracle
     case, wname = build_workload(args.workload, "cpu")
     cores = os.cpu_count() or 1
@@ -743,7 +859,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny", "mixed"], default="mha")
+    ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny", "mixed", "swap"], default="mha")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="sequences (smaller profiling cases)")

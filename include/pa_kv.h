@@ -229,6 +229,29 @@ pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtype, const pa
                             pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Swap whole blocks between the device cache and page-locked host memory:
+ * the data move of swap-based preemption ("Как работает paged attention?"
+ * 4.3: the preempted request's KV cache goes to CPU memory and comes back
+ * when it resumes; vLLM paper summary, section 5: a CPU block allocator
+ * holds the swapped blocks).  Which requests to preempt, and the host-side
+ * block ids, are the caller's (a scheduler's) business.
+ *
+ * host_k, host_v: page-locked host memory (cudaHostAlloc / cudaMallocHost /
+ *   cudaHostRegister, or a pinned torch tensor), 16-byte aligned, laid out
+ *   like the cache: [num_host_blocks][num_kv_heads][block_size][head_size]
+ *   of the cache's dtype.  Pageable memory is rejected (PA_ERR_INVALID_ARG).
+ * pairs: device int32 [n][2] = (device block id, host block id), n <= 65535.
+ *   to_host != 0 copies device -> host (swap out), 0 copies host -> device
+ *   (swap in).  A pair with an id out of range is skipped and reported as
+ *   PA_ERR_BAD_BLOCK.  Destinations must be distinct.
+ * Asynchronous on `stream`; the host buffers must stay valid (and, for swap
+ * out, unread) until the stream reaches this point.
+ * ------------------------------------------------------------------------- */
+pa_status pa_swap_blocks(const pa_kv_cache* cache, void* host_k, void* host_v, int64_t num_host_blocks,
+                         const int32_t* pairs, int32_t n, int32_t to_host, int32_t* dev_status,
+                         pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Slots of new tokens from a block table (host arrays): "Как работает paged
  * attention?" 4.1 (logical block = pos / block_size, offset pos % block_size);
  * vLLM paper summary §3.  For token i of sequence seq_idx[i] at position

@@ -56,6 +56,7 @@ def library():
             "pa_pool_ref_count": ([vp, i64], i32),
             "pa_pool_seq_len": ([vp, i64], i32),
             "pa_slot_mapping": ([vp, i32, i32, i32, vp, vp, i64, vp], C.c_int),
+            "pa_swap_blocks": ([pc, vp, vp, i64, vp, i32, i32, vp, vp], C.c_int),
             "pa_decode_static_ws": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, vp],
                                     C.c_int),
         }
@@ -172,6 +173,24 @@ def pa_copy_blocks(cache: KVCache, src_dst_pairs: torch.Tensor, dev_status: Opti
     st = library().pa_copy_blocks(C.byref(cs), _ptr(src_dst_pairs), n, _ptr(dev_status),
                                   _stream(cache.k_cache))
     _check(st, "pa_copy_blocks")
+
+
+def pa_swap_blocks(cache: KVCache, host_k: torch.Tensor, host_v: torch.Tensor, pairs: torch.Tensor,
+                   to_host: bool, dev_status: Optional[torch.Tensor] = None):
+    """Copies whole blocks between the cache and pinned host tensors shaped
+    like the cache ([host_blocks, Hkv, bs, D]); pairs: device int32 [n, 2] of
+    (device block, host block)."""
+    _need(pairs, "pairs", torch.int32)
+    for name, t in (("host_k", host_k), ("host_v", host_v)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous host tensor" % name)
+        if t.dtype != cache.k_cache.dtype or t.shape[1:] != cache.k_cache.shape[1:]:
+            raise ValueError("%s must match the cache's dtype and block shape" % name)
+    cs = cache.c_struct()
+    st = library().pa_swap_blocks(C.byref(cs), C.c_void_p(host_k.data_ptr()), C.c_void_p(host_v.data_ptr()),
+                                  host_k.shape[0], _ptr(pairs), pairs.numel() // 2, 1 if to_host else 0,
+                                  _ptr(dev_status), _stream(cache.k_cache))
+    _check(st, "pa_swap_blocks")
 
 
 def pa_decode_workspace_size(num_seqs, num_heads, head_size, max_seq_len, block_size, partition_size=0) -> int:
