@@ -252,6 +252,27 @@ pa_status pa_swap_blocks(const pa_kv_cache* cache, void* host_k, void* host_v, i
                          pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Varlen attention over packed K/V: "Paged 어텐션", Varlen 경로 -- the batch's
+ * keys and values are contiguous tensors [Σk][num_kv_heads][head_size]
+ * indexed by cu_seq_lens_k (no cache, no block table), queries as in
+ * pa_prefill_varlen.  Same arithmetic and causal alignment as
+ * pa_prefill_varlen (bottom-right; rows without a visible key give 0).
+ *
+ * k, v: device, total_k rows of num_kv_heads*head_size elements of dtype (F16
+ *   or BF16, the same as q and out), 16-byte aligned; may be NULL when
+ *   total_k == 0.  cu_seq_lens_k[b+1] must be <= total_k, otherwise
+ *   PA_ERR_INVALID_ARG is reported in *dev_status and that sequence's rows are
+ *   unspecified.
+ * Supported: head_size 128; num_heads / num_kv_heads in {1, 2, 4, 8};
+ *   num_seqs <= 6144.
+ * ------------------------------------------------------------------------- */
+pa_status pa_prefill_varlen_packed(void* out, const void* q, const void* k, const void* v, pa_dtype dtype,
+                                   const int32_t* cu_seq_lens_q, const int32_t* cu_seq_lens_k, int32_t num_seqs,
+                                   int32_t max_seqlen_q, int32_t max_seqlen_k, int64_t total_k, int32_t num_heads,
+                                   int32_t num_kv_heads, int32_t head_size, float scale, int32_t causal,
+                                   int32_t* dev_status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Slots of new tokens from a block table (host arrays): "Как работает paged
  * attention?" 4.1 (logical block = pos / block_size, offset pos % block_size);
  * vLLM paper summary §3.  For token i of sequence seq_idx[i] at position

@@ -57,6 +57,8 @@ def library():
             "pa_pool_seq_len": ([vp, i64], i32),
             "pa_slot_mapping": ([vp, i32, i32, i32, vp, vp, i64, vp], C.c_int),
             "pa_swap_blocks": ([pc, vp, vp, i64, vp, i32, i32, vp, vp], C.c_int),
+            "pa_prefill_varlen_packed": ([vp, vp, vp, vp, C.c_int, vp, vp, i32, i32, i32, i64, i32, i32, i32, f32,
+                                          i32, vp, vp], C.c_int),
             "pa_decode_static_ws": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, vp],
                                     C.c_int),
         }
@@ -173,6 +175,24 @@ def pa_copy_blocks(cache: KVCache, src_dst_pairs: torch.Tensor, dev_status: Opti
     st = library().pa_copy_blocks(C.byref(cs), _ptr(src_dst_pairs), n, _ptr(dev_status),
                                   _stream(cache.k_cache))
     _check(st, "pa_copy_blocks")
+
+
+def pa_prefill_varlen_packed(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                             cu_seq_lens_q: torch.Tensor, cu_seq_lens_k: torch.Tensor, max_seqlen_q: int,
+                             max_seqlen_k: int, scale: float, causal: bool = True,
+                             dev_status: Optional[torch.Tensor] = None):
+    """Varlen attention over packed K/V [Σk, Hkv, D] (no cache)."""
+    for name, t in (("out", out), ("q", q), ("k", k), ("v", v)):
+        _need(t, name)
+    _need(cu_seq_lens_q, "cu_seq_lens_q", torch.int32)
+    _need(cu_seq_lens_k, "cu_seq_lens_k", torch.int32)
+    if k.dim() != 3 or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k, v must be [total_k, num_kv_heads, head_size] of q's dtype")
+    st = library().pa_prefill_varlen_packed(_ptr(out), _ptr(q), _ptr(k), _ptr(v), torch_dtype_code(q.dtype),
+                                            _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k), cu_seq_lens_q.numel() - 1,
+                                            max_seqlen_q, max_seqlen_k, k.shape[0], q.shape[1], k.shape[1],
+                                            q.shape[2], scale, 1 if causal else 0, _ptr(dev_status), _stream(q))
+    _check(st, "pa_prefill_varlen_packed")
 
 
 def pa_swap_blocks(cache: KVCache, host_k: torch.Tensor, host_v: torch.Tensor, pairs: torch.Tensor,

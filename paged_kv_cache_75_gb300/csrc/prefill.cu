@@ -87,6 +87,7 @@ struct PrefillParams {
     int32_t max_k;
     int32_t causal;
     float scale_log2;  // scale * log2(e)
+    int64_t total_k;   // packed K/V: rows of K and V (Σ key lengths); -1 for the paged cache
 };
 
 // ---------------------------------------------------------------------------
@@ -241,6 +242,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 3-D tiled TMA load (packed K/V: {element, KV head, token})
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -269,8 +280,9 @@ __device__ __forceinline__ bool seq_lens_ok(const PrefillParams& p, int b, int& 
     const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
     lq = q1 - q0;
     lk = k1 - k0;
-    return lq >= 0 && lk >= 0 && lq <= p.max_q && lk <= p.max_k &&
-           static_cast<int64_t>(lk) <= static_cast<int64_t>(p.max_blocks) * p.block_size;
+    const bool fits = p.total_k >= 0 ? (k0 >= 0 && static_cast<int64_t>(k1) <= p.total_k)
+                                     : static_cast<int64_t>(lk) <= static_cast<int64_t>(p.max_blocks) * p.block_size;
+    return lq >= 0 && lk >= 0 && lq <= p.max_q && lk <= p.max_k && fits;
 }
 
 struct Work {
@@ -297,7 +309,9 @@ __device__ __forceinline__ Work work_item(const PrefillParams& p, const int32_t*
     return w;
 }
 
-template <int DT>
+// PACKED: K and V are contiguous [Σk][num_kv_heads][head_size] tensors indexed
+// by cu_seq_lens_k (no cache, no block table); otherwise the paged cache.
+template <int DT, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                         const PrefillParams p) {
@@ -398,57 +412,90 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         // is done, long before the PV of the same tile has used V.
         uint32_t fill = 0, stage = 0, phase = 0;
         bool ok = true;
+        if constexpr (PACKED) {
+            // a tile is 128 consecutive rows of one KV head: one 3-D box per
+            // 64-column half (rows past the tensor read as zero; rows past the
+            // sequence are masked / zeroed by the softmax warps)
+            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                const Work w = work_item(p, prefix, item);
+                const int row0 = __ldg(p.cu_k + w.b);
+                for (int t = 0; t < w.ntiles && ok; ++t) {
+#pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint32_t full = (kv == 0 ? k_full : v_full) + 8 * stage;
+                        const uint32_t empty = (kv == 0 ? k_empty : v_empty) + 8 * stage;
+                        if (lane == 0) ok = ok && mbar_wait(empty, phase ^ 1u, p.status, abort_flag);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) break;
+                        if (lane == 0) {
+                            mbar_expect_tx(full, kTileBytes);
+                            const uint32_t dst = smem_addr((kv == 0 ? sK : sV) + stage * kTileBytes);
+                            const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
+                            tma_load_3d(dst, map, 0, w.kvh, row0 + t * kBN, full);
+                            tma_load_3d(dst + kBlkBytes, map, 64, w.kvh, row0 + t * kBN, full);
+                        }
+                        __syncwarp();
+                    }
+                    ++fill;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        } else {
         const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
-        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Work w = work_item(p, prefix, item);
-            const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
-            // page ids come in batches of 32 (one per lane, -1: past Lk, -2:
-            // bad id), so the table's latency is paid once per batch
-            const int pages = (w.ntiles * kBN + p.block_size - 1) / p.block_size;
-            int32_t id = -1;
-            for (int t = 0; t < w.ntiles && ok; ++t) {
-                const int pg0 = t * ppt;  // first page of this tile
-                if ((pg0 & 31) == 0) {
-                    const int pg = pg0 + lane;
-                    id = -1;
-                    if (pg < pages && pg * p.block_size < w.lk) {
-                        id = __ldg(bt_row + pg);
-                        if (id < 0 || id >= p.num_blocks) {
-                            report(p.status, PA_ERR_BAD_BLOCK);
-                            id = -2;
+            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+                const Work w = work_item(p, prefix, item);
+                const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
+                // page ids come in batches of 32 (one per lane, -1: past Lk, -2:
+                // bad id), so the table's latency is paid once per batch
+                const int pages = (w.ntiles * kBN + p.block_size - 1) / p.block_size;
+                int32_t id = -1;
+                for (int t = 0; t < w.ntiles && ok; ++t) {
+                    const int pg0 = t * ppt;  // first page of this tile
+                    if ((pg0 & 31) == 0) {
+                        const int pg = pg0 + lane;
+                        id = -1;
+                        if (pg < pages && pg * p.block_size < w.lk) {
+                            id = __ldg(bt_row + pg);
+                            if (id < 0 || id >= p.num_blocks) {
+                                report(p.status, PA_ERR_BAD_BLOCK);
+                                id = -2;
+                            }
                         }
                     }
-                }
-                // lane k < ppt holds the id of page k of this tile
-                const int my_id = __shfl_sync(0xffffffffu, id, (pg0 + (lane & 7)) & 31);
-                const bool have = lane < ppt && my_id >= 0;
-                const uint32_t bytes =
-                    static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, have))) * 2u * p.block_size * kD;
-                const int row = (my_id * p.num_kv_heads + w.kvh) * p.block_size;
-                const uint32_t off = lane * p.block_size * 128;  // page lane's rows in a 64-column block
-#pragma unroll
-                for (int kv = 0; kv < 2; ++kv) {
-                    const uint32_t full = (kv == 0 ? k_full : v_full) + 8 * stage;
-                    const uint32_t empty = (kv == 0 ? k_empty : v_empty) + 8 * stage;
-                    if (lane == 0) ok = ok && mbar_wait(empty, phase ^ 1u, p.status, abort_flag);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
-                    if (lane == 0) {
-                        if (bytes) mbar_expect_tx(full, bytes);
-                        else mbar_arrive(full);
+                    // lane k < ppt holds the id of page k of this tile
+                    const int my_id = __shfl_sync(0xffffffffu, id, (pg0 + (lane & 7)) & 31);
+                    const bool have = lane < ppt && my_id >= 0;
+                    const uint32_t bytes =
+                        static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, have))) * 2u * p.block_size * kD;
+                    const int row = (my_id * p.num_kv_heads + w.kvh) * p.block_size;
+                    const uint32_t off = lane * p.block_size * 128;  // page lane's rows in a 64-column block
+    #pragma unroll
+                    for (int kv = 0; kv < 2; ++kv) {
+                        const uint32_t full = (kv == 0 ? k_full : v_full) + 8 * stage;
+                        const uint32_t empty = (kv == 0 ? k_empty : v_empty) + 8 * stage;
+                        if (lane == 0) ok = ok && mbar_wait(empty, phase ^ 1u, p.status, abort_flag);
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (!ok) break;
+                        if (lane == 0) {
+                            if (bytes) mbar_expect_tx(full, bytes);
+                            else mbar_arrive(full);
+                        }
+                        __syncwarp();
+                        if (have) {
+                            const uint32_t dst = smem_addr((kv == 0 ? sK : sV) + stage * kTileBytes) + off;
+                            const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
+                            tma_load_2d(dst, map, 0, row, full);
+                            tma_load_2d(dst + kBlkBytes, map, 64, row, full);
+                        }
                     }
-                    __syncwarp();
-                    if (have) {
-                        const uint32_t dst = smem_addr((kv == 0 ? sK : sV) + stage * kTileBytes) + off;
-                        const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
-                        tma_load_2d(dst, map, 0, row, full);
-                        tma_load_2d(dst + kBlkBytes, map, 64, row, full);
+                    ++fill;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
-                }
-                ++fill;
-                if (++stage == kStages) {
-                    stage = 0;
-                    phase ^= 1u;
                 }
             }
         }
@@ -865,6 +912,43 @@ bool make_cache_map(CUtensorMap* map, const void* base, int64_t rows, int dtype,
     return r == CUDA_SUCCESS;
 }
 
+// packed K or V as a 3-D tensor {head_size, num_kv_heads, total rows}; a box
+// is 64 elements x 1 head x 128 rows
+bool make_packed_map(CUtensorMap* map, const void* base, int64_t total_k, int num_kv_heads, int dtype) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_kv_heads),
+                                static_cast<cuuint64_t>(total_k)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                   static_cast<cuuint64_t>(num_kv_heads) * kD * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBN)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// launch shared by the paged and packed entry points (p filled in, maps built)
+template <bool PACKED>
+pa_status launch_prefill(const PrefillParams& p, pa_dtype dtype, const CUtensorMap& map_k,
+                         const CUtensorMap& map_v, pa_stream_t stream) {
+    const int smem = kSmemBytes + (p.num_seqs + 1) * 4 + 1024;
+    if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
+    static LaunchCache cache_bf16, cache_f16;
+    auto kern = dtype == PA_BF16 ? paged_prefill_tc_kernel<PA_BF16, PACKED> : paged_prefill_tc_kernel<PA_F16, PACKED>;
+    const int per_sm = blocks_per_sm(kern, kThreads, smem, dtype == PA_BF16 ? cache_bf16 : cache_f16);
+    if (per_sm <= 0) return PA_ERR_CUDA;
+    const int64_t max_items =
+        static_cast<int64_t>(p.num_seqs) * ((p.max_q + p.tq - 1) / p.tq) * p.num_kv_heads;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
+    const int grid = static_cast<int>(max_items < cap ? max_items : cap);
+    if (grid <= 0) return PA_OK;
+    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(map_k, map_v, p);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace pa
 
@@ -919,23 +1003,63 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
     p.max_k = max_seqlen_k;
     p.causal = causal ? 1 : 0;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.total_k = -1;
 
     CUtensorMap map_k, map_v;
     if (!make_cache_map(&map_k, cache->k_cache, rows, q_dtype, bs) ||
         !make_cache_map(&map_v, cache->v_cache, rows, q_dtype, bs))
         return PA_ERR_CUDA;
+    return launch_prefill<false>(p, q_dtype, map_k, map_v, stream);
+}
 
-    const int smem = kSmemBytes + (num_seqs + 1) * 4 + 1024;
-    if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
-    static LaunchCache cache_bf16, cache_f16;
-    auto kern = q_dtype == PA_BF16 ? paged_prefill_tc_kernel<PA_BF16> : paged_prefill_tc_kernel<PA_F16>;
-    const int per_sm = blocks_per_sm(kern, kThreads, smem, q_dtype == PA_BF16 ? cache_bf16 : cache_f16);
-    if (per_sm <= 0) return PA_ERR_CUDA;
-    const int64_t max_items =
-        static_cast<int64_t>(num_seqs) * ((max_seqlen_q + p.tq - 1) / p.tq) * cache->num_kv_heads;
-    const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
-    const int grid = static_cast<int>(max_items < cap ? max_items : cap);
-    if (grid <= 0) return PA_OK;
-    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(map_k, map_v, p);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+extern "C" pa_status pa_prefill_varlen_packed(void* out, const void* q, const void* k, const void* v,
+                                              pa_dtype dtype, const int32_t* cu_seq_lens_q,
+                                              const int32_t* cu_seq_lens_k, int32_t num_seqs,
+                                              int32_t max_seqlen_q, int32_t max_seqlen_k, int64_t total_k,
+                                              int32_t num_heads, int32_t num_kv_heads, int32_t head_size,
+                                              float scale, int32_t causal, int32_t* dev_status,
+                                              pa_stream_t stream) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || max_seqlen_q < 0 || max_seqlen_k < 0 ||
+        total_k < 0 || !(scale == scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || max_seqlen_q == 0) return PA_OK;
+    if (out == nullptr || q == nullptr || cu_seq_lens_q == nullptr || cu_seq_lens_k == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (total_k > 0 && (k == nullptr || v == nullptr)) return PA_ERR_INVALID_ARG;
+    for (const void* ptr : {static_cast<const void*>(out), q, k, v})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int group = num_heads / num_kv_heads;
+    if (head_size != kD) return PA_ERR_UNSUPPORTED;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+    if (dtype != PA_F16 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > kMaxSeqs) return PA_ERR_UNSUPPORTED;
+    if (total_k > INT32_MAX - kBN) return PA_ERR_UNSUPPORTED;
+
+    PrefillParams p{};
+    p.out = out;
+    p.q = static_cast<const uint16_t*>(q);
+    p.cu_q = cu_seq_lens_q;
+    p.cu_k = cu_seq_lens_k;
+    p.status = dev_status;
+    p.block_size = kBN;
+    p.num_kv_heads = num_kv_heads;
+    p.num_heads = num_heads;
+    p.group = group;
+    p.tq = kRows / group;
+    p.num_seqs = num_seqs;
+    p.max_q = max_seqlen_q;
+    p.max_k = max_seqlen_k;
+    p.causal = causal ? 1 : 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.total_k = total_k;
+
+    // an empty K/V still needs a valid map: point it at q (never read, every
+    // sequence then has no key)
+    const int64_t rows = total_k > 0 ? total_k : 1;
+    CUtensorMap map_k, map_v;
+    if (!make_packed_map(&map_k, total_k > 0 ? k : q, rows, num_kv_heads, dtype) ||
+        !make_packed_map(&map_v, total_k > 0 ? v : q, rows, num_kv_heads, dtype))
+        return PA_ERR_CUDA;
+    return launch_prefill<true>(p, dtype, map_k, map_v, stream);
 }
