@@ -252,6 +252,29 @@ pa_status pa_swap_blocks(const pa_kv_cache* cache, void* host_k, void* host_v, i
                          pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Fused cache write + decode: for every sequence b with L = seq_lens[b] >= 1,
+ * the new token's K/V (k_new[b], v_new[b]) is stored at position L-1 -- the
+ * slot block_table[b][(L-1)/block_size]*block_size + (L-1)%block_size, as
+ * pa_kv_cache_write would store it -- and the query attends over all L
+ * tokens including it, in one launch.  Results and cache contents are
+ * bit-identical to pa_kv_cache_write followed by pa_decode ("Paged 어텐션",
+ * Decode 경로: the kernel updates the cache in place; the worked example's
+ * new tokens at positions 30, 32, 70).  The new token's page is read only up
+ * to the row before it.
+ *
+ * k_new, v_new: device [num_seqs][num_kv_heads][head_size] of q_dtype,
+ *   16-byte aligned.  E4M3 caches store e4m3_satfinite(rne(x / scale)).
+ * The block holding position L-1 must already be in the table (an id out of
+ *   range is reported as PA_ERR_BAD_BLOCK and nothing is written for it).
+ * Everything else as pa_decode (same workspace size).
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new, pa_dtype q_dtype,
+                           const pa_kv_cache* cache, const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
+                           float scale, int32_t partition_size, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Varlen attention over packed K/V: "Paged 어텐션", Varlen 경로 -- the batch's
  * keys and values are contiguous tensors [Σk][num_kv_heads][head_size]
  * indexed by cu_seq_lens_k (no cache, no block table), queries as in

@@ -57,6 +57,8 @@ def library():
             "pa_pool_seq_len": ([vp, i64], i32),
             "pa_slot_mapping": ([vp, i32, i32, i32, vp, vp, i64, vp], C.c_int),
             "pa_swap_blocks": ([pc, vp, vp, i64, vp, i32, i32, vp, vp], C.c_int),
+            "pa_decode_append": ([vp, vp, vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, sz, vp,
+                                  vp], C.c_int),
             "pa_prefill_varlen_packed": ([vp, vp, vp, vp, C.c_int, vp, vp, i32, i32, i32, i64, i32, i32, i32, f32,
                                           i32, vp, vp], C.c_int),
             "pa_decode_static_ws": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, vp],
@@ -236,6 +238,33 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: t
                              block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), H, float(scale),
                              int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(q))
     _check(st, "pa_decode")
+
+
+def pa_decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                     cache: KVCache, block_table: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                     scale: float, partition_size: int = 0, workspace: Optional[torch.Tensor] = None,
+                     dev_status: Optional[torch.Tensor] = None):
+    """pa_kv_cache_write of each sequence's new token (k_new, v_new:
+    [num_seqs, num_kv_heads, head_size], position seq_lens-1) fused with
+    pa_decode over seq_lens tokens."""
+    _need(q, "q")
+    _need(out, "out", q.dtype)
+    _need(k_new, "k_new", q.dtype)
+    _need(v_new, "v_new", q.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    B, H, D = q.shape
+    if tuple(k_new.shape) != (B, cache.num_kv_heads, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new, v_new must be [num_seqs, num_kv_heads, head_size]")
+    if workspace is not None:
+        _need(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    cs = cache.c_struct()
+    st = library().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), torch_dtype_code(q.dtype),
+                                    C.byref(cs), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+                                    int(max_seq_len), H, float(scale), int(partition_size), _ptr(workspace),
+                                    ws_bytes, _ptr(dev_status), _stream(q))
+    _check(st, "pa_decode_append")
 
 
 def pa_decode_static_ws(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,

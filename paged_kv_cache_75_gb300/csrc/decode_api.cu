@@ -51,12 +51,15 @@ extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, 
     return ws_layout(num_seqs, num_heads, head_size, max_parts_of(max_seq_len, P)).bytes;
 }
 
-extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
-                               const int32_t* block_table, int32_t max_blocks_per_seq,
-                               const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
-                               int32_t num_heads, float scale, int32_t partition_size,
-                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                               pa_stream_t stream) {
+namespace pa {
+namespace {
+
+// pa_decode, and pa_decode_append when k_new / v_new are given
+pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                       const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                       int32_t num_seqs, int32_t max_seq_len, int32_t num_heads, float scale,
+                       int32_t partition_size, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                       pa_stream_t stream, const void* k_new, const void* v_new) {
     pa_status st = check_cache(cache);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
@@ -66,6 +69,10 @@ extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const
     if (out == nullptr || q == nullptr || block_table == nullptr || seq_lens == nullptr)
         return PA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u))
+        return PA_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PA_ERR_INVALID_ARG;
+    if (k_new != nullptr &&
+        ((reinterpret_cast<uintptr_t>(k_new) & 15u) || (reinterpret_cast<uintptr_t>(v_new) & 15u)))
         return PA_ERR_INVALID_ARG;
     if (num_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     const int group = num_heads / cache->num_kv_heads;
@@ -110,6 +117,10 @@ extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const
     const float k_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->k_scale : 1.f;
     p.qk_scale = scale * k_scale * 1.4426950408889634f;
     p.v_scale = cache->kv_dtype == PA_FP8_E4M3 ? cache->v_scale : 1.f;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_scale_w = cache->k_scale;
+    p.v_scale_w = cache->v_scale;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 #define PA_BS(KV)                                                       \
     if (bs == 16) return launch_decode_##KV##_bs16(p, q_dtype, D, group, s); \
@@ -119,4 +130,33 @@ extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const
     if (cache->kv_dtype == PA_BF16) { PA_BS(bf16) }
     PA_BS(fp8)
 #undef PA_BS
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                               const int32_t* block_table, int32_t max_blocks_per_seq,
+                               const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                               int32_t num_heads, float scale, int32_t partition_size,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                               pa_stream_t stream) {
+    return pa::decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                            max_seq_len, num_heads, scale, partition_size, workspace, workspace_bytes, dev_status,
+                            stream, nullptr, nullptr);
+}
+
+extern "C" pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                      pa_dtype q_dtype, const pa_kv_cache* cache, const int32_t* block_table,
+                                      int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                                      int32_t max_seq_len, int32_t num_heads, float scale,
+                                      int32_t partition_size, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_status, pa_stream_t stream) {
+    if (k_new == nullptr || v_new == nullptr) return num_seqs == 0 ? PA_OK : PA_ERR_INVALID_ARG;
+    if (cache != nullptr && cache->kv_dtype == PA_FP8_E4M3 &&
+        !(cache->k_scale > 0.f && cache->v_scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    return pa::decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                            max_seq_len, num_heads, scale, partition_size, workspace, workspace_bytes, dev_status,
+                            stream, k_new, v_new);
 }

@@ -57,6 +57,11 @@ struct DecodeParams {
     int32_t stages;     // ring depth
     float qk_scale;     // scale * k_scale * log2(e)
     float v_scale;
+    // append mode: the new token of every sequence (position L-1), written to
+    // the cache and attended in the same launch; [B][Hkv][D] of the query type
+    const void* k_new;
+    const void* v_new;
+    float k_scale_w, v_scale_w;  // E4M3 cache: the write's scales
 };
 
 template <int QDT, int KVDT, int D, int G, int BS>
@@ -286,7 +291,62 @@ __device__ __forceinline__ uint64_t pair_of<PA_F16>(uint32_t w) {
     return pk2(f.x, f.y);
 }
 
-template <int QDT, int KVDT, int D, int G, int BS>
+// Append mode: the new token's K and V rows of (sequence it.b, KV head
+// it.kvh), in the cache's type (16-bit: the bits; E4M3: IEEE x/scale rounded
+// to nearest even with saturation, as pa_kv_cache_write stores it), go to the
+// cache slot of position L-1 and to row (L-1) % BS of the stage page at
+// `page` (K at page, V SPAGES pages further).  The whole warp takes part.
+template <typename C, int QDT, int KVDT>
+__device__ __forceinline__ void append_row(const DecodeParams& p, const Item& it, int32_t blk, uint8_t* page,
+                                           int lane) {
+    constexpr int D = C::ROWB / C::KB;
+    const int r = (it.L - 1) % (C::PAGE / C::ROWB);
+    const int64_t src_row = (static_cast<int64_t>(it.b) * p.num_kv_heads + it.kvh) * D;
+    const int64_t cache_off = (static_cast<int64_t>(blk) * p.num_kv_heads + it.kvh) * C::PAGE + r * C::ROWB;
+    uint8_t* srow_k = page + r * C::ROWB;
+    uint8_t* srow_v = page + C::SPAGES * C::PAGE + r * C::ROWB;
+    if constexpr (C::KB == 2) {
+        // 16-byte chunks: D*2 bytes per row
+        constexpr int CH = D * 2 / 16;
+        for (int c = lane; c < 2 * CH; c += 32) {
+            const bool isv = c >= CH;
+            const int cc = isv ? c - CH : c;
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(
+                                      static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src_row * 2) + cc);
+            *reinterpret_cast<uint4*>((isv ? srow_v : srow_k) + cc * 16) = x;
+            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(isv ? p.v_cache : p.k_cache) + cache_off + cc * 16) = x;
+        }
+    } else {
+        // E4M3: 8 input elements (16 bytes) -> 8 codes (8 bytes) per lane step
+        constexpr int CH = D / 8;
+        for (int c = lane; c < 2 * CH; c += 32) {
+            const bool isv = c >= CH;
+            const int cc = isv ? c - CH : c;
+            const float sc = isv ? p.v_scale_w : p.k_scale_w;
+            const uint4 x = __ldg(reinterpret_cast<const uint4*>(
+                                      static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src_row * 2) + cc);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+            uint32_t codes[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float2 a = kv_pair<QDT>(w[2 * h]), b = kv_pair<QDT>(w[2 * h + 1]);
+                const uint32_t lo = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc)), __NV_SATFINITE, __NV_E4M3));
+                const uint32_t hi = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                    make_float2(__fdiv_rn(b.x, sc), __fdiv_rn(b.y, sc)), __NV_SATFINITE, __NV_E4M3));
+                codes[h] = lo | (hi << 16);
+            }
+            const uint2 y = make_uint2(codes[0], codes[1]);
+            *reinterpret_cast<uint2*>((isv ? srow_v : srow_k) + cc * 8) = y;
+            *reinterpret_cast<uint2*>(const_cast<uint8_t*>(isv ? p.v_cache : p.k_cache) + cache_off + cc * 8) = y;
+        }
+    }
+}
+
+// APPEND: the new token of every sequence is written and attended in the
+// same launch (pa_decode_append); a separate instantiation keeps the plain
+// decode's producer loop as lean as it was.
+template <int QDT, int KVDT, int D, int G, int BS, bool APPEND>
 __global__ void __maxnreg__((DecodeCfg<QDT, KVDT, D, G, BS>::MAX_REGS))
 paged_decode_kernel(const DecodeParams p) {
     using C = DecodeCfg<QDT, KVDT, D, G, BS>;
@@ -357,20 +417,71 @@ paged_decode_kernel(const DecodeParams p) {
                     int32_t ids[C::SPAGES];
 #pragma unroll
                     for (int k = 0; k < C::SPAGES; ++k) ids[k] = __shfl_sync(0xffffffffu, id, k0 + k);
-                    if (lane == 0) {
-                        if (fill >= static_cast<uint32_t>(S))
+                    if constexpr (!APPEND) {
+                        // plain decode: one lane fills the stage
+                        if (lane == 0) {
+                            if (fill >= static_cast<uint32_t>(S))
+                                ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status, abort_flag);
+                            if (ok) {
+                                const uint32_t bar = full0 + 8u * stage;
+                                const uint32_t dst = smem_addr(ring) + stage * C::STAGE_BYTES;
+                                int mask = 0;
+                                uint32_t bytes = 0;
+    #pragma unroll
+                                for (int k = 0; k < C::SPAGES; ++k) {
+                                    if (k0 + k >= cnt) continue;  // past the item's pages
+                                    if (ids[k] >= 0 && ids[k] < p.num_blocks) {
+                                        mask |= 1 << k;
+                                        bytes += 2u * C::PAGE;
+                                    } else {
+                                        report(p.status, PA_ERR_BAD_BLOCK);
+                                    }
+                                }
+                                stage_mask[stage] = mask;
+                                if (bytes) {
+                                    mbar_expect_tx(bar, bytes);
+    #pragma unroll
+                                    for (int k = 0; k < C::SPAGES; ++k) {
+                                        if (!(mask & (1 << k))) continue;
+                                        const int64_t off = ids[k] * blk_stride + head_off;
+                                        bulk_g2s_hint(dst + k * C::PAGE, p.k_cache + off, C::PAGE, bar, policy);
+                                        bulk_g2s_hint(dst + (C::SPAGES + k) * C::PAGE, p.v_cache + off, C::PAGE, bar,
+                                                      policy);
+                                    }
+                                    issued = fill + 1;
+                                } else {
+                                    mbar_arrive(bar);
+                                }
+                            }
+                        }
+                    } else {
+                        // append mode: the page holding the new token (position L-1,
+                        // in the item's last partition) copies only the rows before it;
+                        // the warp writes the new row into the stage and the cache
+                        int pk = -1;  // page of this stage that holds the new token
+                        if (it.L > 0 && it.t1 == it.L) {
+                            const int jn = (it.L - 1) / BS - (jb + k0);
+                            if (jn >= 0 && jn < C::SPAGES && jn < cnt - k0) pk = jn;
+                        }
+                        if (lane == 0 && fill >= static_cast<uint32_t>(S))
                             ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status, abort_flag);
-                        if (ok) {
+                        ok = __shfl_sync(0xffffffffu, ok, 0);
+                        if (ok && pk >= 0 && ids[pk] >= 0 && ids[pk] < p.num_blocks)
+                            append_row<C, QDT, KVDT>(p, it, ids[pk], ring + stage * C::STAGE_BYTES + pk * C::PAGE,
+                                                     lane);
+                        __syncwarp();
+                        if (lane == 0 && ok) {
                             const uint32_t bar = full0 + 8u * stage;
                             const uint32_t dst = smem_addr(ring) + stage * C::STAGE_BYTES;
+                            const uint32_t rn = static_cast<uint32_t>((it.L - 1) % BS);  // rows before the new one
                             int mask = 0;
                             uint32_t bytes = 0;
-#pragma unroll
+    #pragma unroll
                             for (int k = 0; k < C::SPAGES; ++k) {
                                 if (k0 + k >= cnt) continue;  // past the item's pages
                                 if (ids[k] >= 0 && ids[k] < p.num_blocks) {
                                     mask |= 1 << k;
-                                    bytes += 2u * C::PAGE;
+                                    bytes += 2u * (k == pk ? rn * C::ROWB : C::PAGE);
                                 } else {
                                     report(p.status, PA_ERR_BAD_BLOCK);
                                 }
@@ -378,13 +489,14 @@ paged_decode_kernel(const DecodeParams p) {
                             stage_mask[stage] = mask;
                             if (bytes) {
                                 mbar_expect_tx(bar, bytes);
-#pragma unroll
+    #pragma unroll
                                 for (int k = 0; k < C::SPAGES; ++k) {
                                     if (!(mask & (1 << k))) continue;
+                                    const uint32_t n = k == pk ? rn * C::ROWB : C::PAGE;
+                                    if (n == 0) continue;
                                     const int64_t off = ids[k] * blk_stride + head_off;
-                                    bulk_g2s_hint(dst + k * C::PAGE, p.k_cache + off, C::PAGE, bar, policy);
-                                    bulk_g2s_hint(dst + (C::SPAGES + k) * C::PAGE, p.v_cache + off, C::PAGE, bar,
-                                                  policy);
+                                    bulk_g2s_hint(dst + k * C::PAGE, p.k_cache + off, n, bar, policy);
+                                    bulk_g2s_hint(dst + (C::SPAGES + k) * C::PAGE, p.v_cache + off, n, bar, policy);
                                 }
                                 issued = fill + 1;
                             } else {

@@ -29,9 +29,10 @@ pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     const DecodeSmem L = DecodeSmem::make(p.stages, C::STAGE_BYTES, C::QBYTES, C::MERGE_FLOATS, p.num_seqs);
     const int smem = static_cast<int>(L.total) + 1024;  // slack for the 1 KB base alignment
     if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
-    auto kern = paged_decode_kernel<QDT, KVDT, D, G, BS>;
-    static LaunchCache cache;
-    const int per_sm = blocks_per_sm(kern, C::THREADS, smem, cache);
+    const bool append = p.k_new != nullptr;
+    auto kern = append ? paged_decode_kernel<QDT, KVDT, D, G, BS, true> : paged_decode_kernel<QDT, KVDT, D, G, BS, false>;
+    static LaunchCache cache, cache_append;
+    const int per_sm = blocks_per_sm(kern, C::THREADS, smem, append ? cache_append : cache);
     if (per_sm <= 0) return PA_ERR_CUDA;
     const int sms = device_sm_count();
     const int64_t max_items = static_cast<int64_t>(p.num_seqs) * p.num_kv_heads * p.max_parts;
