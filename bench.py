@@ -238,6 +238,11 @@ class DecodeStep:
     def write(self):
         self.pk.pa_kv_cache_write(self.cache, self.k_new, self.v_new, self.slots, self.status)
 
+    def append(self):
+        """The same step through pa_decode_append: write and attend in one launch."""
+        self.pk.pa_decode_append(self.out, self.q, self.k_new, self.v_new, self.cache, self.bt, self.lens,
+                                 self.max_len, self.case.scale, self.P, self.ws, self.status)
+
     def decode(self, q=None, out=None, bt=None, lens=None):
         self.pk.pa_decode(self.out if out is None else out, self.q if q is None else q, self.cache,
                           self.bt if bt is None else bt, self.lens if lens is None else lens, self.max_len,
@@ -349,6 +354,25 @@ def timed_decode(step: DecodeStep, steps, warmup, world, flush):
     if st != 0:
         raise RuntimeError("device status %d during the benchmark" % st)
     return total_ms, decode_ms, clk.summary()
+
+
+def timed_append(step: DecodeStep, steps, warmup, flush):
+    """Mean ms of one fused step (pa_decode_append), each step timed on its
+    own with the L2 flush (if any) outside the timed interval."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.append()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        evs[i][0].record(stream)
+        step.append()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError("device status %d in the fused step" % int(step.status.item()))
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
 
 
 def timed_graph(step: DecodeStep, steps, flush):
@@ -726,6 +750,7 @@ def run_ours(args):
     hbm, _, _, peak_kind = measured_peaks()
     achieved = step.kv_bytes / (decode_ms / 1e3) / 1e9
     graph_ms = timed_graph(step, args.steps, flush) if small else None
+    fused_ms = timed_append(step, args.steps, args.warmup, flush)
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((args.workload, src_hash))
     line = {
@@ -757,6 +782,10 @@ def run_ours(args):
                 "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step * args.steps,
+        "fused_append": {"ms_per_step": round(fused_ms, 5),
+                         "value": round(step.kv_bytes / (fused_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                         "note": "the same step (new token written, then attended) as one pa_decode_append launch; "
+                                 "each step timed on its own"},
         "graph": None if graph_ms is None else {
             "us_per_step": round(graph_ms * 1e3, 2), "value": round(step.kv_bytes / (graph_ms / 1e3) / 1e9, 2),
             "unit": "GB/s", "note": "the same step captured once as a CUDA graph and replayed (not in value)"},

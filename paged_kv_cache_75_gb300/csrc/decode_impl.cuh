@@ -417,8 +417,9 @@ paged_decode_kernel(const DecodeParams p) {
                     int32_t ids[C::SPAGES];
 #pragma unroll
                     for (int k = 0; k < C::SPAGES; ++k) ids[k] = __shfl_sync(0xffffffffu, id, k0 + k);
-                    if constexpr (!APPEND) {
-                        // plain decode: one lane fills the stage
+                    // one lane fills the stage (every stage of a plain decode, and
+                    // the stages of an append that do not hold the new token)
+                    auto fill_lane0 = [&]() {
                         if (lane == 0) {
                             if (fill >= static_cast<uint32_t>(S))
                                 ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status, abort_flag);
@@ -427,7 +428,7 @@ paged_decode_kernel(const DecodeParams p) {
                                 const uint32_t dst = smem_addr(ring) + stage * C::STAGE_BYTES;
                                 int mask = 0;
                                 uint32_t bytes = 0;
-    #pragma unroll
+#pragma unroll
                                 for (int k = 0; k < C::SPAGES; ++k) {
                                     if (k0 + k >= cnt) continue;  // past the item's pages
                                     if (ids[k] >= 0 && ids[k] < p.num_blocks) {
@@ -440,7 +441,7 @@ paged_decode_kernel(const DecodeParams p) {
                                 stage_mask[stage] = mask;
                                 if (bytes) {
                                     mbar_expect_tx(bar, bytes);
-    #pragma unroll
+#pragma unroll
                                     for (int k = 0; k < C::SPAGES; ++k) {
                                         if (!(mask & (1 << k))) continue;
                                         const int64_t off = ids[k] * blk_stride + head_off;
@@ -454,6 +455,9 @@ paged_decode_kernel(const DecodeParams p) {
                                 }
                             }
                         }
+                    };
+                    if constexpr (!APPEND) {
+                        fill_lane0();
                     } else {
                         // append mode: the page holding the new token (position L-1,
                         // in the item's last partition) copies only the rows before it;
@@ -463,44 +467,48 @@ paged_decode_kernel(const DecodeParams p) {
                             const int jn = (it.L - 1) / BS - (jb + k0);
                             if (jn >= 0 && jn < C::SPAGES && jn < cnt - k0) pk = jn;
                         }
-                        if (lane == 0 && fill >= static_cast<uint32_t>(S))
-                            ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status, abort_flag);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (ok && pk >= 0 && ids[pk] >= 0 && ids[pk] < p.num_blocks)
-                            append_row<C, QDT, KVDT>(p, it, ids[pk], ring + stage * C::STAGE_BYTES + pk * C::PAGE,
-                                                     lane);
-                        __syncwarp();
-                        if (lane == 0 && ok) {
-                            const uint32_t bar = full0 + 8u * stage;
-                            const uint32_t dst = smem_addr(ring) + stage * C::STAGE_BYTES;
-                            const uint32_t rn = static_cast<uint32_t>((it.L - 1) % BS);  // rows before the new one
-                            int mask = 0;
-                            uint32_t bytes = 0;
-    #pragma unroll
-                            for (int k = 0; k < C::SPAGES; ++k) {
-                                if (k0 + k >= cnt) continue;  // past the item's pages
-                                if (ids[k] >= 0 && ids[k] < p.num_blocks) {
-                                    mask |= 1 << k;
-                                    bytes += 2u * (k == pk ? rn * C::ROWB : C::PAGE);
-                                } else {
-                                    report(p.status, PA_ERR_BAD_BLOCK);
-                                }
-                            }
-                            stage_mask[stage] = mask;
-                            if (bytes) {
-                                mbar_expect_tx(bar, bytes);
-    #pragma unroll
+                        if (pk < 0) {
+                            fill_lane0();
+                        } else {
+                            if (lane == 0 && fill >= static_cast<uint32_t>(S))
+                                ok = mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status, abort_flag);
+                            ok = __shfl_sync(0xffffffffu, ok, 0);
+                            if (ok && pk >= 0 && ids[pk] >= 0 && ids[pk] < p.num_blocks)
+                                append_row<C, QDT, KVDT>(p, it, ids[pk], ring + stage * C::STAGE_BYTES + pk * C::PAGE,
+                                                         lane);
+                            __syncwarp();
+                            if (lane == 0 && ok) {
+                                const uint32_t bar = full0 + 8u * stage;
+                                const uint32_t dst = smem_addr(ring) + stage * C::STAGE_BYTES;
+                                const uint32_t rn = static_cast<uint32_t>((it.L - 1) % BS);  // rows before the new one
+                                int mask = 0;
+                                uint32_t bytes = 0;
+#pragma unroll
                                 for (int k = 0; k < C::SPAGES; ++k) {
-                                    if (!(mask & (1 << k))) continue;
-                                    const uint32_t n = k == pk ? rn * C::ROWB : C::PAGE;
-                                    if (n == 0) continue;
-                                    const int64_t off = ids[k] * blk_stride + head_off;
-                                    bulk_g2s_hint(dst + k * C::PAGE, p.k_cache + off, n, bar, policy);
-                                    bulk_g2s_hint(dst + (C::SPAGES + k) * C::PAGE, p.v_cache + off, n, bar, policy);
+                                    if (k0 + k >= cnt) continue;  // past the item's pages
+                                    if (ids[k] >= 0 && ids[k] < p.num_blocks) {
+                                        mask |= 1 << k;
+                                        bytes += 2u * (k == pk ? rn * C::ROWB : C::PAGE);
+                                    } else {
+                                        report(p.status, PA_ERR_BAD_BLOCK);
+                                    }
                                 }
-                                issued = fill + 1;
-                            } else {
-                                mbar_arrive(bar);
+                                stage_mask[stage] = mask;
+                                if (bytes) {
+                                    mbar_expect_tx(bar, bytes);
+#pragma unroll
+                                    for (int k = 0; k < C::SPAGES; ++k) {
+                                        if (!(mask & (1 << k))) continue;
+                                        const uint32_t n = k == pk ? rn * C::ROWB : C::PAGE;
+                                        if (n == 0) continue;
+                                        const int64_t off = ids[k] * blk_stride + head_off;
+                                        bulk_g2s_hint(dst + k * C::PAGE, p.k_cache + off, n, bar, policy);
+                                        bulk_g2s_hint(dst + (C::SPAGES + k) * C::PAGE, p.v_cache + off, n, bar, policy);
+                                    }
+                                    issued = fill + 1;
+                                } else {
+                                    mbar_arrive(bar);
+                                }
                             }
                         }
                     }
@@ -627,45 +635,45 @@ paged_decode_kernel(const DecodeParams p) {
                 // steps' dot products and shuffle reductions interleave (twice the
                 // independent chains), and the softmax takes one lazy-rescale
                 // decision per pair
-    #pragma unroll
+#pragma unroll
                 for (int u0 = 0; u0 < C::SUB; u0 += C::NB) {
                     bool valid[C::NB];
                     uint32_t vw[C::NB][C::NV][4];
                     float sc[C::NB][C::GW];
-    #pragma unroll
+#pragma unroll
                     for (int h = 0; h < C::NB; ++h) {
                         const int tis = (u0 + h) * C::TPI;  // step offset inside the stage
                         valid[h] = FULL || (((mask >> ((tis + tw * C::TG + tg) / BS)) & 1) && tok0 + tis < it.t1);
                         // value chunks are loaded up front (unconditionally: the
                         // rows are in shared memory) so the loads overlap the QK math
-    #pragma unroll
+#pragma unroll
                         for (int v = 0; v < C::NV; ++v) load_chunk<C::VB>(Vp + tis * C::ROWB + v * C::LPT * C::VB, vw[h][v]);
                     }
                     // ---- QK: this lane's chunks of both steps, then butterflies over the group ----
                     {
                         float s0[C::NB][C::GW], s1[C::NB][C::GW];
-    #pragma unroll
+#pragma unroll
                         for (int h = 0; h < C::NB; ++h)
-    #pragma unroll
+#pragma unroll
                             for (int g = 0; g < C::GW; ++g) s0[h][g] = s1[h][g] = 0.f;
-    #pragma unroll
+#pragma unroll
                         for (int h = 0; h < C::NB; ++h) {
                             const uint8_t* krow = Kp + (u0 + h) * C::TPI * C::ROWB;
-    #pragma unroll
+#pragma unroll
                             for (int v = 0; v < C::NV; ++v) {
                                 uint32_t w[4];
                                 load_chunk<C::VB>(krow + v * C::LPT * C::VB, w);
-    #pragma unroll
+#pragma unroll
                                 for (int x = 0; x < C::VB / 4; ++x) {
                                     if constexpr (C::KB == 2) {
                                         const int pi = (v * C::EV) / 2 + x;
-    #pragma unroll
+#pragma unroll
                                         for (int g = 0; g < C::GW; ++g)
                                             fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi], w[x]);
                                     } else {
                                         const uint32_t h0 = e4m3x2_to_h2(w[x]), h1 = e4m3x2_to_h2(w[x] >> 16);
                                         const int pi = (v * C::EV) / 2 + 2 * x;
-    #pragma unroll
+#pragma unroll
                                         for (int g = 0; g < C::GW; ++g) {
                                             fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi], h0);
                                             fma_mixed2<KT>(s0[h][g], s1[h][g], qw[g][pi + 1], h1);
@@ -675,34 +683,34 @@ paged_decode_kernel(const DecodeParams p) {
                             }
                         }
                         float t[C::NB][C::GW];
-    #pragma unroll
+#pragma unroll
                         for (int h = 0; h < C::NB; ++h)
-    #pragma unroll
+#pragma unroll
                             for (int g = 0; g < C::GW; ++g) t[h][g] = s0[h][g] + s1[h][g];
-    #pragma unroll
+#pragma unroll
                         for (int o = 1; o < C::LPT; o <<= 1)
-    #pragma unroll
+#pragma unroll
                             for (int h = 0; h < C::NB; ++h)
-    #pragma unroll
+#pragma unroll
                                 for (int g = 0; g < C::GW; ++g) t[h][g] += __shfl_xor_sync(0xffffffffu, t[h][g], o);
-    #pragma unroll
+#pragma unroll
                         for (int h = 0; h < C::NB; ++h)
-    #pragma unroll
+#pragma unroll
                             for (int g = 0; g < C::GW; ++g) sc[h][g] = (FULL || valid[h]) ? t[h][g] * qk_scale : -INFINITY;
                     }
                     // ---- online softmax of this group over the NB steps, lazy rescale (warp-uniform test) ----
                     float smax[C::GW];
-    #pragma unroll
+#pragma unroll
                     for (int g = 0; g < C::GW; ++g) {
                         smax[g] = sc[0][g];
-    #pragma unroll
+#pragma unroll
                         for (int h = 1; h < C::NB; ++h) smax[g] = fmaxf(smax[g], sc[h][g]);
                     }
                     bool need = false;
-    #pragma unroll
+#pragma unroll
                     for (int g = 0; g < C::GW; ++g) need |= smax[g] > m[g] + kTau;
                     if (__any_sync(0xffffffffu, need)) {
-    #pragma unroll
+#pragma unroll
                         for (int g = 0; g < C::GW; ++g) {
                             const float mx = smax[g];
                             const bool r = mx > m[g] + kTau;
@@ -710,38 +718,38 @@ paged_decode_kernel(const DecodeParams p) {
                             m[g] = r ? mx : m[g];
                             l[g] *= a;
                             const uint64_t aa = pk2(a, a);
-    #pragma unroll
+#pragma unroll
                             for (int x = 0; x < C::PL; ++x) acc[g][x] = fmul2(acc[g][x], aa);
                         }
                     }
                     uint64_t pp[C::NB][C::GW];
-    #pragma unroll
+#pragma unroll
                     for (int h = 0; h < C::NB; ++h)
-    #pragma unroll
+#pragma unroll
                         for (int g = 0; g < C::GW; ++g) {
                             const float pr = (FULL || valid[h]) ? fast_exp2(sc[h][g] - m[g]) : 0.f;
                             l[g] += pr;
                             pp[h][g] = pk2(pr, pr);
                         }
                     // ---- PV over this lane's value chunks (masked rows are not read) ----
-    #pragma unroll
+#pragma unroll
                     for (int h = 0; h < C::NB; ++h) {
                         if (FULL || valid[h]) {
-    #pragma unroll
+#pragma unroll
                             for (int v = 0; v < C::NV; ++v) {
                                 const uint32_t (&w)[4] = vw[h][v];
-    #pragma unroll
+#pragma unroll
                                 for (int x = 0; x < C::VB / 4; ++x) {
                                     if constexpr (C::KB == 2) {
                                         const uint64_t v2 = pair_of<KVDT>(w[x]);
                                         const int pi = (v * C::EV) / 2 + x;
-    #pragma unroll
+#pragma unroll
                                         for (int g = 0; g < C::GW; ++g) acc[g][pi] = ffma2(pp[h][g], v2, acc[g][pi]);
                                     } else {
                                         const uint64_t v0 = pair_of<PA_F16>(e4m3x2_to_h2(w[x]));
                                         const uint64_t v1 = pair_of<PA_F16>(e4m3x2_to_h2(w[x] >> 16));
                                         const int pi = (v * C::EV) / 2 + 2 * x;
-    #pragma unroll
+#pragma unroll
                                         for (int g = 0; g < C::GW; ++g) {
                                             acc[g][pi] = ffma2(pp[h][g], v0, acc[g][pi]);
                                             acc[g][pi + 1] = ffma2(pp[h][g], v1, acc[g][pi + 1]);
