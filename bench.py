@@ -456,11 +456,43 @@ def timed_prefill_e2e(step: PrefillStep, steps, warmup, world):
     return start.elapsed_time(end), h2d, d2h
 
 
+def timed_split(step: PrefillStep, steps, warmup):
+    """The mixed batch through pa_varlen_mixed: the varlen kernel takes the
+    prefill sequences, the decode kernel the trailing one-token sequences.
+    Returns mean ms per step (write + attention)."""
+    import paged_kv_cache_75_gb300 as pk
+    B = len(step.lq)
+    host_cu_q = np.concatenate([[0], np.cumsum(step.lq)]).astype(np.int32)
+    ws_n = pk.pa_varlen_mixed_workspace_size(B, step.case.num_heads, step.case.head_size, step.max_k,
+                                             step.case.block_size)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=step.device)
+    stream = torch.cuda.current_stream()
+
+    def one():
+        step.write()
+        pk.pa_varlen_mixed(step.out, step.q, step.cache, step.bt, step.cu_q, step.cu_k, host_cu_q, step.max_q,
+                           step.max_k, step.case.scale, True, ws, step.status)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError("device status %d in the dispatched step" % int(step.status.item()))
+    return start.elapsed_time(end) / steps
+
+
 def run_prefill(args, case, wname, dev, rank, world):
     step = PrefillStep(case, dev, wname)
     total_ms, main_ms, clocks = timed_prefill(step, args.steps, args.warmup, world)
     total_ms, flops_sum = aggregate(total_ms, float(step.flops) * args.steps, world)
     e2e_ms, h2d, d2h = timed_prefill_e2e(step, args.steps, args.warmup, world)
+    split_ms = timed_split(step, args.steps, args.warmup)
     e2e_ms, flops_e2e = aggregate(e2e_ms, float(step.flops) * args.steps, world)
     _, tflops_peak, tflops_sustained, peak_kind = measured_peaks()
     achieved = step.flops / (main_ms / 1e3) / 1e12
@@ -489,6 +521,11 @@ def run_prefill(args, case, wname, dev, rank, world):
                 "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": step.launches_per_step * args.steps,
+        "split": None if split_ms is None else {
+            "ms_per_step": round(split_ms, 5), "value": round(step.flops / (split_ms / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s",
+            "note": "the same step through pa_varlen_mixed: the varlen kernel on the prefill sequences, "
+                    "the decode kernel on the trailing one-token sequences (same FLOPs counted)"},
         "roofline": {"bound": "tensor", "kernel": "pa_prefill_varlen", "achieved": round(achieved, 2),
                      "peak": tflops_sustained, "unit": "TFLOP/s", "frac": round(achieved / tflops_sustained, 4),
                      "peak_kind": "of %s (bf16 dense, sustained)" % peak_kind,

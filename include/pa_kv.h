@@ -275,6 +275,32 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
                            int32_t* dev_status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Mixed batch dispatcher: a varlen batch (as pa_prefill_varlen) whose
+ * trailing sequences have one query token each is split -- the leading
+ * sequences go to the varlen tensor-core kernel, the trailing one-token run
+ * to the decode kernel, which reads each length as cu_seq_lens_k[b+1] -
+ * cu_seq_lens_k[b] ("Paged 어텐션": the decode path is the faster one for
+ * single-query sequences, the varlen path takes the prefills).  A single
+ * query sees all of its keys, causal or not, so the split computes the same
+ * attention.
+ *
+ * host_cu_seq_lens_q: host int32 [num_seqs+1], a copy of cu_seq_lens_q (the
+ *   split is decided on the host; nothing is read back from the device).
+ * workspace: device scratch of pa_varlen_mixed_workspace_size(...) bytes,
+ *   16-byte aligned (NULL if that is 0), for the decode kernel's partitions.
+ * Everything else as pa_prefill_varlen; head_size 64 is only served when
+ * every sequence is a one-token sequence.
+ * ------------------------------------------------------------------------- */
+size_t pa_varlen_mixed_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                                      int32_t max_seqlen_k, int32_t block_size);
+pa_status pa_varlen_mixed(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                          const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* cu_seq_lens_q,
+                          const int32_t* cu_seq_lens_k, const int32_t* host_cu_seq_lens_q, int32_t num_seqs,
+                          int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t num_heads, float scale,
+                          int32_t causal, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                          pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Varlen attention over packed K/V: "Paged 어텐션", Varlen 경로 -- the batch's
  * keys and values are contiguous tensors [Σk][num_kv_heads][head_size]
  * indexed by cu_seq_lens_k (no cache, no block table), queries as in

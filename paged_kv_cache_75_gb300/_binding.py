@@ -57,6 +57,9 @@ def library():
             "pa_pool_seq_len": ([vp, i64], i32),
             "pa_slot_mapping": ([vp, i32, i32, i32, vp, vp, i64, vp], C.c_int),
             "pa_swap_blocks": ([pc, vp, vp, i64, vp, i32, i32, vp, vp], C.c_int),
+            "pa_varlen_mixed_workspace_size": ([i32, i32, i32, i32, i32], sz),
+            "pa_varlen_mixed": ([vp, vp, C.c_int, pc, vp, i32, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp, sz, vp,
+                                 vp], C.c_int),
             "pa_decode_append": ([vp, vp, vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, sz, vp,
                                   vp], C.c_int),
             "pa_prefill_varlen_packed": ([vp, vp, vp, vp, C.c_int, vp, vp, i32, i32, i32, i64, i32, i32, i32, f32,
@@ -195,6 +198,37 @@ def pa_prefill_varlen_packed(out: torch.Tensor, q: torch.Tensor, k: torch.Tensor
                                             max_seqlen_q, max_seqlen_k, k.shape[0], q.shape[1], k.shape[1],
                                             q.shape[2], scale, 1 if causal else 0, _ptr(dev_status), _stream(q))
     _check(st, "pa_prefill_varlen_packed")
+
+
+def pa_varlen_mixed_workspace_size(num_seqs, num_heads, head_size, max_seqlen_k, block_size) -> int:
+    return int(library().pa_varlen_mixed_workspace_size(num_seqs, num_heads, head_size, max_seqlen_k, block_size))
+
+
+def pa_varlen_mixed(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,
+                    cu_seq_lens_q: torch.Tensor, cu_seq_lens_k: torch.Tensor, host_cu_seq_lens_q, max_seqlen_q: int,
+                    max_seqlen_k: int, scale: float, causal: bool = True, workspace: Optional[torch.Tensor] = None,
+                    dev_status: Optional[torch.Tensor] = None):
+    """pa_prefill_varlen with the trailing one-token sequences sent to the
+    decode kernel; host_cu_seq_lens_q: the same offsets on the host."""
+    import numpy as np
+    _need(q, "q")
+    _need(out, "out", q.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(cu_seq_lens_q, "cu_seq_lens_q", torch.int32)
+    _need(cu_seq_lens_k, "cu_seq_lens_k", torch.int32)
+    hq = np.ascontiguousarray(host_cu_seq_lens_q, np.int32)
+    if hq.shape[0] != cu_seq_lens_q.numel():
+        raise ValueError("host_cu_seq_lens_q must match cu_seq_lens_q")
+    if workspace is not None:
+        _need(workspace, "workspace")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    cs = cache.c_struct()
+    st = library().pa_varlen_mixed(_ptr(out), _ptr(q), torch_dtype_code(q.dtype), C.byref(cs), _ptr(block_table),
+                                   block_table.shape[1], _ptr(cu_seq_lens_q), _ptr(cu_seq_lens_k),
+                                   hq.ctypes.data_as(C.c_void_p), hq.shape[0] - 1, int(max_seqlen_q),
+                                   int(max_seqlen_k), q.shape[1], float(scale), 1 if causal else 0, _ptr(workspace),
+                                   ws_bytes, _ptr(dev_status), _stream(q))
+    _check(st, "pa_varlen_mixed")
 
 
 def pa_swap_blocks(cache: KVCache, host_k: torch.Tensor, host_v: torch.Tensor, pairs: torch.Tensor,

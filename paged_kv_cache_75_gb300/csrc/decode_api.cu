@@ -59,14 +59,15 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
                        const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                        int32_t num_seqs, int32_t max_seq_len, int32_t num_heads, float scale,
                        int32_t partition_size, void* workspace, size_t workspace_bytes, int32_t* dev_status,
-                       pa_stream_t stream, const void* k_new, const void* v_new) {
+                       pa_stream_t stream, const void* k_new, const void* v_new,
+                       const int32_t* cu_seq_lens_k = nullptr) {
     pa_status st = check_cache(cache);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
         partition_size < 0 || !std::isfinite(scale))
         return PA_ERR_INVALID_ARG;
     if (num_seqs == 0) return PA_OK;
-    if (out == nullptr || q == nullptr || block_table == nullptr || seq_lens == nullptr)
+    if (out == nullptr || q == nullptr || block_table == nullptr || (seq_lens == nullptr && cu_seq_lens_k == nullptr))
         return PA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(out) & 15u) || (reinterpret_cast<uintptr_t>(q) & 15u))
         return PA_ERR_INVALID_ARG;
@@ -102,6 +103,7 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     p.v_cache = static_cast<const uint8_t*>(cache->v_cache);
     p.block_table = block_table;
     p.seq_lens = seq_lens;
+    p.cu_seq_lens_k = cu_seq_lens_k;
     p.ws_lse = w.bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse_off) : nullptr;
     p.ws_o = w.bytes ? reinterpret_cast<float*>(static_cast<char*>(workspace) + w.o_off) : nullptr;
     p.status = dev_status;
@@ -159,4 +161,43 @@ extern "C" pa_status pa_decode_append(void* out, const void* q, const void* k_ne
     return pa::decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                             max_seq_len, num_heads, scale, partition_size, workspace, workspace_bytes, dev_status,
                             stream, k_new, v_new);
+}
+
+extern "C" size_t pa_varlen_mixed_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                                                 int32_t max_seqlen_k, int32_t block_size) {
+    return pa_decode_workspace_size(num_seqs, num_heads, head_size, max_seqlen_k, block_size, 0);
+}
+
+extern "C" pa_status pa_varlen_mixed(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                                     const int32_t* block_table, int32_t max_blocks_per_seq,
+                                     const int32_t* cu_seq_lens_q, const int32_t* cu_seq_lens_k,
+                                     const int32_t* host_cu_seq_lens_q, int32_t num_seqs, int32_t max_seqlen_q,
+                                     int32_t max_seqlen_k, int32_t num_heads, float scale, int32_t causal,
+                                     void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                                     pa_stream_t stream) {
+    if (num_seqs < 0 || max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (host_cu_seq_lens_q == nullptr || cache == nullptr) return PA_ERR_INVALID_ARG;
+    // the trailing run of one-token sequences goes to the decode kernel
+    int n_dec = 0;
+    while (n_dec < num_seqs &&
+           host_cu_seq_lens_q[num_seqs - n_dec] - host_cu_seq_lens_q[num_seqs - n_dec - 1] == 1)
+        ++n_dec;
+    const int n_pre = num_seqs - n_dec;
+    if (n_pre > 0) {
+        const pa_status st = pa_prefill_varlen(out, q, q_dtype, cache, block_table, max_blocks_per_seq,
+                                               cu_seq_lens_q, cu_seq_lens_k, n_pre, max_seqlen_q, max_seqlen_k,
+                                               num_heads, scale, causal, dev_status, stream);
+        if (st != PA_OK) return st;
+    }
+    if (n_dec > 0) {
+        // one query per sequence: causal or not, it sees all of its keys
+        const int64_t r0 = host_cu_seq_lens_q[n_pre];
+        const int64_t row_bytes = static_cast<int64_t>(num_heads) * cache->head_size * 2;
+        return decode_entry(static_cast<char*>(out) + r0 * row_bytes, static_cast<const char*>(q) + r0 * row_bytes,
+                            q_dtype, cache, block_table + static_cast<int64_t>(n_pre) * max_blocks_per_seq,
+                            max_blocks_per_seq, nullptr, n_dec, max_seqlen_k, num_heads, scale, 0, workspace,
+                            workspace_bytes, dev_status, stream, nullptr, nullptr, cu_seq_lens_k + n_pre);
+    }
+    return PA_OK;
 }

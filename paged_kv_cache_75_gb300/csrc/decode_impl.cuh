@@ -42,6 +42,7 @@ struct DecodeParams {
     const uint8_t* v_cache;
     const int32_t* block_table;
     const int32_t* seq_lens;
+    const int32_t* cu_seq_lens_k;  // when set: L_b = cu[b+1] - cu[b] (seq_lens unused)
     float* ws_lse;  // [B*H*max_parts]
     float* ws_o;    // [B*H*max_parts*D]
     int32_t* status;
@@ -134,7 +135,9 @@ __device__ __forceinline__ int parts_of(int L, int P) { return L <= P ? 1 : (L +
 
 // A length is usable iff 0 <= L <= max_seq_len and L fits the table row.
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
-    int L = __ldg(p.seq_lens + b);
+    // lengths from seq_lens, or as differences of cumulative key lengths
+    int L = p.cu_seq_lens_k != nullptr ? __ldg(p.cu_seq_lens_k + b + 1) - __ldg(p.cu_seq_lens_k + b)
+                                       : __ldg(p.seq_lens + b);
     if (L < 0 || L > p.max_seq_len || static_cast<int64_t>(L) > static_cast<int64_t>(p.max_blocks) * p.block_size)
         return -1;
     return L;
