@@ -26,6 +26,8 @@ cache_write_copy16(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                    const int64_t* __restrict__ slot_mapping, int64_t num_tokens,
                    int64_t token_stride_chunks, int32_t num_kv_heads, int32_t chunks_per_row,
                    int32_t block_size, int64_t num_slots, int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t chunks_per_token = static_cast<int64_t>(num_kv_heads) * chunks_per_row;
     const int64_t total = num_tokens * chunks_per_token;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -64,6 +66,8 @@ cache_write_e4m3(uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
                  int64_t token_stride_chunks, int32_t num_kv_heads, int32_t chunks_per_row,
                  int32_t block_size, int64_t num_slots, float k_scale, float v_scale,
                  int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t chunks_per_token = static_cast<int64_t>(num_kv_heads) * chunks_per_row;
     const int64_t total = num_tokens * chunks_per_token;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -106,6 +110,8 @@ cache_write_scalar(void* __restrict__ k_cache, void* __restrict__ v_cache,
                    int64_t token_stride, int32_t num_kv_heads, int32_t head_size,
                    int32_t block_size, int64_t num_slots, float k_scale, float v_scale,
                    int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t per_token = static_cast<int64_t>(num_kv_heads) * head_size;
     const int64_t total = num_tokens * per_token;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -180,30 +186,32 @@ extern "C" pa_status pa_kv_cache_write(const pa_kv_cache* cache, const void* k, 
     const int sms = device_sm_count();
     if (sms <= 0) return PA_ERR_CUDA;
     if (vec) {
+        cudaError_t st = cudaSuccess;
         const int32_t chunks_per_row = cache->head_size / 8;
         const int64_t total = num_tokens * cache->num_kv_heads * chunks_per_row;
         const int64_t want = (total + kThreads - 1) / kThreads;
         const int grid = static_cast<int>(want < sms * 16 ? want : sms * 16);
         if (cache->kv_dtype == PA_FP8_E4M3) {
             if (in_dtype == PA_F16)
-                cache_write_e4m3<PA_F16><<<grid, kThreads, 0, s>>>(
+                st = launch_pdl(cache_write_e4m3<PA_F16>, grid, kThreads, 0, s,
                     static_cast<uint2*>(cache->k_cache), static_cast<uint2*>(cache->v_cache),
                     static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping,
                     num_tokens, token_stride / 8, cache->num_kv_heads, chunks_per_row,
                     cache->block_size, num_slots, cache->k_scale, cache->v_scale, dev_status);
             else
-                cache_write_e4m3<PA_BF16><<<grid, kThreads, 0, s>>>(
+                st = launch_pdl(cache_write_e4m3<PA_BF16>, grid, kThreads, 0, s,
                     static_cast<uint2*>(cache->k_cache), static_cast<uint2*>(cache->v_cache),
                     static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping,
                     num_tokens, token_stride / 8, cache->num_kv_heads, chunks_per_row,
                     cache->block_size, num_slots, cache->k_scale, cache->v_scale, dev_status);
         } else {
-            cache_write_copy16<<<grid, kThreads, 0, s>>>(
+            st = launch_pdl(cache_write_copy16, grid, kThreads, 0, s,
                 static_cast<uint4*>(cache->k_cache), static_cast<uint4*>(cache->v_cache),
                 static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping,
                 num_tokens, token_stride / 8, cache->num_kv_heads, chunks_per_row,
                 cache->block_size, num_slots, dev_status);
         }
+        if (st != cudaSuccess) return PA_ERR_CUDA;
     } else {
         const int64_t total = num_tokens * row;
         const int64_t want = (total + kThreads - 1) / kThreads;

@@ -125,6 +125,17 @@ __device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Programmatic dependent launch.  The library launches its kernels with
+// programmatic stream serialization, so a kernel may become resident while the
+// previous kernel on the stream is still finishing.  pdl_wait() blocks until
+// every grid this one depends on has completed and its memory operations are
+// visible; each kernel calls it before its first global load or store.
+// pdl_trigger() lets the next launch's blocks be scheduled early (they still
+// wait in their own pdl_wait() for this grid to complete).  Both are no-ops for
+// a launch without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // conversions
 // ---------------------------------------------------------------------------

@@ -294,55 +294,59 @@ __device__ __forceinline__ uint64_t pair_of<PA_F16>(uint32_t w) {
     return pk2(f.x, f.y);
 }
 
-// Append mode: the new token's K and V rows of (sequence it.b, KV head
-// it.kvh), in the cache's type (16-bit: the bits; E4M3: IEEE x/scale rounded
-// to nearest even with saturation, as pa_kv_cache_write stores it), go to the
-// cache slot of position L-1 and to row (L-1) % BS of the stage page at
-// `page` (K at page, V SPAGES pages further).  The whole warp takes part.
+// Append mode, first half: lane c of the producer warp loads its 16-byte
+// chunk of the new token's input rows (chunks 0..CH-1 of K, then CH..2CH-1 of
+// V; CH = 16-byte chunks per input row) when the item starts, so the stage that
+// holds the token does not wait on this load.  Lanes past 2*CH load nothing.
+template <typename C, int QDT>
+__device__ __forceinline__ uint4 append_prefetch(const DecodeParams& p, const Item& it, int lane) {
+    constexpr int D = C::ROWB / C::KB;
+    constexpr int CH = D * 2 / 16;  // the input rows are 16-bit
+    static_assert(2 * CH <= 32, "one chunk per lane");
+    if (lane >= 2 * CH) return make_uint4(0u, 0u, 0u, 0u);
+    const bool isv = lane >= CH;
+    const int64_t src_row = (static_cast<int64_t>(it.b) * p.num_kv_heads + it.kvh) * D;
+    return __ldg(reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src_row * 2) +
+                 (isv ? lane - CH : lane));
+}
+
+// Append mode, second half: the prefetched chunk `x`, in the cache's type
+// (16-bit: the bits; E4M3: IEEE x/scale rounded to nearest even with
+// saturation, as pa_kv_cache_write stores it), goes to the cache slot of
+// position L-1 and to row (L-1) % BS of the stage page at `page` (K at page,
+// V SPAGES pages further).
 template <typename C, int QDT, int KVDT>
 __device__ __forceinline__ void append_row(const DecodeParams& p, const Item& it, int32_t blk, uint8_t* page,
-                                           int lane) {
+                                           int lane, uint4 x) {
     constexpr int D = C::ROWB / C::KB;
+    constexpr int CH = D * 2 / 16;
+    if (lane >= 2 * CH) return;
     const int r = (it.L - 1) % (C::PAGE / C::ROWB);
-    const int64_t src_row = (static_cast<int64_t>(it.b) * p.num_kv_heads + it.kvh) * D;
     const int64_t cache_off = (static_cast<int64_t>(blk) * p.num_kv_heads + it.kvh) * C::PAGE + r * C::ROWB;
-    uint8_t* srow_k = page + r * C::ROWB;
-    uint8_t* srow_v = page + C::SPAGES * C::PAGE + r * C::ROWB;
+    const bool isv = lane >= CH;
+    const int cc = isv ? lane - CH : lane;
+    uint8_t* srow = page + (isv ? C::SPAGES * C::PAGE : 0) + r * C::ROWB;
+    uint8_t* crow = const_cast<uint8_t*>(isv ? p.v_cache : p.k_cache) + cache_off;
     if constexpr (C::KB == 2) {
-        // 16-byte chunks: D*2 bytes per row
-        constexpr int CH = D * 2 / 16;
-        for (int c = lane; c < 2 * CH; c += 32) {
-            const bool isv = c >= CH;
-            const int cc = isv ? c - CH : c;
-            const uint4 x = __ldg(reinterpret_cast<const uint4*>(
-                                      static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src_row * 2) + cc);
-            *reinterpret_cast<uint4*>((isv ? srow_v : srow_k) + cc * 16) = x;
-            *reinterpret_cast<uint4*>(const_cast<uint8_t*>(isv ? p.v_cache : p.k_cache) + cache_off + cc * 16) = x;
-        }
+        *reinterpret_cast<uint4*>(srow + cc * 16) = x;
+        *reinterpret_cast<uint4*>(crow + cc * 16) = x;
     } else {
-        // E4M3: 8 input elements (16 bytes) -> 8 codes (8 bytes) per lane step
-        constexpr int CH = D / 8;
-        for (int c = lane; c < 2 * CH; c += 32) {
-            const bool isv = c >= CH;
-            const int cc = isv ? c - CH : c;
-            const float sc = isv ? p.v_scale_w : p.k_scale_w;
-            const uint4 x = __ldg(reinterpret_cast<const uint4*>(
-                                      static_cast<const uint8_t*>(isv ? p.v_new : p.k_new) + src_row * 2) + cc);
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-            uint32_t codes[2];
+        // E4M3: 8 input elements (16 bytes) -> 8 codes (8 bytes)
+        const float sc = isv ? p.v_scale_w : p.k_scale_w;
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t codes[2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float2 a = kv_pair<QDT>(w[2 * h]), b = kv_pair<QDT>(w[2 * h + 1]);
-                const uint32_t lo = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc)), __NV_SATFINITE, __NV_E4M3));
-                const uint32_t hi = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
-                    make_float2(__fdiv_rn(b.x, sc), __fdiv_rn(b.y, sc)), __NV_SATFINITE, __NV_E4M3));
-                codes[h] = lo | (hi << 16);
-            }
-            const uint2 y = make_uint2(codes[0], codes[1]);
-            *reinterpret_cast<uint2*>((isv ? srow_v : srow_k) + cc * 8) = y;
-            *reinterpret_cast<uint2*>(const_cast<uint8_t*>(isv ? p.v_cache : p.k_cache) + cache_off + cc * 8) = y;
+        for (int h = 0; h < 2; ++h) {
+            const float2 a = kv_pair<QDT>(w[2 * h]), b = kv_pair<QDT>(w[2 * h + 1]);
+            const uint32_t lo = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                make_float2(__fdiv_rn(a.x, sc), __fdiv_rn(a.y, sc)), __NV_SATFINITE, __NV_E4M3));
+            const uint32_t hi = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+                make_float2(__fdiv_rn(b.x, sc), __fdiv_rn(b.y, sc)), __NV_SATFINITE, __NV_E4M3));
+            codes[h] = lo | (hi << 16);
         }
+        const uint2 y = make_uint2(codes[0], codes[1]);
+        *reinterpret_cast<uint2*>(srow + cc * 8) = y;
+        *reinterpret_cast<uint2*>(crow + cc * 8) = y;
     }
 }
 
@@ -371,6 +375,8 @@ paged_decode_kernel(const DecodeParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr uint32_t QSLOT = (C::QBYTES + 127) & ~127;
 
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8u * s, 1);
@@ -409,6 +415,12 @@ paged_decode_kernel(const DecodeParams p) {
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
+            // append mode: the item whose last partition holds the new token
+            // loads that token's rows now
+            uint4 xnew = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (APPEND) {
+                if (it.L > 0 && it.t1 == it.L) xnew = append_prefetch<C, QDT>(p, it, lane);
+            }
             const int32_t* row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
             const int64_t head_off = static_cast<int64_t>(it.kvh) * C::PAGE;
             const int64_t blk_stride = static_cast<int64_t>(p.num_kv_heads) * C::PAGE;
@@ -478,7 +490,7 @@ paged_decode_kernel(const DecodeParams p) {
                             ok = __shfl_sync(0xffffffffu, ok, 0);
                             if (ok && pk >= 0 && ids[pk] >= 0 && ids[pk] < p.num_blocks)
                                 append_row<C, QDT, KVDT>(p, it, ids[pk], ring + stage * C::STAGE_BYTES + pk * C::PAGE,
-                                                         lane);
+                                                         lane, xnew);
                             __syncwarp();
                             if (lane == 0 && ok) {
                                 const uint32_t bar = full0 + 8u * stage;
@@ -856,6 +868,8 @@ paged_decode_kernel(const DecodeParams p) {
 template <int QDT, int D>
 __global__ void __launch_bounds__(256)
 paged_decode_reduce_kernel(const DecodeParams p) {
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t bh = static_cast<int64_t>(blockIdx.x) * 8 + warp;
     if (bh >= static_cast<int64_t>(p.num_seqs) * p.num_heads) return;

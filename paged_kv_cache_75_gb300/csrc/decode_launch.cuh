@@ -39,13 +39,12 @@ pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     const int64_t cap = static_cast<int64_t>(sms) * per_sm;
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);
     if (grid <= 0) return PA_OK;
-    kern<<<grid, C::THREADS, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (launch_pdl(kern, grid, C::THREADS, smem, stream, p) != cudaSuccess) return PA_ERR_CUDA;
     if (p.max_parts > 1) {
         const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_heads;
         const int rgrid = static_cast<int>((pairs + 7) / 8);
-        paged_decode_reduce_kernel<QDT, D><<<rgrid, 256, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+        if (launch_pdl(paged_decode_reduce_kernel<QDT, D>, rgrid, 256, 0, stream, p) != cudaSuccess)
+            return PA_ERR_CUDA;
     }
     return PA_OK;
 }

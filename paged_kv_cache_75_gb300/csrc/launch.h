@@ -6,6 +6,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <utility>
 
 #include "pa_kv.h"
 
@@ -58,6 +59,26 @@ int blocks_per_sm(Kernel kern, int threads, int smem, LaunchCache& c) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) return 0;
     c.occ.store(key | static_cast<uint64_t>(n & 0xffff), std::memory_order_relaxed);
     return n;
+}
+
+// Launch with programmatic stream serialization: the kernel's blocks may be
+// scheduled while the previous kernel on the stream drains, which hides the
+// launch gap between back-to-back calls.  Every kernel launched this way calls
+// pdl_wait() before touching global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), int grid, int block, int smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace pa

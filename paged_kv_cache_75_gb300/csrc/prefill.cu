@@ -340,6 +340,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = p.num_seqs;
 
+    pdl_wait();
+    pdl_trigger();
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(k_full + 8 * s, 1);
@@ -945,8 +947,10 @@ pa_status launch_prefill(const PrefillParams& p, pa_dtype dtype, const CUtensorM
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);
     if (grid <= 0) return PA_OK;
-    kern<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(map_k, map_v, p);
-    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_pdl(kern, grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream), map_k, map_v, p) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 }  // namespace
