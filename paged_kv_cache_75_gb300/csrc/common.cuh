@@ -136,6 +136,17 @@ __device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Snake order of a persistent grid over a work list: in round r a CTA takes
+// item r*grid + blockIdx.x when r is even and r*grid + (grid-1-blockIdx.x)
+// when r is odd; -1 once past the list.  Over a list sorted longest first this
+// evens out the CTAs' totals.
+__device__ __forceinline__ int snake_item(int r, int n_items) {
+    const int64_t base = static_cast<int64_t>(r) * gridDim.x;
+    const int64_t i = base + ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                                      : static_cast<int>(blockIdx.x));
+    return i < n_items ? static_cast<int>(i) : -1;
+}
+
 // ---------------------------------------------------------------------------
 // conversions
 // ---------------------------------------------------------------------------

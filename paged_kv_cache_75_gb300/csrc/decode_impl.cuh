@@ -150,7 +150,7 @@ __device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
 // last holds L - (n-1)*partition.  The list puts every full partition first
 // (in sequence order), then the last partitions, longest first (64 length
 // classes, ties in sequence order); each entry stands for num_kv_heads items,
-// one per KV head.  CTAs deal the items out in snake order (see next_item),
+// one per KV head.  CTAs deal the items out in snake order (snake_item),
 // so the long items spread over all CTAs and the short ones fill the gaps:
 // with mixed lengths this keeps the busiest CTA within a few percent of the
 // mean, where plain round-robin in sequence order left it 20-35 % above.
@@ -282,15 +282,6 @@ __device__ __forceinline__ Item decode_item(const DecodeParams& p, const int32_t
     it.j0 = t0 / p.block_size;
     it.j1 = it.t1 > t0 ? (it.t1 + p.block_size - 1) / p.block_size : it.j0;
     return it;
-}
-
-// Snake order: in round r a CTA takes item r*grid + blockIdx.x when r is even
-// and r*grid + (grid-1-blockIdx.x) when r is odd; -1 once past the list.
-__device__ __forceinline__ int next_item(int r, int n_items) {
-    const int64_t base = static_cast<int64_t>(r) * gridDim.x;
-    const int64_t i = base + ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
-                                      : static_cast<int>(blockIdx.x));
-    return i < n_items ? static_cast<int>(i) : -1;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -485,7 +476,7 @@ paged_decode_kernel(const DecodeParams p) {
         uint32_t issued = 0;  // fills that started copies
         uint32_t qn = 0;      // items issued so far
         bool ok = true;
-        for (int r = 0, i; ok && (i = next_item(r, n_items)) >= 0; ++r, ++qn) {
+        for (int rnd = 0, i; ok && (i = snake_item(rnd, n_items)) >= 0; ++rnd, ++qn) {
             const Item it = decode_item(p, prefix, order, i);
             if (lane == 0) {
                 const uint32_t slot = qn & 1u;
@@ -650,7 +641,7 @@ paged_decode_kernel(const DecodeParams p) {
     const uint32_t lane_off = (tw * C::TG + tg) * C::ROWB + c * C::VB;
     uint32_t stage = 0, phase = 0;
     uint32_t qn = 0;
-    for (int r = 0, i; (i = next_item(r, n_items)) >= 0; ++r, ++qn) {
+    for (int rnd = 0, i; (i = snake_item(rnd, n_items)) >= 0; ++rnd, ++qn) {
         const Item it = decode_item(p, prefix, order, i);
         const uint32_t slot = qn & 1u;
         bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8u * slot, (qn >> 1) & 1u, p.status, abort_flag));

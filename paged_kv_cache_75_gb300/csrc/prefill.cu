@@ -88,6 +88,7 @@ struct PrefillParams {
     int32_t causal;
     float scale_log2;  // scale * log2(e)
     int64_t total_k;   // packed K/V: rows of K and V (Σ key lengths); -1 for the paged cache
+    int32_t order_cap; // query tiles the shared-memory work order holds (set by the launch)
 };
 
 // ---------------------------------------------------------------------------
@@ -289,10 +290,98 @@ struct Work {
     int b, i0, kvh, lq, lk, kend, ntiles;
 };
 
-__device__ __forceinline__ Work work_item(const PrefillParams& p, const int32_t* prefix, int item) {
+// Work order.  An item's cost is its number of key tiles, which under the
+// causal mask grows along a sequence's query tiles and differs widely between
+// sequences.  When the query tiles fit the shared-memory order array, every
+// CTA sorts them by cost class (64 classes, most key tiles first, ties in
+// list order) and deals the items out in snake order (snake_item): the
+// CTAs' totals then stay within about 1 % of each other on a mixed batch,
+// where round-robin in sequence order left the busiest 11 % above the mean.
+// Otherwise the items keep sequence order.
+__device__ __forceinline__ int tile_seq(const PrefillParams& p, const int32_t* prefix, int tile) {
+    int lo = 0, hi = p.num_seqs - 1;  // largest b with prefix[b] <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= tile) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int tile_class(const PrefillParams& p, const int32_t* prefix, int tile) {
+    const int b = tile_seq(p, prefix, tile);
+    int lq, lk;
+    seq_lens_ok(p, b, lq, lk);
+    const int i0 = (tile - prefix[b]) * p.tq;
+    int kend = lk;
+    if (p.causal) kend = min(lk, lk - lq + min(i0 + p.tq, lq));
+    const int maxt = (p.max_k + kBN - 1) / kBN;
+    const int nt = kend > 0 ? min(maxt, (kend + kBN - 1) / kBN) : 0;
+    return 63 - static_cast<int>((static_cast<int64_t>(nt) * 64) / (maxt + 1));  // 0 = most key tiles
+}
+
+// Stable counting sort of the n query tiles by class: each warp counts a
+// contiguous chunk (lanes of equal class found by match.any), warp 0 turns
+// the [warp][class] counts into class-major offsets, each warp then places its
+// chunk in order.  All threads of the block take part; hist holds 12*64 ints.
+__device__ void build_tile_order(const PrefillParams& p, const int32_t* prefix, int n, int32_t* order,
+                                 int32_t* hist) {
+    constexpr int NW = kThreads / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = ((n + NW - 1) / NW + 31) & ~31;
+    const int t0 = warp * chunk, t1 = min(n, t0 + chunk);
+    int32_t* h = hist + warp * 64;
+    h[lane] = 0;
+    h[lane + 32] = 0;
+    __syncwarp();
+    for (int c0 = t0; c0 < t1; c0 += 32) {
+        const int t = c0 + lane;
+        const int key = t < t1 ? tile_class(p, prefix, t) : 64;
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        if (t < t1 && lane == __ffs(same) - 1) h[key] += __popc(same);
+        __syncwarp();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int tot0 = 0, tot1 = 0;
+        for (int w = 0; w < NW; ++w) {
+            tot0 += hist[w * 64 + 2 * lane];
+            tot1 += hist[w * 64 + 2 * lane + 1];
+        }
+        int incl = tot0 + tot1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
+        }
+        int base0 = incl - tot0 - tot1, base1 = incl - tot1;
+        for (int w = 0; w < NW; ++w) {
+            const int x0 = hist[w * 64 + 2 * lane], x1 = hist[w * 64 + 2 * lane + 1];
+            hist[w * 64 + 2 * lane] = base0;
+            hist[w * 64 + 2 * lane + 1] = base1;
+            base0 += x0;
+            base1 += x1;
+        }
+    }
+    __syncthreads();
+    for (int c0 = t0; c0 < t1; c0 += 32) {
+        const int t = c0 + lane;
+        const int key = t < t1 ? tile_class(p, prefix, t) : 64;
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        if (t < t1) order[h[key] + __popc(same & ((1u << lane) - 1u))] = t;
+        __syncwarp();
+        if (t < t1 && lane == __ffs(same) - 1) h[key] += __popc(same);
+        __syncwarp();
+    }
+    __syncthreads();
+}
+
+__device__ __forceinline__ Work work_item(const PrefillParams& p, const int32_t* prefix, const int32_t* order,
+                                          int item) {
     Work w;
-    const int tile_id = item / p.num_kv_heads;
+    int tile_id = item / p.num_kv_heads;
     w.kvh = item - tile_id * p.num_kv_heads;
+    if (order != nullptr) tile_id = order[tile_id];
     int lo = 0, hi = p.num_seqs - 1;  // largest b with prefix[b] <= tile_id
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -405,6 +494,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         }
         __syncthreads();
     }
+    // ---- work order of the query tiles ----
+    const int32_t* order = nullptr;
+    if (p.order_cap > 0 && prefix[B] <= p.order_cap) {
+        int32_t* ord = prefix + B + 1;
+        build_tile_order(p, prefix, prefix[B], ord, ord + p.order_cap);
+        order = ord;
+    }
     const uint32_t tmem = *tmem_slot;
     const int n_items = prefix[B] * p.num_kv_heads;
     const int64_t hstride = static_cast<int64_t>(p.num_heads) * kD;  // elements per q/out row
@@ -418,8 +514,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             // a tile is 128 consecutive rows of one KV head: one 3-D box per
             // 64-column half (rows past the tensor read as zero; rows past the
             // sequence are masked / zeroed by the softmax warps)
-            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-                const Work w = work_item(p, prefix, item);
+            for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
+                const Work w = work_item(p, prefix, order, item);
                 const int row0 = __ldg(p.cu_k + w.b);
                 for (int t = 0; t < w.ntiles && ok; ++t) {
 #pragma unroll
@@ -447,8 +543,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             }
         } else {
         const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
-            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-                const Work w = work_item(p, prefix, item);
+            for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
+                const Work w = work_item(p, prefix, order, item);
                 const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
                 // page ids come in batches of 32 (one per lane, -1: past Lk, -2:
                 // bad id), so the table's latency is paid once per batch
@@ -550,8 +646,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             }
             return true;
         };
-        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-            const Work w = work_item(p, prefix, item);
+        for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
+            const Work w = work_item(p, prefix, order, item);
             if (w.ntiles == 0) continue;
             ok = mbar_wait(q_full, q_cnt & 1u, p.status, abort_flag);
             ++q_cnt;
@@ -630,8 +726,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             return stop != 0;
         };
         bool stop = false;
-        for (int item = blockIdx.x; item < n_items && !stop; item += gridDim.x) {
-            const Work w = work_item(p, prefix, item);
+        for (int rnd = 0, item; !stop && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
+            const Work w = work_item(p, prefix, order, item);
             const int shift = w.lk - w.lq;
             const int t_row = r / p.group, g_row = r - t_row * p.group;
             const int qi = w.i0 + t_row;  // query index of this row in its sequence
@@ -936,8 +1032,17 @@ bool make_packed_map(CUtensorMap* map, const void* base, int64_t total_k, int nu
 template <bool PACKED>
 pa_status launch_prefill(const PrefillParams& p, pa_dtype dtype, const CUtensorMap& map_k,
                          const CUtensorMap& map_v, pa_stream_t stream) {
-    const int smem = kSmemBytes + (p.num_seqs + 1) * 4 + 1024;
-    if (smem > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
+    // shared memory past the fixed layout: the tile prefix (B+1 ints), the
+    // work order (up to every query tile the bounds allow, within what the
+    // device offers) and the sort's [12 warps][64 classes] counts
+    const int base = kSmemBytes + (p.num_seqs + 1) * 4 + 1024;
+    if (base > device_max_smem_optin()) return PA_ERR_UNSUPPORTED;
+    const int64_t tiles_bound = static_cast<int64_t>(p.num_seqs) * ((p.max_q + p.tq - 1) / p.tq);
+    // (2 KB kept back for the kernel's static shared memory)
+    const int64_t room = (device_max_smem_optin() - 2048 - base) / 4 - (kThreads / 32) * 64;
+    PrefillParams q = p;
+    q.order_cap = static_cast<int32_t>(room <= 0 ? 0 : (tiles_bound < room ? tiles_bound : room));
+    const int smem = base + (q.order_cap > 0 ? (q.order_cap + (kThreads / 32) * 64) * 4 : 0);
     static LaunchCache cache_bf16, cache_f16;
     auto kern = dtype == PA_BF16 ? paged_prefill_tc_kernel<PA_BF16, PACKED> : paged_prefill_tc_kernel<PA_F16, PACKED>;
     const int per_sm = blocks_per_sm(kern, kThreads, smem, dtype == PA_BF16 ? cache_bf16 : cache_f16);
@@ -947,7 +1052,7 @@ pa_status launch_prefill(const PrefillParams& p, pa_dtype dtype, const CUtensorM
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);
     if (grid <= 0) return PA_OK;
-    return launch_pdl(kern, grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream), map_k, map_v, p) ==
+    return launch_pdl(kern, grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream), map_k, map_v, q) ==
                    cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
