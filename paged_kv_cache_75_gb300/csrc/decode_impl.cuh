@@ -67,10 +67,13 @@ struct DecodeParams {
 
 template <int QDT, int KVDT, int D, int G, int BS>
 struct DecodeCfg {
-    // query heads per consumer warp: two for G = 4 (fewer registers, three
-    // CTAs per SM hide more latency), four for G = 8, where E4M3 conversions
-    // are shared by more heads
-    static constexpr int GW = G == 8 ? 4 : (G < 2 ? G : 2);
+    // Four or more query heads per KV head: the QK and PV products of a
+    // 16-token slice are dense [16 x D] x [D x G] contractions, run on tensor
+    // cores (mma.sync m16n8k16, heads on N) by warps that each hold all G heads.
+    // Fewer heads keep the CUDA-core consumer.
+    static constexpr bool MMA = G >= 4;
+    // query heads per consumer warp (CUDA-core consumer): one or two
+    static constexpr int GW = MMA ? G : (G < 2 ? G : 2);
     static constexpr int HG = G / GW;                 // head groups (warp sets)
     static constexpr int TW = 4 / HG;                 // token warps per head group
     static constexpr int NCW = TW * HG;               // consumer warps (4)
@@ -93,15 +96,18 @@ struct DecodeCfg {
     static constexpr int STAGE_BYTES = 2 * SPAGES * PAGE;  // K pages, then V pages
     static constexpr int QBYTES = G * D * QB;         // one item's queries
     static constexpr int MERGE_FLOATS = NCW * GW * (D + 2);
-    // register cap: two 5-warp CTAs per SM when a warp holds 4 heads, three
-    // otherwise (a block's register share is counted in pairs of warps)
-    static constexpr int MAX_REGS = GW == 4 ? 168 : 128;
+    // register cap: three 5-warp CTAs per SM (a block's register share is
+    // counted in pairs of warps)
+    static constexpr int MAX_REGS = 128;
     static_assert(EPL * KB >= 4 && EPL % 4 == 0, "unsupported head size");
     static_assert(STOK % TPI == 0, "block size must be a multiple of the step");
     // steps handled together: one head per warp has enough independent work
     // per step; several heads gain from interleaving two steps' reductions
     static constexpr int NB = GW == 1 ? 1 : 2;
-    static_assert(SUB % NB == 0, "steps of a stage go in groups of NB");
+    static_assert(MMA || SUB % NB == 0, "steps of a stage go in groups of NB");
+    // tensor-core consumer: 16-token slices per stage, one warp each
+    static constexpr int SLICES = STOK / 16;
+    static_assert(!MMA || (SLICES == 2 || SLICES == 4), "stages of 32 or 64 tokens");
 };
 
 // shared memory carve-up (byte offsets from the 1 KB-aligned base)
@@ -367,6 +373,349 @@ __device__ __forceinline__ uint64_t pair_of<PA_F16>(uint32_t w) {
     return pk2(f.x, f.y);
 }
 
+// End of a work item: the consumer warps have left their per-warp partials
+// (max m and sum l in log2 units, unnormalised outputs) in `merge`, laid out
+// [head group][token warp][head][D + 2]; merge them and write the output row
+// (unsplit sequence) or the partition's normalised row and log-sum-exp
+// (split sequence).  All consumer warps call it; it brackets its work with the
+// consumers' named barrier.
+template <typename C, int QDT, int D, int G>
+__device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it, float* merge) {
+    named_bar_sync(1, C::NCW * 32);
+    {
+        const int tid = threadIdx.x;  // 0 .. NCW*32-1
+        const bool direct = it.nparts == 1;
+        for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
+            const int g = (2 * e) / D, d = (2 * e) % D;
+            const int ghg = g / C::GW, gw = g % C::GW;
+            float M = -INFINITY;
+#pragma unroll
+            for (int t = 0; t < C::TW; ++t) M = fmaxf(M, merge[((ghg * C::TW + t) * C::GW + gw) * (D + 2) + D]);
+            float o0 = 0.f, o1 = 0.f, lsum = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int t = 0; t < C::TW; ++t) {
+                    const float* mw = merge + ((ghg * C::TW + t) * C::GW + gw) * (D + 2);
+                    const float a = fast_exp2(mw[D] - M);
+                    lsum = fmaf(a, mw[D + 1], lsum);
+                    o0 = fmaf(a, mw[d], o0);
+                    o1 = fmaf(a, mw[d + 1], o1);
+                }
+                const float inv = p.v_scale / lsum;
+                o0 *= inv;
+                o1 *= inv;
+            }
+            const int h = it.kvh * G + g;
+            const int64_t bh = static_cast<int64_t>(it.b) * p.num_heads + h;
+            if (direct) {
+                using T = typename dtype_traits<QDT>::storage;
+                T* out = static_cast<T*>(p.out) + bh * D + d;
+                out[0] = dtype_traits<QDT>::from_f(o0);
+                out[1] = dtype_traits<QDT>::from_f(o1);
+            } else {
+                const int64_t r = bh * p.max_parts + it.part;
+                *reinterpret_cast<float2*>(p.ws_o + r * D + d) = make_float2(o0, o1);
+                if (d == 0) p.ws_lse[r] = M == -INFINITY ? -INFINITY : M + __log2f(lsum);
+            }
+        }
+    }
+    named_bar_sync(1, C::NCW * 32);
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core consumer (G >= 4)
+// ---------------------------------------------------------------------------
+// One m16n8k16 MMA with fp32 accumulators; MT = PA_F16 or PA_BF16 operands.
+template <int MT>
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    if constexpr (MT == PA_BF16) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    } else {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+// Transpose of an 8x8 matrix of 16-bit elements held one pair per lane (lane
+// 4r+c holds row r, columns 2c and 2c+1): afterwards lane 4r+c holds column r,
+// rows 2c and 2c+1.
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// two fp32 values -> packed pair of the MMA operand type (RN)
+template <int MT>
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
+    if constexpr (MT == PA_BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// Consumer warps of the tensor-core path.  Every stage of 32 (or 64) tokens
+// is cut into 16-token slices; slice k of the f-th stage the consumers see
+// goes to warp (f*SLICES + k) % 4, which holds all G query heads (all four
+// warps still wait for and release every stage).  For a
+// slice, with lane = 4*gi + ti:
+//  * S^T[16 tokens x 8 heads] = K[16 x D] . Q^T[D x 8]: tokens on M, heads on N
+//    (heads G..7 zero), D/16 k-steps.  The contraction order over d is free, so
+//    lane ti's k-columns are the d-span [W*ti, W*ti + W) (W = D/4) of its rows:
+//    k-step s takes elements 4s..4s+3 of every span, and each A fragment comes
+//    straight from 16-byte shared-memory loads of the K rows gi and gi+8;
+//  * scores scaled, masked, one online-softmax state per head (the max is
+//    reduced over the slice's tokens, so every weight of a head in the MMA
+//    below shares one reference; lazy rescale as in the CUDA-core path);
+//  * O^T[D x 8] += V^T[D x 16] . P^T[16 x 8]: the weights' C layout (token,
+//    head pair) becomes the B layout (token pair, head) by one movmatrix per
+//    8 tokens; V rows load like K rows, and a movmatrix per 8x8 tile turns
+//    them into V^T A fragments, whose rows (d) then follow the span order:
+//    m-tile mt, row r<8 is d = W*(r/2) + 4*mt + r%2, row r>=8 that d + 2;
+//  * bf16 weights go in as hi + lo (two MMAs) so they keep 16 bits; fp16
+//    weights (fp16 and E4M3 caches, V exact in fp16) take one MMA.
+// Masked tokens (past the item or on a missing page) get weight 0 and their
+// V rows are zeroed before the MMA, so stale stage bytes never reach a sum.
+template <typename C, int QDT, int KVDT, int D, int G, int BS>
+__device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8_t* ring, const uint8_t* qbuf,
+                                                    float* merge, const int32_t* prefix, const int32_t* order,
+                                                    int n_items, uint32_t full0, uint32_t empty0, uint32_t qfull0,
+                                                    uint32_t qempty0, volatile int* abort_flag,
+                                                    volatile int* stage_mask, int warp, int lane) {
+    constexpr int MT = C::KB == 2 ? KVDT : PA_F16;  // operand type of both products
+    constexpr bool HILO = MT == PA_BF16;
+    constexpr int W = D / 4;   // d-span of a lane, elements
+    constexpr int KS = D / 16; // QK k-steps = PV m-tiles
+    constexpr int SL = C::SLICES;
+    constexpr uint32_t QSLOT = (C::QBYTES + 127) & ~127;
+    constexpr float kTau = 8.f;
+    const int gi = lane >> 2, ti = lane & 3;
+    const int S = p.stages;
+    uint32_t stage = 0, phase = 0, fc = 0, qn = 0;
+    for (int rnd = 0, i; (i = snake_item(rnd, n_items)) >= 0; ++rnd, ++qn) {
+        const Item it = decode_item(p, prefix, order, i);
+        const uint32_t slot = qn & 1u;
+        bool ok = __all_sync(0xffffffffu, mbar_wait(qfull0 + 8u * slot, (qn >> 1) & 1u, p.status, abort_flag));
+        // ---- Q^T fragments: head gi, span [W*ti, W*ti + W) as pairs ----
+        uint32_t qb[KS][2];
+        float qk_scale = p.qk_scale;
+        {
+            const uint8_t* qs = qbuf + slot * QSLOT + (gi * D + W * ti) * C::QB;
+            if constexpr (C::KB == 2) {
+#pragma unroll
+                for (int c = 0; c < W / 8; ++c) {
+                    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                    if (gi < G) x = *reinterpret_cast<const uint4*>(qs + 16 * c);
+                    qb[2 * c][0] = x.x;
+                    qb[2 * c][1] = x.y;
+                    qb[2 * c + 1][0] = x.z;
+                    qb[2 * c + 1][1] = x.w;
+                }
+            } else {
+                // E4M3 cache: queries to fp16 scaled by a power of two so that
+                // the largest lands in [2^14, 2^15); the scale is folded back
+                // into the score scale
+                float qv[W];
+                float mx = 0.f;
+#pragma unroll
+                for (int c = 0; c < W / 2; ++c) {
+                    float2 f = make_float2(0.f, 0.f);
+                    if (gi < G) f = kv_pair<QDT>(*reinterpret_cast<const uint32_t*>(qs + 4 * c));
+                    qv[2 * c] = f.x;
+                    qv[2 * c + 1] = f.y;
+                    mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                int ex = mx > 0.f ? ((__float_as_int(mx) >> 23) & 0xff) - 127 - 14 : 0;
+                ex = max(-100, min(100, ex));
+                const float down = __int_as_float((127 - ex) << 23), up = __int_as_float((127 + ex) << 23);
+                qk_scale *= up;
+#pragma unroll
+                for (int s2 = 0; s2 < KS; ++s2) {
+                    qb[s2][0] = pack_pair<PA_F16>(qv[4 * s2] * down, qv[4 * s2 + 1] * down);
+                    qb[s2][1] = pack_pair<PA_F16>(qv[4 * s2 + 2] * down, qv[4 * s2 + 3] * down);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qempty0 + 8u * slot);
+
+        float o[KS][4];
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2ti, 2ti+1
+
+        for (int js = it.j0; js < it.j1 && ok; js += C::SPAGES, ++fc) {
+            // Every consumer warp waits for every stage and releases it, also
+            // when the stage holds no slice of its own: then no warp can fall a
+            // whole ring behind the producer, so no parity wait can match an
+            // older phase of the same stage, and every copy has landed before
+            // the block exits.
+            if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8u * stage, phase, p.status, abort_flag))) {
+                ok = false;
+                break;
+            }
+            const int k = (warp - static_cast<int>((fc * SL) & 3u)) & 3;  // this warp's slice of the stage
+            if (k < SL) {
+                const int mask = stage_mask[stage];
+                const int tk0 = 16 * k + gi, tk1 = tk0 + 8;  // stage tokens of rows gi and gi+8
+                const bool v0 = ((mask >> (tk0 / BS)) & 1) && js * BS + tk0 < it.t1;
+                const bool v1 = ((mask >> (tk1 / BS)) & 1) && js * BS + tk1 < it.t1;
+                const uint8_t* kr0 = ring + stage * C::STAGE_BYTES + tk0 * C::ROWB + W * ti * C::KB;
+                const uint8_t* kr1 = kr0 + 8 * C::ROWB;
+                // ---- S^T = K Q^T ----
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (C::KB == 2) {
+#pragma unroll
+                    for (int c = 0; c < W / 8; ++c) {
+                        const uint4 x0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
+                        const uint4 x1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
+                        mma16816<MT>(sc, x0.x, x1.x, x0.y, x1.y, qb[2 * c][0], qb[2 * c][1]);
+                        mma16816<MT>(sc, x0.z, x1.z, x0.w, x1.w, qb[2 * c + 1][0], qb[2 * c + 1][1]);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < W / 16; ++c) {
+                        const uint4 x0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
+                        const uint4 x1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
+                        const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma16816<MT>(sc, e4m3x2_to_h2(w0[j]), e4m3x2_to_h2(w1[j]), e4m3x2_to_h2(w0[j] >> 16),
+                                         e4m3x2_to_h2(w1[j] >> 16), qb[4 * c + j][0], qb[4 * c + j][1]);
+                    }
+                }
+                // ---- online softmax: c0/c1 = token gi, heads 2ti/2ti+1; c2/c3 = token gi+8 ----
+                const float s0 = v0 ? sc[0] * qk_scale : -INFINITY, s1 = v0 ? sc[1] * qk_scale : -INFINITY;
+                const float s2 = v1 ? sc[2] * qk_scale : -INFINITY, s3 = v1 ? sc[3] * qk_scale : -INFINITY;
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+                }
+                if (__any_sync(0xffffffffu, mx0 > m0 + kTau || mx1 > m1 + kTau)) {
+                    const bool r0 = mx0 > m0 + kTau, r1 = mx1 > m1 + kTau;
+                    const float a0 = r0 ? fast_exp2(m0 - mx0) : 1.f, a1 = r1 ? fast_exp2(m1 - mx1) : 1.f;
+                    m0 = r0 ? mx0 : m0;
+                    m1 = r1 ? mx1 : m1;
+                    l0 *= a0;
+                    l1 *= a1;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+                        o[mt][0] *= a0;
+                        o[mt][1] *= a1;
+                        o[mt][2] *= a0;
+                        o[mt][3] *= a1;
+                    }
+                }
+                const float p0 = v0 ? fast_exp2(s0 - m0) : 0.f, p1 = v0 ? fast_exp2(s1 - m1) : 0.f;
+                const float p2 = v1 ? fast_exp2(s2 - m0) : 0.f, p3 = v1 ? fast_exp2(s3 - m1) : 0.f;
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                // ---- P^T fragments (token pair, head gi) ----
+                uint32_t pb0, pb1, pl0 = 0u, pl1 = 0u;
+                if constexpr (HILO) {
+                    // hi = the top 16 bits (truncation), lo = the rest rounded to bf16
+                    const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+                    const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
+                    pb0 = movtrans(__byte_perm(u0, u1, 0x7632));
+                    pb1 = movtrans(__byte_perm(u2, u3, 0x7632));
+                    pl0 = movtrans(pack_pair<PA_BF16>(p0 - __uint_as_float(u0 & 0xffff0000u),
+                                                      p1 - __uint_as_float(u1 & 0xffff0000u)));
+                    pl1 = movtrans(pack_pair<PA_BF16>(p2 - __uint_as_float(u2 & 0xffff0000u),
+                                                      p3 - __uint_as_float(u3 & 0xffff0000u)));
+                } else {
+                    pb0 = movtrans(pack_pair<MT>(p0, p1));
+                    pb1 = movtrans(pack_pair<MT>(p2, p3));
+                }
+                // ---- O^T += V^T P^T ----
+                const uint8_t* vr0 = kr0 + C::SPAGES * C::PAGE;
+                const uint8_t* vr1 = vr0 + 8 * C::ROWB;
+                if constexpr (C::KB == 2) {
+#pragma unroll
+                    for (int c = 0; c < W / 8; ++c) {
+                        uint4 y0 = *reinterpret_cast<const uint4*>(vr0 + 16 * c);
+                        uint4 y1 = *reinterpret_cast<const uint4*>(vr1 + 16 * c);
+                        if (!v0) y0 = make_uint4(0u, 0u, 0u, 0u);
+                        if (!v1) y1 = make_uint4(0u, 0u, 0u, 0u);
+                        // pairs 4c..4c+3 of the span: m-tiles 2c (pairs 4c, 4c+1) and 2c+1
+                        const uint32_t ta0 = movtrans(y0.x), tb0 = movtrans(y0.y), tc0 = movtrans(y0.z),
+                                       td0 = movtrans(y0.w);
+                        const uint32_t ta1 = movtrans(y1.x), tb1 = movtrans(y1.y), tc1 = movtrans(y1.z),
+                                       td1 = movtrans(y1.w);
+                        mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pb0, pb1);
+                        mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pb0, pb1);
+                        if constexpr (HILO) {
+                            mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pl0, pl1);
+                            mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pl0, pl1);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < W / 16; ++c) {
+                        uint4 y0 = *reinterpret_cast<const uint4*>(vr0 + 16 * c);
+                        uint4 y1 = *reinterpret_cast<const uint4*>(vr1 + 16 * c);
+                        if (!v0) y0 = make_uint4(0u, 0u, 0u, 0u);
+                        if (!v1) y1 = make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t w0[4] = {y0.x, y0.y, y0.z, y0.w}, w1[4] = {y1.x, y1.y, y1.z, y1.w};
+                        // word j: elements 4j..4j+3 = pairs 2j, 2j+1 of this chunk = m-tile 4c + j
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma16816<MT>(o[4 * c + j], movtrans(e4m3x2_to_h2(w0[j])),
+                                         movtrans(e4m3x2_to_h2(w0[j] >> 16)), movtrans(e4m3x2_to_h2(w1[j])),
+                                         movtrans(e4m3x2_to_h2(w1[j] >> 16)), pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8u * stage);
+            if (++stage == static_cast<uint32_t>(S)) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+
+        // ---- this warp's partials to the merge area ----
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
+        }
+        {
+            float* mw = merge + warp * G * (D + 2);
+            const int h0 = 2 * ti, h1 = 2 * ti + 1;
+            if (h0 < G) {
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    const int da = W * (gi >> 1) + 4 * mt + (gi & 1), db = da + 2;
+                    mw[h0 * (D + 2) + da] = o[mt][0];
+                    mw[h1 * (D + 2) + da] = o[mt][1];
+                    mw[h0 * (D + 2) + db] = o[mt][2];
+                    mw[h1 * (D + 2) + db] = o[mt][3];
+                }
+                if (gi == 0) {
+                    mw[h0 * (D + 2) + D] = m0;
+                    mw[h0 * (D + 2) + D + 1] = l0;
+                    mw[h1 * (D + 2) + D] = m1;
+                    mw[h1 * (D + 2) + D + 1] = l1;
+                }
+            }
+        }
+        store_item<C, QDT, D, G>(p, it, merge);
+    }
+}
+
 // Append mode, first half: lane c of the producer warp loads its 16-byte
 // chunk of the new token's input rows (chunks 0..CH-1 of K, then CH..2CH-1 of
 // V; CH = 16-byte chunks per input row) when the item starts, so the stage that
@@ -627,6 +976,11 @@ paged_decode_kernel(const DecodeParams p) {
     }
 
     // ------------------------------- consumers ------------------------------
+    if constexpr (C::MMA) {
+        decode_consumer_mma<C, QDT, KVDT, D, G, BS>(p, ring, qbuf, merge, prefix, order, n_items, full0, empty0,
+                                                    qfull0, qempty0, abort_flag, stage_mask, warp, lane);
+        return;
+    }
     // Consumer warp w works for head group hg = w / TW (query heads hg*GW ..
     // hg*GW+GW-1 of the KV head) as token warp tw = w % TW.  A warp is TG token
     // groups of LPT lanes; in every TPI-token step of a stage, group tg takes
@@ -895,45 +1249,7 @@ paged_decode_kernel(const DecodeParams p) {
                 }
             }
         }
-        named_bar_sync(1, C::NCW * 32);
-        {
-            const int tid = threadIdx.x;  // 0 .. NCW*32-1
-            const bool direct = it.nparts == 1;
-            for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
-                const int g = (2 * e) / D, d = (2 * e) % D;
-                const int ghg = g / C::GW, gw = g % C::GW;
-                float M = -INFINITY;
-#pragma unroll
-                for (int t = 0; t < C::TW; ++t) M = fmaxf(M, merge[((ghg * C::TW + t) * C::GW + gw) * (D + 2) + D]);
-                float o0 = 0.f, o1 = 0.f, lsum = 0.f;
-                if (M != -INFINITY) {
-#pragma unroll
-                    for (int t = 0; t < C::TW; ++t) {
-                        const float* mw = merge + ((ghg * C::TW + t) * C::GW + gw) * (D + 2);
-                        const float a = fast_exp2(mw[D] - M);
-                        lsum = fmaf(a, mw[D + 1], lsum);
-                        o0 = fmaf(a, mw[d], o0);
-                        o1 = fmaf(a, mw[d + 1], o1);
-                    }
-                    const float inv = p.v_scale / lsum;
-                    o0 *= inv;
-                    o1 *= inv;
-                }
-                const int h = it.kvh * G + g;
-                const int64_t bh = static_cast<int64_t>(it.b) * p.num_heads + h;
-                if (direct) {
-                    using T = typename dtype_traits<QDT>::storage;
-                    T* out = static_cast<T*>(p.out) + bh * D + d;
-                    out[0] = dtype_traits<QDT>::from_f(o0);
-                    out[1] = dtype_traits<QDT>::from_f(o1);
-                } else {
-                    const int64_t r = bh * p.max_parts + it.part;
-                    *reinterpret_cast<float2*>(p.ws_o + r * D + d) = make_float2(o0, o1);
-                    if (d == 0) p.ws_lse[r] = M == -INFINITY ? -INFINITY : M + __log2f(lsum);
-                }
-            }
-        }
-        named_bar_sync(1, C::NCW * 32);
+        store_item<C, QDT, D, G>(p, it, merge);
     }
 }
 
