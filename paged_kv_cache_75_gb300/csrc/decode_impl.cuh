@@ -480,7 +480,8 @@ __device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
 //    head pair) becomes the B layout (token pair, head) by one movmatrix per
 //    8 tokens; V rows load like K rows, and a movmatrix per 8x8 tile turns
 //    them into V^T A fragments, whose rows (d) then follow the span order:
-//    m-tile mt, row r<8 is d = W*(r/2) + 4*mt + r%2, row r>=8 that d + 2;
+//    m-tile mt, row r<8 is d = W*(r/2) + 4*mt + r%2 (with the chunk rotation
+//    below, the owner's chunk in place of mt/2), row r>=8 that d + 2;
 //  * bf16 weights go in as hi + lo (two MMAs) so they keep 16 bits; fp16
 //    weights (fp16 and E4M3 caches, V exact in fp16) take one MMA.
 // Masked tokens (past the item or on a missing page) get weight 0 and their
@@ -498,7 +499,15 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
     constexpr int SL = C::SLICES;
     constexpr uint32_t QSLOT = (C::QBYTES + 127) & ~127;
     constexpr float kTau = 8.f;
+    // 16-byte chunks of a lane's span.  With four (16-bit rows of 128), the
+    // spans of lanes ti and ti+2 start 128 bytes apart, on the same banks;
+    // those lanes take their chunks in an order rotated by two, which halves
+    // the bank conflicts of every row load.  The rotation depends on ti only
+    // (the owner of the k-columns), so Q and the output rows follow it.
+    constexpr int NCH = W * C::KB / 16;
+    constexpr bool ROT = NCH == 4;
     const int gi = lane >> 2, ti = lane & 3;
+    const int rot = ROT ? 2 * (ti >> 1) : 0;
     const int S = p.stages;
     uint32_t stage = 0, phase = 0, fc = 0, qn = 0;
     for (int rnd = 0, i; (i = snake_item(rnd, n_items)) >= 0; ++rnd, ++qn) {
@@ -514,7 +523,7 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
 #pragma unroll
                 for (int c = 0; c < W / 8; ++c) {
                     uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                    if (gi < G) x = *reinterpret_cast<const uint4*>(qs + 16 * c);
+                    if (gi < G) x = *reinterpret_cast<const uint4*>(qs + 16 * ((c + rot) & (NCH - 1)));
                     qb[2 * c][0] = x.x;
                     qb[2 * c][1] = x.y;
                     qb[2 * c + 1][0] = x.z;
@@ -569,114 +578,127 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
             if (k < SL) {
                 const int mask = stage_mask[stage];
                 const int tk0 = 16 * k + gi, tk1 = tk0 + 8;  // stage tokens of rows gi and gi+8
-                const bool v0 = ((mask >> (tk0 / BS)) & 1) && js * BS + tk0 < it.t1;
-                const bool v1 = ((mask >> (tk1 / BS)) & 1) && js * BS + tk1 < it.t1;
                 const uint8_t* kr0 = ring + stage * C::STAGE_BYTES + tk0 * C::ROWB + W * ti * C::KB;
                 const uint8_t* kr1 = kr0 + 8 * C::ROWB;
-                // ---- S^T = K Q^T ----
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (C::KB == 2) {
+                // a stage whose pages are all present and whose tokens all lie
+                // before the item's end needs no per-token masks
+                const bool full_stage = mask == (1 << C::SPAGES) - 1 && js * BS + C::STOK <= it.t1;
+                auto slice = [&](auto full_tag) {
+                    constexpr bool FULL = decltype(full_tag)::value;
+                    const bool v0 = FULL || (((mask >> (tk0 / BS)) & 1) && js * BS + tk0 < it.t1);
+                    const bool v1 = FULL || (((mask >> (tk1 / BS)) & 1) && js * BS + tk1 < it.t1);
+                    // ---- S^T = K Q^T (two accumulators: two independent MMA chains) ----
+                    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                    if constexpr (C::KB == 2) {
 #pragma unroll
-                    for (int c = 0; c < W / 8; ++c) {
-                        const uint4 x0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
-                        const uint4 x1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
-                        mma16816<MT>(sc, x0.x, x1.x, x0.y, x1.y, qb[2 * c][0], qb[2 * c][1]);
-                        mma16816<MT>(sc, x0.z, x1.z, x0.w, x1.w, qb[2 * c + 1][0], qb[2 * c + 1][1]);
-                    }
-                } else {
+                        for (int c = 0; c < W / 8; ++c) {
+                            const int cc = (c + rot) & (NCH - 1);
+                            const uint4 x0 = *reinterpret_cast<const uint4*>(kr0 + 16 * cc);
+                            const uint4 x1 = *reinterpret_cast<const uint4*>(kr1 + 16 * cc);
+                            mma16816<MT>(sa, x0.x, x1.x, x0.y, x1.y, qb[2 * c][0], qb[2 * c][1]);
+                            mma16816<MT>(sb, x0.z, x1.z, x0.w, x1.w, qb[2 * c + 1][0], qb[2 * c + 1][1]);
+                        }
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < W / 16; ++c) {
-                        const uint4 x0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
-                        const uint4 x1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
-                        const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+                        for (int c = 0; c < W / 16; ++c) {
+                            const uint4 x0 = *reinterpret_cast<const uint4*>(kr0 + 16 * c);
+                            const uint4 x1 = *reinterpret_cast<const uint4*>(kr1 + 16 * c);
+                            const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            mma16816<MT>(sc, e4m3x2_to_h2(w0[j]), e4m3x2_to_h2(w1[j]), e4m3x2_to_h2(w0[j] >> 16),
-                                         e4m3x2_to_h2(w1[j] >> 16), qb[4 * c + j][0], qb[4 * c + j][1]);
-                    }
-                }
-                // ---- online softmax: c0/c1 = token gi, heads 2ti/2ti+1; c2/c3 = token gi+8 ----
-                const float s0 = v0 ? sc[0] * qk_scale : -INFINITY, s1 = v0 ? sc[1] * qk_scale : -INFINITY;
-                const float s2 = v1 ? sc[2] * qk_scale : -INFINITY, s3 = v1 ? sc[3] * qk_scale : -INFINITY;
-                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-                for (int o2 = 4; o2 < 32; o2 <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
-                }
-                if (__any_sync(0xffffffffu, mx0 > m0 + kTau || mx1 > m1 + kTau)) {
-                    const bool r0 = mx0 > m0 + kTau, r1 = mx1 > m1 + kTau;
-                    const float a0 = r0 ? fast_exp2(m0 - mx0) : 1.f, a1 = r1 ? fast_exp2(m1 - mx1) : 1.f;
-                    m0 = r0 ? mx0 : m0;
-                    m1 = r1 ? mx1 : m1;
-                    l0 *= a0;
-                    l1 *= a1;
-#pragma unroll
-                    for (int mt = 0; mt < KS; ++mt) {
-                        o[mt][0] *= a0;
-                        o[mt][1] *= a1;
-                        o[mt][2] *= a0;
-                        o[mt][3] *= a1;
-                    }
-                }
-                const float p0 = v0 ? fast_exp2(s0 - m0) : 0.f, p1 = v0 ? fast_exp2(s1 - m1) : 0.f;
-                const float p2 = v1 ? fast_exp2(s2 - m0) : 0.f, p3 = v1 ? fast_exp2(s3 - m1) : 0.f;
-                l0 += p0 + p2;
-                l1 += p1 + p3;
-                // ---- P^T fragments (token pair, head gi) ----
-                uint32_t pb0, pb1, pl0 = 0u, pl1 = 0u;
-                if constexpr (HILO) {
-                    // hi = the top 16 bits (truncation), lo = the rest rounded to bf16
-                    const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
-                    const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
-                    pb0 = movtrans(__byte_perm(u0, u1, 0x7632));
-                    pb1 = movtrans(__byte_perm(u2, u3, 0x7632));
-                    pl0 = movtrans(pack_pair<PA_BF16>(p0 - __uint_as_float(u0 & 0xffff0000u),
-                                                      p1 - __uint_as_float(u1 & 0xffff0000u)));
-                    pl1 = movtrans(pack_pair<PA_BF16>(p2 - __uint_as_float(u2 & 0xffff0000u),
-                                                      p3 - __uint_as_float(u3 & 0xffff0000u)));
-                } else {
-                    pb0 = movtrans(pack_pair<MT>(p0, p1));
-                    pb1 = movtrans(pack_pair<MT>(p2, p3));
-                }
-                // ---- O^T += V^T P^T ----
-                const uint8_t* vr0 = kr0 + C::SPAGES * C::PAGE;
-                const uint8_t* vr1 = vr0 + 8 * C::ROWB;
-                if constexpr (C::KB == 2) {
-#pragma unroll
-                    for (int c = 0; c < W / 8; ++c) {
-                        uint4 y0 = *reinterpret_cast<const uint4*>(vr0 + 16 * c);
-                        uint4 y1 = *reinterpret_cast<const uint4*>(vr1 + 16 * c);
-                        if (!v0) y0 = make_uint4(0u, 0u, 0u, 0u);
-                        if (!v1) y1 = make_uint4(0u, 0u, 0u, 0u);
-                        // pairs 4c..4c+3 of the span: m-tiles 2c (pairs 4c, 4c+1) and 2c+1
-                        const uint32_t ta0 = movtrans(y0.x), tb0 = movtrans(y0.y), tc0 = movtrans(y0.z),
-                                       td0 = movtrans(y0.w);
-                        const uint32_t ta1 = movtrans(y1.x), tb1 = movtrans(y1.y), tc1 = movtrans(y1.z),
-                                       td1 = movtrans(y1.w);
-                        mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pb0, pb1);
-                        mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pb0, pb1);
-                        if constexpr (HILO) {
-                            mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pl0, pl1);
-                            mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pl0, pl1);
+                            for (int j = 0; j < 4; ++j)
+                                mma16816<MT>((j & 1) ? sb : sa, e4m3x2_to_h2(w0[j]), e4m3x2_to_h2(w1[j]),
+                                             e4m3x2_to_h2(w0[j] >> 16), e4m3x2_to_h2(w1[j] >> 16), qb[4 * c + j][0],
+                                             qb[4 * c + j][1]);
                         }
                     }
-                } else {
+                    // ---- online softmax: c0/c1 = token gi, heads 2ti/2ti+1; c2/c3 = token gi+8 ----
+                    const float s0 = v0 ? (sa[0] + sb[0]) * qk_scale : -INFINITY;
+                    const float s1 = v0 ? (sa[1] + sb[1]) * qk_scale : -INFINITY;
+                    const float s2 = v1 ? (sa[2] + sb[2]) * qk_scale : -INFINITY;
+                    const float s3 = v1 ? (sa[3] + sb[3]) * qk_scale : -INFINITY;
+                    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-                    for (int c = 0; c < W / 16; ++c) {
-                        uint4 y0 = *reinterpret_cast<const uint4*>(vr0 + 16 * c);
-                        uint4 y1 = *reinterpret_cast<const uint4*>(vr1 + 16 * c);
-                        if (!v0) y0 = make_uint4(0u, 0u, 0u, 0u);
-                        if (!v1) y1 = make_uint4(0u, 0u, 0u, 0u);
-                        const uint32_t w0[4] = {y0.x, y0.y, y0.z, y0.w}, w1[4] = {y1.x, y1.y, y1.z, y1.w};
-                        // word j: elements 4j..4j+3 = pairs 2j, 2j+1 of this chunk = m-tile 4c + j
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            mma16816<MT>(o[4 * c + j], movtrans(e4m3x2_to_h2(w0[j])),
-                                         movtrans(e4m3x2_to_h2(w0[j] >> 16)), movtrans(e4m3x2_to_h2(w1[j])),
-                                         movtrans(e4m3x2_to_h2(w1[j] >> 16)), pb0, pb1);
+                    for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
                     }
-                }
+                    if (__any_sync(0xffffffffu, mx0 > m0 + kTau || mx1 > m1 + kTau)) {
+                        const bool r0 = mx0 > m0 + kTau, r1 = mx1 > m1 + kTau;
+                        const float a0 = r0 ? fast_exp2(m0 - mx0) : 1.f, a1 = r1 ? fast_exp2(m1 - mx1) : 1.f;
+                        m0 = r0 ? mx0 : m0;
+                        m1 = r1 ? mx1 : m1;
+                        l0 *= a0;
+                        l1 *= a1;
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            o[mt][0] *= a0;
+                            o[mt][1] *= a1;
+                            o[mt][2] *= a0;
+                            o[mt][3] *= a1;
+                        }
+                    }
+                    const float p0 = v0 ? fast_exp2(s0 - m0) : 0.f, p1 = v0 ? fast_exp2(s1 - m1) : 0.f;
+                    const float p2 = v1 ? fast_exp2(s2 - m0) : 0.f, p3 = v1 ? fast_exp2(s3 - m1) : 0.f;
+                    l0 += p0 + p2;
+                    l1 += p1 + p3;
+                    // ---- P^T fragments (token pair, head gi) ----
+                    uint32_t pb0, pb1, pl0 = 0u, pl1 = 0u;
+                    if constexpr (HILO) {
+                        // hi = the top 16 bits (truncation), lo = the rest rounded to bf16
+                        const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+                        const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
+                        pb0 = movtrans(__byte_perm(u0, u1, 0x7632));
+                        pb1 = movtrans(__byte_perm(u2, u3, 0x7632));
+                        pl0 = movtrans(pack_pair<PA_BF16>(p0 - __uint_as_float(u0 & 0xffff0000u),
+                                                          p1 - __uint_as_float(u1 & 0xffff0000u)));
+                        pl1 = movtrans(pack_pair<PA_BF16>(p2 - __uint_as_float(u2 & 0xffff0000u),
+                                                          p3 - __uint_as_float(u3 & 0xffff0000u)));
+                    } else {
+                        pb0 = movtrans(pack_pair<MT>(p0, p1));
+                        pb1 = movtrans(pack_pair<MT>(p2, p3));
+                    }
+                    // ---- O^T += V^T P^T (masked rows zeroed) ----
+                    const uint8_t* vr0 = kr0 + C::SPAGES * C::PAGE;
+                    const uint8_t* vr1 = vr0 + 8 * C::ROWB;
+                    if constexpr (C::KB == 2) {
+#pragma unroll
+                        for (int c = 0; c < W / 8; ++c) {
+                            const int cc = (c + rot) & (NCH - 1);
+                            uint4 y0 = *reinterpret_cast<const uint4*>(vr0 + 16 * cc);
+                            uint4 y1 = *reinterpret_cast<const uint4*>(vr1 + 16 * cc);
+                            if (!FULL && !v0) y0 = make_uint4(0u, 0u, 0u, 0u);
+                            if (!FULL && !v1) y1 = make_uint4(0u, 0u, 0u, 0u);
+                            // pairs 4cc..4cc+3 of the span: m-tiles 2c (pairs 4cc, 4cc+1) and 2c+1
+                            const uint32_t ta0 = movtrans(y0.x), tb0 = movtrans(y0.y), tc0 = movtrans(y0.z),
+                                           td0 = movtrans(y0.w);
+                            const uint32_t ta1 = movtrans(y1.x), tb1 = movtrans(y1.y), tc1 = movtrans(y1.z),
+                                           td1 = movtrans(y1.w);
+                            mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pb0, pb1);
+                            mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pb0, pb1);
+                            if constexpr (HILO) {
+                                mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pl0, pl1);
+                                mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pl0, pl1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < W / 16; ++c) {
+                            uint4 y0 = *reinterpret_cast<const uint4*>(vr0 + 16 * c);
+                            uint4 y1 = *reinterpret_cast<const uint4*>(vr1 + 16 * c);
+                            if (!FULL && !v0) y0 = make_uint4(0u, 0u, 0u, 0u);
+                            if (!FULL && !v1) y1 = make_uint4(0u, 0u, 0u, 0u);
+                            const uint32_t w0[4] = {y0.x, y0.y, y0.z, y0.w}, w1[4] = {y1.x, y1.y, y1.z, y1.w};
+                            // word j: elements 4j..4j+3 = pairs 2j, 2j+1 of this chunk = m-tile 4c + j
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                mma16816<MT>(o[4 * c + j], movtrans(e4m3x2_to_h2(w0[j])),
+                                             movtrans(e4m3x2_to_h2(w0[j] >> 16)), movtrans(e4m3x2_to_h2(w1[j])),
+                                             movtrans(e4m3x2_to_h2(w1[j] >> 16)), pb0, pb1);
+                        }
+                    }
+                };
+                if (full_stage) slice(std::true_type{});
+                else slice(std::false_type{});
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8u * stage);
@@ -698,7 +720,16 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
             if (h0 < G) {
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
-                    const int da = W * (gi >> 1) + 4 * mt + (gi & 1), db = da + 2;
+                    // rows gi, gi+8 of m-tile mt: the d of the pair the span owner
+                    // (lane ti = gi/2 of the V load) held in that tile
+                    int da;
+                    if constexpr (C::KB == 2) {
+                        const int cc = ROT ? ((mt >> 1) + 2 * (gi >> 2)) & (NCH - 1) : (mt >> 1);
+                        da = W * (gi >> 1) + 8 * cc + 4 * (mt & 1) + (gi & 1);
+                    } else {
+                        da = W * (gi >> 1) + 4 * mt + (gi & 1);
+                    }
+                    const int db = da + 2;
                     mw[h0 * (D + 2) + da] = o[mt][0];
                     mw[h1 * (D + 2) + da] = o[mt][1];
                     mw[h0 * (D + 2) + db] = o[mt][2];

@@ -95,6 +95,20 @@ class PagedCase:
         lens = self.seq_lens.cpu().numpy() if lens is None else np.asarray(lens)
         return int(lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_size * 2 * ELEM_BYTES[self.kv_dtype]
 
+    def unique_kv_bytes(self, lens=None) -> int:
+        """K+V bytes of the distinct cache rows a decode over `lens` reads: a
+        physical block shared by several sequences counts once, with the
+        most rows any of them attends in it (the least DRAM traffic possible)."""
+        lens = self.seq_lens.cpu().numpy() if lens is None else np.asarray(lens)
+        table = self.block_table.cpu().numpy()
+        bs = self.block_size
+        rows = {}
+        for b, L in enumerate(lens.astype(np.int64)):
+            for j in range(int((L + bs - 1) // bs)):
+                blk = int(table[b, j])
+                rows[blk] = max(rows.get(blk, 0), int(min(bs, L - j * bs)))
+        return sum(rows.values()) * self.num_kv_heads * self.head_size * 2 * ELEM_BYTES[self.kv_dtype]
+
 
 def _fill_cache(gen_t, num_blocks, hkv, bs, d, dtype, device):
     return random_values(gen_t, (num_blocks, hkv, bs, d), dtype, device)

@@ -74,3 +74,20 @@ def test_aggregate_two_ranks_gloo():
     for p in procs:
         p.join(timeout=60)
     assert res == [(0, 20.0, 201.0), (1, 20.0, 201.0)]
+
+
+def test_unique_bytes_count_shared_blocks_once():
+    # two sequences share physical block 5 (16 rows of a prompt); the second
+    # uses only 9 of its rows, and block 7 is private to the first
+    bs, hkv, d = 16, 2, 64
+    case = W.make_decode_case(7, [20, 9], 4, hkv, d, bs, 8, W.F16, W.F16,
+                              block_table=np.array([[5, 7], [5, -1]], np.int32))
+    row = hkv * d * 2 * 2  # K and V, fp16
+    assert case.kv_bytes() == (20 + 9) * row
+    assert case.unique_kv_bytes() == (16 + 4) * row
+    # the bench's GQA workload: the groups' shared prompt blocks make the
+    # distinct rows a strict subset of the logical ones
+    g = W.gqa_shared_decode()
+    assert 0 < g.unique_kv_bytes() < g.kv_bytes()
+    m = W.mha_decode()
+    assert m.unique_kv_bytes() == m.kv_bytes()
