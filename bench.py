@@ -234,6 +234,16 @@ class DecodeStep:
         self.split = self.max_len > P
         self.launches_per_step = 2 + (1 if self.split else 0)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.has_groups = "cu_groups" in case.meta
+        if self.has_groups:
+            cu, sl = case.meta["cu_groups"], case.meta["shared_lens"]
+            self.cu_groups = torch.as_tensor(cu).to(device)
+            self.shared_lens = torch.as_tensor(sl).to(device)
+            self.max_group = int(np.diff(cu).max())
+            self.max_shared = int(sl.max())
+            nws = pk.pa_decode_cascade_workspace_size(B, case.num_heads, case.head_size, self.max_len,
+                                                      case.block_size, partition_size)
+            self.ws_cascade = torch.empty(nws, dtype=torch.uint8, device=device)
 
     def write(self):
         self.pk.pa_kv_cache_write(self.cache, self.k_new, self.v_new, self.slots, self.status)
@@ -242,6 +252,13 @@ class DecodeStep:
         """The same step through pa_decode_append: write and attend in one launch."""
         self.pk.pa_decode_append(self.out, self.q, self.k_new, self.v_new, self.cache, self.bt, self.lens,
                                  self.max_len, self.case.scale, self.P, self.ws, self.status)
+
+    def cascade(self):
+        """The same step's attention through pa_decode_cascade (the workload's
+        sampling groups read their shared prompt blocks once)."""
+        self.pk.pa_decode_cascade(self.out, self.q, self.cache, self.bt, self.lens, self.max_len, self.case.scale,
+                                  self.cu_groups, self.shared_lens, self.max_group, self.max_shared, self.ws_cascade,
+                                  self.P, self.status)
 
     def decode(self, q=None, out=None, bt=None, lens=None):
         self.pk.pa_decode(self.out if out is None else out, self.q if q is None else q, self.cache,
@@ -372,6 +389,27 @@ def timed_append(step: DecodeStep, steps, warmup, flush):
     torch.cuda.synchronize()
     if int(step.status.item()) != 0:
         raise RuntimeError("device status %d in the fused step" % int(step.status.item()))
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def timed_cascade(step: DecodeStep, steps, warmup, flush):
+    """Mean ms of the step (new token written, then pa_decode_cascade), each
+    step timed on its own with the L2 flush (if any) outside the interval."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.write()
+        step.cascade()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        evs[i][0].record(stream)
+        step.write()
+        step.cascade()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError("device status %d in the cascade step" % int(step.status.item()))
     return sum(a.elapsed_time(b) for a, b in evs) / steps
 
 
@@ -793,6 +831,7 @@ def run_ours(args):
     achieved_logical = step.kv_bytes / (decode_ms / 1e3) / 1e9
     graph_ms = timed_graph(step, args.steps, flush) if small else None
     fused_ms = timed_append(step, args.steps, args.warmup, flush)
+    cascade_ms = timed_cascade(step, args.steps, args.warmup, flush) if step.has_groups else None
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((args.workload, src_hash))
     line = {
@@ -829,6 +868,11 @@ def run_ours(args):
                          "value": round(step.kv_bytes / (fused_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                          "note": "the same step (new token written, then attended) as one pa_decode_append launch; "
                                  "each step timed on its own"},
+        "cascade": None if cascade_ms is None else {
+            "ms_per_step": round(cascade_ms, 5), "value": round(step.kv_bytes / (cascade_ms / 1e3) / 1e9, 2),
+            "unit": "GB/s",
+            "note": "the same step with the attention through pa_decode_cascade: each sampling group's shared "
+                    "prompt blocks attended once for all members (logical bytes counted as in value)"},
         "graph": None if graph_ms is None else {
             "us_per_step": round(graph_ms * 1e3, 2), "value": round(step.kv_bytes / (graph_ms / 1e3) / 1e9, 2),
             "unit": "GB/s", "note": "the same step captured once as a CUDA graph and replayed (not in value)"},

@@ -275,6 +275,47 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
                            int32_t* dev_status, pa_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Shared-prefix ("cascade") decode.  "Как работает paged attention?
+ * (детально)" §3.3: sequences of parallel sampling or beam search refer to the
+ * same physical blocks for their common prefix (copy-on-write on change); §7:
+ * requests with the same prefix reuse its physical blocks (prefix caching);
+ * the vLLM paper summary lists parallel sampling and shared prefixes among its
+ * decoding scenarios.  The pages give no kernel for it; this entry point
+ * computes exactly what pa_decode computes (the same softmax(q K^T scale) V per
+ * sequence and head, up to fp32 rounding order) but reads a group's shared
+ * blocks once for all of its members: a prefix pass (the varlen tensor-core
+ * kernel, no causal mask) attends every member's query to the shared tokens,
+ * a suffix pass (the decode kernel) attends each member's own tokens, and the
+ * log-sum-exp merge of pa_decode combines the two.
+ *
+ * cu_groups: device int32 [num_groups+1], 0 = cu_groups[0] <= ... <=
+ *   cu_groups[num_groups] = num_seqs; sequences cu_groups[g] .. cu_groups[g+1]-1
+ *   form group g (consecutive rows of q, out, block_table and seq_lens).
+ * shared_lens: device int32 [num_groups]: group g's first shared_lens[g] tokens
+ *   are whole blocks (a multiple of block_size) that every member's block-table
+ *   row names identically and every member attends (shared_lens[g] <= each
+ *   member's length).  The blocks are read through the group's first row; a
+ *   member whose row differs there, or a shared length that breaks these rules,
+ *   is reported as PA_ERR_INVALID_ARG in dev_status.
+ * max_group_size: the largest group (host bound); at most 128 / (num_heads /
+ *   num_kv_heads).  max_shared_len: host bound on shared_lens (a multiple of
+ *   block_size, <= max_seq_len).
+ * workspace: pa_decode_cascade_workspace_size(...) bytes, 16-byte aligned (never
+ *   0: every (sequence, head) keeps a prefix and a suffix partial).
+ * Supported: fp16/bf16 caches with q of the same type, head_size 128, block
+ *   sizes 16/32/64, num_heads / num_kv_heads in {1, 2, 4, 8}; other shapes return
+ *   PA_ERR_UNSUPPORTED with nothing launched.  Everything else as pa_decode.
+ * ------------------------------------------------------------------------- */
+size_t pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                                        int32_t max_seq_len, int32_t block_size, int32_t partition_size);
+pa_status pa_decode_cascade(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                            const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t num_seqs, int32_t max_seq_len, int32_t num_heads, float scale,
+                            const int32_t* cu_groups, const int32_t* shared_lens, int32_t num_groups,
+                            int32_t max_group_size, int32_t max_shared_len, int32_t partition_size,
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status, pa_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Mixed batch dispatcher: a varlen batch (as pa_prefill_varlen) whose
  * trailing sequences have one query token each is split -- the leading
  * sequences go to the varlen tensor-core kernel, the trailing one-token run

@@ -66,6 +66,9 @@ def library():
                                           i32, vp, vp], C.c_int),
             "pa_decode_static_ws": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, vp],
                                     C.c_int),
+            "pa_decode_cascade_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+            "pa_decode_cascade": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, vp, vp, i32, i32, i32,
+                                   i32, vp, sz, vp, vp], C.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -272,6 +275,40 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: t
                              block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), H, float(scale),
                              int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(q))
     _check(st, "pa_decode")
+
+
+def pa_decode_cascade_workspace_size(num_seqs, num_heads, head_size, max_seq_len, block_size,
+                                     partition_size=0) -> int:
+    return int(library().pa_decode_cascade_workspace_size(num_seqs, num_heads, head_size, max_seq_len,
+                                                          block_size, partition_size))
+
+
+def pa_decode_cascade(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,
+                      seq_lens: torch.Tensor, max_seq_len: int, scale: float, cu_groups: torch.Tensor,
+                      shared_lens: torch.Tensor, max_group_size: int, max_shared_len: int,
+                      workspace: torch.Tensor, partition_size: int = 0,
+                      dev_status: Optional[torch.Tensor] = None):
+    """pa_decode for groups of sequences that share their first blocks:
+    cu_groups int32 [num_groups+1] (group g = rows cu_groups[g] ..
+    cu_groups[g+1]-1), shared_lens int32 [num_groups] (tokens, whole blocks)."""
+    _need(q, "q")
+    _need(out, "out", q.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    _need(cu_groups, "cu_groups", torch.int32)
+    _need(shared_lens, "shared_lens", torch.int32)
+    _need(workspace, "workspace")
+    B, H, D = q.shape
+    G = shared_lens.shape[0]
+    if cu_groups.shape[0] != G + 1:
+        raise ValueError("cu_groups must have num_groups + 1 entries")
+    cs = cache.c_struct()
+    st = library().pa_decode_cascade(_ptr(out), _ptr(q), torch_dtype_code(q.dtype), C.byref(cs), _ptr(block_table),
+                                     block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), H, float(scale),
+                                     _ptr(cu_groups), _ptr(shared_lens), G, int(max_group_size),
+                                     int(max_shared_len), int(partition_size), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(q))
+    _check(st, "pa_decode_cascade")
 
 
 def pa_decode_append(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,

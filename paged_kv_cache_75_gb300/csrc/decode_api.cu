@@ -60,7 +60,8 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
                        int32_t num_seqs, int32_t max_seq_len, int32_t num_heads, float scale,
                        int32_t partition_size, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                        pa_stream_t stream, const void* k_new, const void* v_new,
-                       const int32_t* cu_seq_lens_k = nullptr) {
+                       const int32_t* cu_seq_lens_k = nullptr, const int32_t* cu_groups = nullptr,
+                       const int32_t* shared_lens = nullptr, int32_t num_groups = 0) {
     pa_status st = check_cache(cache);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
@@ -90,7 +91,10 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     const int P = resolve_partition(partition_size, bs, group);
     if (P % bs != 0) return PA_ERR_INVALID_ARG;
     if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
-    const int max_parts = max_parts_of(max_seq_len, P);
+    if (cu_groups != nullptr && (shared_lens == nullptr || num_groups <= 0 || k_new != nullptr))
+        return PA_ERR_INVALID_ARG;
+    // cascade: one more part per (sequence, head) for the shared prefix's partial
+    const int max_parts = max_parts_of(max_seq_len, P) + (cu_groups != nullptr ? 1 : 0);
     const WsLayout w = ws_layout(num_seqs, num_heads, D, max_parts);
     if (w.bytes > 0 && (workspace == nullptr || workspace_bytes < w.bytes ||
                         (reinterpret_cast<uintptr_t>(workspace) & 15u)))
@@ -123,6 +127,9 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     p.v_new = v_new;
     p.k_scale_w = cache->k_scale;
     p.v_scale_w = cache->v_scale;
+    p.cu_groups = cu_groups;
+    p.shared_lens = shared_lens;
+    p.num_groups = num_groups;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 #define PA_BS(KV)                                                       \
     if (bs == 16) return launch_decode_##KV##_bs16(p, q_dtype, D, group, s); \
@@ -161,6 +168,61 @@ extern "C" pa_status pa_decode_append(void* out, const void* q, const void* k_ne
     return pa::decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                             max_seq_len, num_heads, scale, partition_size, workspace, workspace_bytes, dev_status,
                             stream, k_new, v_new);
+}
+
+extern "C" size_t pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
+                                                   int32_t max_seq_len, int32_t block_size,
+                                                   int32_t partition_size) {
+    if (num_seqs <= 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0 || block_size <= 0 ||
+        partition_size < 0)
+        return 0;
+    const int P = resolve_partition(partition_size, block_size, 1);
+    return ws_layout(num_seqs, num_heads, head_size, max_parts_of(max_seq_len, P) + 1).bytes;
+}
+
+extern "C" pa_status pa_decode_cascade(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                                       const int32_t* block_table, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                       int32_t num_heads, float scale, const int32_t* cu_groups,
+                                       const int32_t* shared_lens, int32_t num_groups, int32_t max_group_size,
+                                       int32_t max_shared_len, int32_t partition_size, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, pa_stream_t stream) {
+    pa_status st = check_cache(cache);
+    if (st != PA_OK) return st;
+    if (num_seqs < 0 || num_groups < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
+        partition_size < 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (num_groups == 0 || cu_groups == nullptr || shared_lens == nullptr || seq_lens == nullptr ||
+        out == nullptr || q == nullptr || block_table == nullptr || workspace == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    const int group = num_heads / cache->num_kv_heads;
+    const int bs = cache->block_size;
+    // the prefix pass runs on the varlen tensor-core kernel: 16-bit caches of
+    // head size 128, a group's members within one 128-row tile
+    if (cache->head_size != 128 || (q_dtype != PA_F16 && q_dtype != PA_BF16) || cache->kv_dtype != q_dtype)
+        return PA_ERR_UNSUPPORTED;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+    if (max_group_size < 1 || max_group_size > 128 / group) return PA_ERR_UNSUPPORTED;
+    if (max_shared_len < 0 || max_shared_len > max_seq_len || max_shared_len % bs != 0) return PA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u)) return PA_ERR_INVALID_ARG;
+    const int P = resolve_partition(partition_size, bs, group);
+    if (P <= 0 || P % bs != 0) return PA_ERR_INVALID_ARG;
+    const int max_parts = max_parts_of(max_seq_len, P) + 1;
+    const WsLayout w = ws_layout(num_seqs, num_heads, cache->head_size, max_parts);
+    if (workspace_bytes < w.bytes) return PA_ERR_INVALID_ARG;
+    float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse_off);
+    float* ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.o_off);
+    // 1) shared prefixes, once per group; 2) every member's own suffix; 3) the
+    //    log-sum-exp merge of both (launched by the decode entry)
+    st = cascade_prefix_partials(q, q_dtype, cache, block_table, max_blocks_per_seq, cu_groups, shared_lens,
+                                 num_groups, max_group_size, max_shared_len, num_heads, scale, ws_o, ws_lse,
+                                 max_parts, dev_status, stream);
+    if (st != PA_OK) return st;
+    return decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                        num_heads, scale, partition_size, workspace, workspace_bytes, dev_status, stream, nullptr,
+                        nullptr, nullptr, cu_groups, shared_lens, num_groups);
 }
 
 extern "C" size_t pa_varlen_mixed_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,

@@ -63,6 +63,14 @@ struct DecodeParams {
     const void* k_new;
     const void* v_new;
     float k_scale_w, v_scale_w;  // E4M3 cache: the write's scales
+    // cascade suffix pass: sequences cu_groups[g] .. cu_groups[g+1]-1 form group
+    // g, whose first shared_lens[g] tokens (whole blocks, the same physical
+    // blocks in every member) a prefix pass has attended; this launch attends
+    // tokens [shared_lens[g], L) and writes every partial to the workspace from
+    // part 1 on (part 0 holds the prefix's)
+    const int32_t* cu_groups;
+    const int32_t* shared_lens;
+    int32_t num_groups;
 };
 
 template <int QDT, int KVDT, int D, int G, int BS>
@@ -141,6 +149,30 @@ struct DecodeSmem {
 // number of partitions a sequence of length L splits into (>= 1)
 __device__ __forceinline__ int parts_of(int L, int P) { return L <= P ? 1 : (L + P - 1) / P; }
 
+// Cascade suffix pass: the group of sequence b (largest g with cu_groups[g] <= b).
+__device__ __forceinline__ int group_of(const DecodeParams& p, int b) {
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(p.cu_groups + mid) <= b) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// First token of sequence b (length L) this launch attends: its group's shared
+// length in a cascade suffix pass, else 0.  A shared length that is negative,
+// past L or not a whole number of blocks is reported and taken as 0.
+__device__ __forceinline__ int seq_start(const DecodeParams& p, int b, int L) {
+    if (p.cu_groups == nullptr) return 0;
+    const int s0 = __ldg(p.shared_lens + group_of(p, b));
+    if (s0 < 0 || s0 > L || s0 % p.block_size != 0) {
+        report(p.status, PA_ERR_INVALID_ARG);
+        return 0;
+    }
+    return s0;
+}
+
 // A length is usable iff 0 <= L <= max_seq_len and L fits the table row.
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
     // lengths from seq_lens, or as differences of cumulative key lengths
@@ -178,7 +210,8 @@ __device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, in
     for (int b = b0; b < b1; ++b) {
         int L = checked_len(p, b);
         if (L < 0) report(p.status, PA_ERR_INVALID_ARG);
-        local += parts_of(L < 0 ? 0 : L, p.partition) - 1;
+        L = L < 0 ? 0 : L;
+        local += parts_of(L - seq_start(p, b, L), p.partition) - 1;
     }
     // inclusive scan inside the warp
     const int lane = t & 31, warp = t >> 5;
@@ -204,7 +237,8 @@ __device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, in
     for (int b = b0; b < b1; ++b) {
         prefix[b] = run;
         int L = checked_len(p, b);
-        run += parts_of(L < 0 ? 0 : L, p.partition) - 1;
+        L = L < 0 ? 0 : L;
+        run += parts_of(L - seq_start(p, b, L), p.partition) - 1;
     }
     // last partitions: a stable counting sort by length class, done by warp 0
     // 32 sequences at a time (lanes with equal classes found by match.any)
@@ -217,8 +251,9 @@ __device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, in
             const int b = c0 + lane;
             int key = 64;
             if (b < B) {
-                const int L = checked_len(p, b);
-                key = tail_class(L < 0 ? 0 : L, p.partition);
+                int L = checked_len(p, b);
+                L = L < 0 ? 0 : L;
+                key = tail_class(L - seq_start(p, b, L), p.partition);
             }
             const unsigned same = __match_any_sync(0xffffffffu, key);
             if (b < B && lane == __ffs(same) - 1) bins[key] += __popc(same);
@@ -240,8 +275,9 @@ __device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, in
             const int b = c0 + lane;
             int key = 64;
             if (b < B) {
-                const int L = checked_len(p, b);
-                key = tail_class(L < 0 ? 0 : L, p.partition);
+                int L = checked_len(p, b);
+                L = L < 0 ? 0 : L;
+                key = tail_class(L - seq_start(p, b, L), p.partition);
             }
             const unsigned same = __match_any_sync(0xffffffffu, key);
             if (b < B) order[bins[key] + __popc(same & ((1u << lane) - 1u))] = b;
@@ -254,7 +290,7 @@ __device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, in
 }
 
 struct Item {
-    int b, part, kvh, L, t1, j0, j1, nparts;
+    int b, part, kvh, L, s0, t1, j0, j1, nparts;
 };
 
 __device__ __forceinline__ Item decode_item(const DecodeParams& p, const int32_t* prefix, const int32_t* order,
@@ -275,15 +311,17 @@ __device__ __forceinline__ Item decode_item(const DecodeParams& p, const int32_t
         it.part = sp - prefix[lo];
         L = checked_len(p, lo);
         it.L = L < 0 ? 0 : L;
-        it.nparts = parts_of(it.L, p.partition);
+        it.s0 = seq_start(p, lo, it.L);
+        it.nparts = parts_of(it.L - it.s0, p.partition);
     } else {
         it.b = order[sp - F];
         L = checked_len(p, it.b);
         it.L = L < 0 ? 0 : L;
-        it.nparts = parts_of(it.L, p.partition);
+        it.s0 = seq_start(p, it.b, it.L);
+        it.nparts = parts_of(it.L - it.s0, p.partition);
         it.part = it.nparts - 1;
     }
-    const int t0 = it.part * p.partition;
+    const int t0 = it.s0 + it.part * p.partition;
     it.t1 = min(it.L, t0 + p.partition);
     it.j0 = t0 / p.block_size;
     it.j1 = it.t1 > t0 ? (it.t1 + p.block_size - 1) / p.block_size : it.j0;
@@ -384,7 +422,8 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
     named_bar_sync(1, C::NCW * 32);
     {
         const int tid = threadIdx.x;  // 0 .. NCW*32-1
-        const bool direct = it.nparts == 1;
+        const bool direct = it.nparts == 1 && p.cu_groups == nullptr;
+        const int part = it.part + (p.cu_groups != nullptr ? 1 : 0);  // cascade: part 0 is the prefix's
         for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
             const int g = (2 * e) / D, d = (2 * e) % D;
             const int ghg = g / C::GW, gw = g % C::GW;
@@ -413,7 +452,7 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
                 out[0] = dtype_traits<QDT>::from_f(o0);
                 out[1] = dtype_traits<QDT>::from_f(o1);
             } else {
-                const int64_t r = bh * p.max_parts + it.part;
+                const int64_t r = bh * p.max_parts + part;
                 *reinterpret_cast<float2*>(p.ws_o + r * D + d) = make_float2(o0, o1);
                 if (d == 0) p.ws_lse[r] = M == -INFINITY ? -INFINITY : M + __log2f(lsum);
             }
@@ -876,6 +915,17 @@ paged_decode_kernel(const DecodeParams p) {
                 if (it.L > 0 && it.t1 == it.L) xnew = append_prefetch<C, QDT>(p, it, lane);
             }
             const int32_t* row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
+            // cascade: the prefix pass read the shared blocks through the group's
+            // first row; a member whose row names other blocks there is reported
+            if (p.cu_groups != nullptr && it.part == 0 && it.kvh == 0 && it.s0 > 0) {
+                const int b0 = __ldg(p.cu_groups + group_of(p, it.b));
+                if (b0 != it.b) {
+                    const int32_t* row0 = p.block_table + static_cast<int64_t>(b0) * p.max_blocks;
+                    bool bad = false;
+                    for (int j = lane; j < it.s0 / BS; j += 32) bad |= __ldg(row0 + j) != __ldg(row + j);
+                    if (__any_sync(0xffffffffu, bad) && lane == 0) report(p.status, PA_ERR_INVALID_ARG);
+                }
+            }
             const int64_t head_off = static_cast<int64_t>(it.kvh) * C::PAGE;
             const int64_t blk_stride = static_cast<int64_t>(p.num_kv_heads) * C::PAGE;
             for (int jb = it.j0; jb < it.j1 && ok; jb += 32) {
@@ -1297,7 +1347,8 @@ paged_decode_reduce_kernel(const DecodeParams p) {
     const int b = static_cast<int>(bh / p.num_heads);
     const int Lc = checked_len(p, b);
     const int L = Lc < 0 ? 0 : Lc;
-    const int np = parts_of(L, p.partition);
+    // cascade: the prefix's partial (part 0), then the suffix's partitions
+    const int np = parts_of(L - seq_start(p, b, L), p.partition) + (p.cu_groups != nullptr ? 1 : 0);
     if (np <= 1) return;
     const float* lse = p.ws_lse + bh * p.max_parts;
     float M = -INFINITY;

@@ -89,6 +89,15 @@ struct PrefillParams {
     float scale_log2;  // scale * log2(e)
     int64_t total_k;   // packed K/V: rows of K and V (Σ key lengths); -1 for the paged cache
     int32_t order_cap; // query tiles the shared-memory work order holds (set by the launch)
+    // Shared-prefix pass of the cascade decode: key lengths from k_lens[b]
+    // (cu_k unused), sequence b's block-table row is row cu_q[b] (its first
+    // query's row in the decode batch), and every query row writes its fp32
+    // O / l and log-sum-exp (log2 units) into part 0 of the decode workspace
+    // slot (query row, head) instead of `out`.
+    const int32_t* k_lens;
+    float* ws_o;
+    float* ws_lse;
+    int32_t ws_parts;
 };
 
 // ---------------------------------------------------------------------------
@@ -278,7 +287,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // lengths of sequence b; false if they break the stated bounds
 __device__ __forceinline__ bool seq_lens_ok(const PrefillParams& p, int b, int& lq, int& lk) {
     const int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
-    const int k0 = __ldg(p.cu_k + b), k1 = __ldg(p.cu_k + b + 1);
+    const int k0 = p.k_lens != nullptr ? 0 : __ldg(p.cu_k + b);
+    const int k1 = p.k_lens != nullptr ? __ldg(p.k_lens + b) : __ldg(p.cu_k + b + 1);
     lq = q1 - q0;
     lk = k1 - k0;
     const bool fits = p.total_k >= 0 ? (k0 >= 0 && static_cast<int64_t>(k1) <= p.total_k)
@@ -545,7 +555,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
             for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
                 const Work w = work_item(p, prefix, order, item);
-                const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
+                const int64_t trow = p.k_lens != nullptr ? __ldg(p.cu_q + w.b) : w.b;
+                const int32_t* bt_row = p.block_table + trow * p.max_blocks;
                 // page ids come in batches of 32 (one per lane, -1: past Lk, -2:
                 // bad id), so the table's latency is paid once per batch
                 const int pages = (w.ntiles * kBN + p.block_size - 1) / p.block_size;
@@ -736,10 +747,22 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const int64_t row_off =
                 (static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * hstride + (w.kvh * p.group + g_row) * kD;
             uint16_t* dst = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
+            // cascade prefix pass: this row's workspace slot (part 0)
+            const int64_t ws_slot =
+                ((static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * p.num_heads + w.kvh * p.group + g_row) *
+                p.ws_parts;
             if (w.ntiles == 0) {
                 // no visible key for any row of the item: output 0
-                if (row_valid)
-                    for (int c = 0; c < 64; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
+                if (row_valid) {
+                    if (p.ws_o != nullptr) {
+                        float4* wo = reinterpret_cast<float4*>(p.ws_o + ws_slot * kD + 64 * x);
+                        for (int c = 0; c < 16; ++c) wo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (x == 0) p.ws_lse[ws_slot] = -INFINITY;
+                    } else {
+                        for (int c = 0; c < 64; c += 8)
+                            *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
                 continue;
             }
             // ---- Q row -> tensor memory (warpgroup x: elements 64x .. 64x+63), zero past Lq ----
@@ -950,11 +973,19 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 tc_fence_after();
                 const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
                 const float inv = L > 0.f ? 1.f / L : 0.f;
+                if (p.ws_o != nullptr && row_valid && x == 0)
+                    p.ws_lse[ws_slot] = L > 0.f ? m + __log2f(L) : -INFINITY;
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     float o[32];
                     tmem_ld32(tmem_o + c0, o);
-                    if (row_valid) {
+                    if (row_valid && p.ws_o != nullptr) {
+                        float4* wo = reinterpret_cast<float4*>(p.ws_o + ws_slot * kD + 64 * x + c0);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            wo[j] = make_float4(o[4 * j] * inv, o[4 * j + 1] * inv, o[4 * j + 2] * inv,
+                                                o[4 * j + 3] * inv);
+                    } else if (row_valid) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             uint4 q4;
@@ -1120,6 +1151,57 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
         return PA_ERR_CUDA;
     return launch_prefill<false>(p, q_dtype, map_k, map_v, stream);
 }
+
+namespace pa {
+
+// Prefix pass of pa_decode_cascade: group g's members (decode rows
+// cu_groups[g] .. cu_groups[g+1]-1, consecutive in q) attend the group's first
+// shared_lens[g] keys, read through the first member's block-table row, without
+// a causal mask (every member's query comes after the shared prompt); each
+// (member, head) row goes to part 0 of the decode workspace as fp32 O / l and
+// its log-sum-exp.  The caller (pa_decode_cascade) has checked the cache, the
+// types (16-bit, q and cache alike), head size 128 and the group size bound.
+pa_status cascade_prefix_partials(const void* q, pa_dtype dtype, const pa_kv_cache* cache,
+                                  const int32_t* block_table, int32_t max_blocks, const int32_t* cu_groups,
+                                  const int32_t* shared_lens, int32_t num_groups, int32_t max_group_size,
+                                  int32_t max_shared_len, int32_t num_heads, float scale, float* ws_o,
+                                  float* ws_lse, int32_t ws_parts, int32_t* dev_status, pa_stream_t stream) {
+    if (num_groups > kMaxSeqs) return PA_ERR_UNSUPPORTED;
+    const int bs = cache->block_size;
+    const int64_t rows = cache->num_blocks * cache->num_kv_heads * bs;
+    if (rows > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    PrefillParams p{};
+    p.out = nullptr;
+    p.q = static_cast<const uint16_t*>(q);
+    p.block_table = block_table;
+    p.cu_q = cu_groups;
+    p.cu_k = nullptr;
+    p.k_lens = shared_lens;
+    p.status = dev_status;
+    p.num_blocks = cache->num_blocks;
+    p.block_size = bs;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.num_heads = num_heads;
+    p.group = num_heads / cache->num_kv_heads;
+    p.tq = kRows / p.group;
+    p.num_seqs = num_groups;
+    p.max_blocks = max_blocks;
+    p.max_q = max_group_size;
+    p.max_k = max_shared_len;
+    p.causal = 0;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.total_k = -1;
+    p.ws_o = ws_o;
+    p.ws_lse = ws_lse;
+    p.ws_parts = ws_parts;
+    CUtensorMap map_k, map_v;
+    if (!make_cache_map(&map_k, cache->k_cache, rows, dtype, bs) ||
+        !make_cache_map(&map_v, cache->v_cache, rows, dtype, bs))
+        return PA_ERR_CUDA;
+    return launch_prefill<false>(p, dtype, map_k, map_v, stream);
+}
+
+}  // namespace pa
 
 extern "C" pa_status pa_prefill_varlen_packed(void* out, const void* q, const void* k, const void* v,
                                               pa_dtype dtype, const int32_t* cu_seq_lens_q,

@@ -217,6 +217,10 @@ def gqa_shared_decode(seed=3000, device="cpu", groups=64, group_size=4, block_si
                             block_table=np.stack(tables), device=device)
     case.meta["unique_blocks"] = unique
     case.meta["group_size"] = group_size
+    # the sampling groups as a cascade decode sees them: members are
+    # consecutive rows; the shared length is the prompt's whole blocks
+    case.meta["cu_groups"] = np.arange(0, groups * group_size + 1, group_size, dtype=np.int32)
+    case.meta["shared_lens"] = np.array([ns * bs for ns, _ in counts], np.int32)
     # copy-on-write pairs (source = member 0's partial prompt block)
     case.meta["cow_pairs"] = np.array(cow_pairs, np.int32).reshape(-1, 2)
     return case

@@ -91,3 +91,20 @@ def test_unique_bytes_count_shared_blocks_once():
     assert 0 < g.unique_kv_bytes() < g.kv_bytes()
     m = W.mha_decode()
     assert m.unique_kv_bytes() == m.kv_bytes()
+
+
+def test_gqa_groups_share_their_prompt_blocks():
+    # the cascade metadata of the GQA workload: consecutive groups of four whose
+    # rows name the same blocks over the shared length, and differ right after
+    g = W.gqa_shared_decode()
+    cu, sl = g.meta["cu_groups"], g.meta["shared_lens"]
+    bt = g.block_table.numpy()
+    lens = g.seq_lens.numpy()
+    assert cu[0] == 0 and cu[-1] == len(lens) and len(sl) == len(cu) - 1
+    for k in range(len(sl)):
+        rows = bt[cu[k]:cu[k + 1]]
+        nb = sl[k] // g.block_size
+        assert sl[k] % g.block_size == 0 and np.all(sl[k] <= lens[cu[k]:cu[k + 1]])
+        assert np.all(rows[:, :nb] == rows[0, :nb])
+        if cu[k + 1] - cu[k] > 1 and lens[cu[k]] > sl[k]:
+            assert len(set(rows[:, nb].tolist())) == cu[k + 1] - cu[k]
