@@ -1335,40 +1335,84 @@ paged_decode_kernel(const DecodeParams p) {
 }
 
 // Log-sum-exp merge of the partitions of every (sequence, head) that was
-// split.  One warp per (sequence, head); lanes own D/32 output columns.
-template <int QDT, int D>
+// split.  WPP warps share one (sequence, head): each takes every WPP-th
+// partition (four at a time, so their loads overlap), weighting it by
+// exp2(lse - M) against the pair's overall max M; the warps' sums then meet in
+// shared memory.  Lanes own D/32 consecutive output columns.  With hundreds of
+// partitions per pair (long contexts) one warp per pair left most of the GPU
+// idle and each warp waiting on one row load at a time.
+template <int QDT, int D, int WPP>
 __global__ void __launch_bounds__(256)
 paged_decode_reduce_kernel(const DecodeParams p) {
     pdl_wait();
     pdl_trigger();
+    constexpr int DL = D / 32;
+    constexpr int PPC = 8 / WPP;  // (sequence, head) pairs per block
+    __shared__ float red[8][D + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t bh = static_cast<int64_t>(blockIdx.x) * 8 + warp;
-    if (bh >= static_cast<int64_t>(p.num_seqs) * p.num_heads) return;
-    const int b = static_cast<int>(bh / p.num_heads);
-    const int Lc = checked_len(p, b);
-    const int L = Lc < 0 ? 0 : Lc;
-    // cascade: the prefix's partial (part 0), then the suffix's partitions
-    const int np = parts_of(L - seq_start(p, b, L), p.partition) + (p.cu_groups != nullptr ? 1 : 0);
-    if (np <= 1) return;
+    const int sub = warp % WPP;
+    const int64_t bh = static_cast<int64_t>(blockIdx.x) * PPC + warp / WPP;
+    int np = 0;
+    if (bh < static_cast<int64_t>(p.num_seqs) * p.num_heads) {
+        const int b = static_cast<int>(bh / p.num_heads);
+        const int Lc = checked_len(p, b);
+        const int L = Lc < 0 ? 0 : Lc;
+        // cascade: the prefix's partial (part 0), then the suffix's partitions
+        np = parts_of(L - seq_start(p, b, L), p.partition) + (p.cu_groups != nullptr ? 1 : 0);
+    }
+    const bool work = np > 1;  // unsplit pairs were written by the decode kernel
     const float* lse = p.ws_lse + bh * p.max_parts;
     float M = -INFINITY;
-    for (int i = lane; i < np; i += 32) M = fmaxf(M, lse[i]);
+    if (work) {
+        for (int i = lane; i < np; i += 32) M = fmaxf(M, lse[i]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    constexpr int DL = D / 32;
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    }
     float acc[DL];
 #pragma unroll
     for (int d = 0; d < DL; ++d) acc[d] = 0.f;
     float wsum = 0.f;
-    if (M != -INFINITY) {
+    if (work && M != -INFINITY) {
         const float* o = p.ws_o + bh * p.max_parts * D + lane * DL;
-        for (int i = 0; i < np; ++i) {
-            const float w = fast_exp2(lse[i] - M);
-            wsum += w;
+        int i = sub;
+        for (; i + 3 * WPP < np; i += 4 * WPP) {
+            float w[4], v[4][DL];
 #pragma unroll
-            for (int d = 0; d < DL; ++d) acc[d] = fmaf(w, o[static_cast<int64_t>(i) * D + d], acc[d]);
+            for (int u = 0; u < 4; ++u) {
+                w[u] = lse[i + u * WPP];
+#pragma unroll
+                for (int d = 0; d < DL; ++d) v[u][d] = o[static_cast<int64_t>(i + u * WPP) * D + d];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float x = fast_exp2(w[u] - M);
+                wsum += x;
+#pragma unroll
+                for (int d = 0; d < DL; ++d) acc[d] = fmaf(x, v[u][d], acc[d]);
+            }
+        }
+        for (; i < np; i += WPP) {
+            const float x = fast_exp2(lse[i] - M);
+            wsum += x;
+#pragma unroll
+            for (int d = 0; d < DL; ++d) acc[d] = fmaf(x, o[static_cast<int64_t>(i) * D + d], acc[d]);
         }
     }
+    if constexpr (WPP > 1) {
+#pragma unroll
+        for (int d = 0; d < DL; ++d) red[warp][lane * DL + d] = acc[d];
+        if (lane == 0) red[warp][D] = wsum;
+        __syncthreads();
+        if (sub == 0 && work) {
+#pragma unroll
+            for (int k = 1; k < WPP; ++k) {
+#pragma unroll
+                for (int d = 0; d < DL; ++d) acc[d] += red[warp + k][lane * DL + d];
+                wsum += red[warp + k][D];
+            }
+        }
+    }
+    if (sub != 0 || !work) return;
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     using T = typename dtype_traits<QDT>::storage;
     T* out = static_cast<T*>(p.out) + bh * D + lane * DL;
