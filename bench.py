@@ -54,6 +54,7 @@ NCU_TRAFFIC = {
     ("gqa", "07c6a73572c19639"): 1_003_785_472,
     ("long", "07c6a73572c19639"): 1_748_673_610,
     ("mixed", "0932f6a3353bb5b1"): 1_314_560_216,
+    ("mixed", "e5e1d4af739c4631"): 1_554_890_240,
 }
 L2_BYTES = 129 * 1024 * 1024
 DECODE_SOURCES = ("decode_impl.cuh", "decode_launch.cuh", "decode_api.cu", "common.cuh")
