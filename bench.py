@@ -55,6 +55,9 @@ NCU_TRAFFIC = {
     ("long", "07c6a73572c19639"): 1_748_673_610,
     ("mixed", "0932f6a3353bb5b1"): 1_314_560_216,
     ("mixed", "e5e1d4af739c4631"): 1_554_890_240,
+    ("mha", "c47a7983c3cb25e9"): 945_337_856,
+    ("gqa", "c47a7983c3cb25e9"): 939_493_120,
+    ("long", "c47a7983c3cb25e9"): 1_748_532_224,
 }
 L2_BYTES = 129 * 1024 * 1024
 DECODE_SOURCES = ("decode_impl.cuh", "decode_launch.cuh", "decode_api.cu", "common.cuh")
