@@ -13,22 +13,23 @@
 //
 // Work item = (sequence, tile of TQ = 128/G query tokens, KV head): its 128
 // rows are the G query heads of the KV head for TQ tokens (row = t*G + g), so
-// one key/value tile serves the whole GQA group.  Per item, key tiles of 64
-// keys stream through a 3-stage shared-memory ring:
+// one key/value tile serves the whole GQA group.  Items are sorted by their
+// key-tile count and dealt to the persistent blocks in snake order.  Per
+// item, key tiles of 128 keys stream through separate 3-stage K and V rings:
 //   warp 0      loads pages with TMA tensor copies (128B swizzle), through the
-//               block table;
-//   warp 1      allocates tensor memory and issues the MMAs (one thread):
-//               S = Q K^T into S[t & 1], then O[t & 1] += P[t & 1] V;
-//   warps 4..7, two softmax warpgroups; warpgroup x takes the key tiles
-//   8..11       t = x, x+2, ... of the item with its own S buffer, P buffer
-//               and O accumulator: one row per thread, online max / sum in
-//               fp32 (exp2 domain, lazy rescale of its O in tensor memory), P
-//               to shared memory as 16-bit (bf16: a hi + lo pair, so the
-//               weights keep ~16 bits).  The two partial results are merged
-//               by their log-sum-exp in the epilogue, O / l.
-// Scores are streamed from tensor memory in halves of 32 columns (a max pass,
-// then an exp / sum / store pass), which keeps a softmax thread's registers
-// low enough for 12 warps.
+//               block table (or 3-D boxes of packed K/V);
+//   warp 1      allocates tensor memory and issues every MMA from one thread:
+//               S[t & 1] = Q K(t)^T with Q in tensor memory, then
+//               O += P V(t) with the weights P written over S[t & 1];
+//   warps 4..7, two softmax warpgroups that split the 128 key columns of each
+//   8..11       tile (a thread: 64 columns of one row, its tensor-memory
+//               lane).  They take weights against a shared reference max and
+//               vote at a barrier whether any row's sum would pass 2^64; only
+//               then (and on an item's first tile) is the true max taken,
+//               exchanged through shared memory, O rescaled in tensor memory
+//               and the weights recomputed.  Weights go to tensor memory as
+//               bf16 hi + lo (both truncated, ~16 bits together; two PV
+//               passes) or one fp16.  The epilogue writes O / l.
 // Causal alignment is bottom-right: query i of a sequence with Lq queries and
 // Lk keys sits at position Lk - Lq + i.  Every wait is bounded.
 #include <cuda.h>
