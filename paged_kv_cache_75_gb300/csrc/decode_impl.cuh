@@ -120,7 +120,7 @@ struct DecodeCfg {
 
 // shared memory carve-up (byte offsets from the 1 KB-aligned base)
 struct DecodeSmem {
-    uint32_t ring, qbuf, merge, prefix, order, bars, flags, total;
+    uint32_t ring, qbuf, merge, prefix, order, keys, hist, bars, flags, total;
     __host__ __device__ static DecodeSmem make(int stages, int stage_bytes, int qbytes,
                                                int merge_floats, int num_seqs) {
         DecodeSmem s;
@@ -136,6 +136,10 @@ struct DecodeSmem {
         o += (static_cast<uint32_t>(num_seqs) + 1u) * 4u;
         s.order = o;
         o += static_cast<uint32_t>(num_seqs) * 4u;
+        s.hist = o;  // [8 warps][64 classes] ints
+        o += 8u * 64u * 4u;
+        s.keys = o;  // one class byte per sequence
+        o += (static_cast<uint32_t>(num_seqs) + 15u) & ~15u;
         o = (o + 7u) & ~7u;
         s.bars = o;
         o += (2u * stages + 4u) * 8u;
@@ -195,13 +199,15 @@ __device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
 //
 // prefix[b] = full partitions of sequences < b, prefix[B] = their total F;
 // order[k] = the sequence whose last partition is entry F + k.
-// All threads of the block take part; scratch holds >= 72 ints.
+// All threads of the block take part; scratch holds one int per warp, keys
+// one byte per sequence, hist 64 ints per warp.
 __device__ __forceinline__ int tail_class(int L, int P) {
     const int t = L - (parts_of(L, P) - 1) * P;  // tokens of the last partition, 0..P
     return static_cast<int>((static_cast<int64_t>(P - t) * 64) / (P + 1));  // 0 = longest
 }
 
-__device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, int32_t* order, int32_t* scratch) {
+__device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, int32_t* order, int32_t* scratch,
+                                      uint8_t* keys, int32_t* hist) {
     const int B = p.num_seqs;
     const int nt = blockDim.x, t = threadIdx.x;
     const int chunk = (B + nt - 1) / nt;
@@ -211,7 +217,9 @@ __device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, in
         int L = checked_len(p, b);
         if (L < 0) report(p.status, PA_ERR_INVALID_ARG);
         L = L < 0 ? 0 : L;
-        local += parts_of(L - seq_start(p, b, L), p.partition) - 1;
+        const int n = L - seq_start(p, b, L);
+        local += parts_of(n, p.partition) - 1;
+        keys[b] = static_cast<uint8_t>(tail_class(n, p.partition));
     }
     // inclusive scan inside the warp
     const int lane = t & 31, warp = t >> 5;
@@ -240,51 +248,55 @@ __device__ inline void build_schedule(const DecodeParams& p, int32_t* prefix, in
         L = L < 0 ? 0 : L;
         run += parts_of(L - seq_start(p, b, L), p.partition) - 1;
     }
-    // last partitions: a stable counting sort by length class, done by warp 0
-    // 32 sequences at a time (lanes with equal classes found by match.any)
-    if (warp == 0) {
-        int* bins = scratch + 8;
-        bins[lane] = 0;
-        bins[lane + 32] = 0;
+    // last partitions: a stable counting sort by the class bytes, every warp
+    // counting a contiguous chunk (lanes of equal class found by match.any),
+    // warp 0 turning the [warp][class] counts into class-major offsets, every
+    // warp then placing its chunk in order
+    const int NW = nt / 32;
+    const int wch = ((B + NW - 1) / NW + 31) & ~31;
+    const int c0 = warp * wch, c1 = min(B, c0 + wch);
+    int32_t* h = hist + warp * 64;
+    h[lane] = 0;
+    h[lane + 32] = 0;
+    __syncwarp();
+    for (int cb = c0; cb < c1; cb += 32) {
+        const int b = cb + lane;
+        const int key = b < c1 ? keys[b] : 64;
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        if (b < c1 && lane == __ffs(same) - 1) h[key] += __popc(same);
         __syncwarp();
-        for (int c0 = 0; c0 < B; c0 += 32) {
-            const int b = c0 + lane;
-            int key = 64;
-            if (b < B) {
-                int L = checked_len(p, b);
-                L = L < 0 ? 0 : L;
-                key = tail_class(L - seq_start(p, b, L), p.partition);
-            }
-            const unsigned same = __match_any_sync(0xffffffffu, key);
-            if (b < B && lane == __ffs(same) - 1) bins[key] += __popc(same);
-            __syncwarp();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int tot0 = 0, tot1 = 0;
+        for (int w = 0; w < NW; ++w) {
+            tot0 += hist[w * 64 + 2 * lane];
+            tot1 += hist[w * 64 + 2 * lane + 1];
         }
-        // exclusive scan of the 64 class counts, two per lane
-        const int h0 = bins[2 * lane], h1 = bins[2 * lane + 1];
-        int incl = h0 + h1;
+        int incl = tot0 + tot1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
+            const int x = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += x;
         }
-        __syncwarp();
-        bins[2 * lane] = incl - h0 - h1;
-        bins[2 * lane + 1] = incl - h1;
-        __syncwarp();
-        for (int c0 = 0; c0 < B; c0 += 32) {
-            const int b = c0 + lane;
-            int key = 64;
-            if (b < B) {
-                int L = checked_len(p, b);
-                L = L < 0 ? 0 : L;
-                key = tail_class(L - seq_start(p, b, L), p.partition);
-            }
-            const unsigned same = __match_any_sync(0xffffffffu, key);
-            if (b < B) order[bins[key] + __popc(same & ((1u << lane) - 1u))] = b;
-            __syncwarp();
-            if (b < B && lane == __ffs(same) - 1) bins[key] += __popc(same);
-            __syncwarp();
+        int base0 = incl - tot0 - tot1, base1 = incl - tot1;
+        for (int w = 0; w < NW; ++w) {
+            const int x0 = hist[w * 64 + 2 * lane], x1 = hist[w * 64 + 2 * lane + 1];
+            hist[w * 64 + 2 * lane] = base0;
+            hist[w * 64 + 2 * lane + 1] = base1;
+            base0 += x0;
+            base1 += x1;
         }
+    }
+    __syncthreads();
+    for (int cb = c0; cb < c1; cb += 32) {
+        const int b = cb + lane;
+        const int key = b < c1 ? keys[b] : 64;
+        const unsigned same = __match_any_sync(0xffffffffu, key);
+        if (b < c1) order[h[key] + __popc(same & ((1u << lane) - 1u))] = b;
+        __syncwarp();
+        if (b < c1 && lane == __ffs(same) - 1) h[key] += __popc(same);
+        __syncwarp();
     }
     __syncthreads();
 }
@@ -883,7 +895,8 @@ paged_decode_kernel(const DecodeParams p) {
     }
     // merge area doubles as scan scratch before the first item
     int32_t* order = reinterpret_cast<int32_t*>(smem_raw + L.order);
-    build_schedule(p, prefix, order, reinterpret_cast<int32_t*>(merge));
+    build_schedule(p, prefix, order, reinterpret_cast<int32_t*>(merge), smem_raw + L.keys,
+                   reinterpret_cast<int32_t*>(smem_raw + L.hist));
     const int n_items = (prefix[p.num_seqs] + p.num_seqs) * p.num_kv_heads;
 
     if (warp == C::NCW) {

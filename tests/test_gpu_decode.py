@@ -198,3 +198,16 @@ def test_full_long_fp8_decode_sampled():
     case = W.long_fp8_decode(device=DEV)
     lens = case.seq_lens.cpu().numpy()
     _sampled_check(case, [int(np.argmax(lens))], P=512)
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_many_short_sequences_sampled(G):
+    # 3000 sequences of 1..300 tokens: the work list is sorted across every
+    # warp of a block; sampled sequences checked against the oracle
+    rng = np.random.default_rng(17 + G)
+    lens = rng.integers(1, 301, size=3000)
+    lens[:3] = [1, 300, 16]
+    nb = int(sum(W.pages_for(int(x), 16) for x in lens)) + 5
+    case = W.make_decode_case(40 + G, lens, 2 * G, 2, 128, 16, nb, W.BF16, W.BF16, device=DEV)
+    sample = [0, 1, 2, int(np.argmax(lens)), 2999] + list(range(7, 3000, 331))
+    _sampled_check(case, sample)
