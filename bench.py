@@ -58,6 +58,10 @@ NCU_TRAFFIC = {
     ("mha", "c47a7983c3cb25e9"): 945_337_856,
     ("gqa", "c47a7983c3cb25e9"): 939_493_120,
     ("long", "c47a7983c3cb25e9"): 1_748_532_224,
+    ("mha", "7cb5cae478ced3ab"): 945_331_968,
+    ("gqa", "7cb5cae478ced3ab"): 939_895_040,
+    ("long", "7cb5cae478ced3ab"): 1_748_656_896,
+    ("mixed", "530d95a1f63ff18c"): 1_556_752_896,
 }
 L2_BYTES = 129 * 1024 * 1024
 DECODE_SOURCES = ("decode_impl.cuh", "decode_launch.cuh", "decode_api.cu", "common.cuh")
