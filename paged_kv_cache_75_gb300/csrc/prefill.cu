@@ -514,7 +514,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     }
     const uint32_t tmem = *tmem_slot;
     const int n_items = prefix[B] * p.num_kv_heads;
-    const int64_t hstride = static_cast<int64_t>(p.num_heads) * kD;  // elements per q/out row
     if (warp == 0) {
         // ------------------------------- loader -------------------------------
         // K and V have rings of their own: a K stage is free again once its QK
@@ -745,13 +744,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const int qi = w.i0 + t_row;  // query index of this row in its sequence
             const bool row_valid = qi < w.lq;
             const int lim = p.causal ? min(w.lk, shift + qi + 1) : w.lk;  // keys [0, lim) visible
-            const int64_t row_off =
-                (static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * hstride + (w.kvh * p.group + g_row) * kD;
+            // this row's (query row, head); its place in q / out and (cascade
+            // prefix pass) its workspace slot, part 0, follow from these two
+            const int qrow = __ldg(p.cu_q + w.b) + qi, head = w.kvh * p.group + g_row;
+            const int64_t row_off = (static_cast<int64_t>(qrow) * p.num_heads + head) * kD;
             uint16_t* dst = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
-            // cascade prefix pass: this row's workspace slot (part 0)
-            const int64_t ws_slot =
-                ((static_cast<int64_t>(__ldg(p.cu_q + w.b)) + qi) * p.num_heads + w.kvh * p.group + g_row) *
-                p.ws_parts;
+            const int64_t ws_slot = (static_cast<int64_t>(qrow) * p.num_heads + head) * p.ws_parts;
             if (w.ntiles == 0) {
                 // no visible key for any row of the item: output 0
                 if (row_valid) {
@@ -974,14 +972,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 tc_fence_after();
                 const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
                 const float inv = L > 0.f ? 1.f / L : 0.f;
+                const int64_t ws_e = (static_cast<int64_t>(qrow) * p.num_heads + head) * p.ws_parts;
+                uint16_t* dst_e = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_heads + head) * kD +
+                                  64 * x;
                 if (p.ws_o != nullptr && row_valid && x == 0)
-                    p.ws_lse[ws_slot] = L > 0.f ? m + __log2f(L) : -INFINITY;
+                    p.ws_lse[ws_e] = L > 0.f ? m + __log2f(L) : -INFINITY;
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     float o[32];
                     tmem_ld32(tmem_o + c0, o);
                     if (row_valid && p.ws_o != nullptr) {
-                        float4* wo = reinterpret_cast<float4*>(p.ws_o + ws_slot * kD + 64 * x + c0);
+                        float4* wo = reinterpret_cast<float4*>(p.ws_o + ws_e * kD + 64 * x + c0);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             wo[j] = make_float4(o[4 * j] * inv, o[4 * j + 1] * inv, o[4 * j + 2] * inv,
@@ -994,7 +995,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                             q4.y = pack2<DT>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
                             q4.z = pack2<DT>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
                             q4.w = pack2<DT>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
-                            *reinterpret_cast<uint4*>(dst + c0 + 8 * j) = q4;
+                            *reinterpret_cast<uint4*>(dst_e + c0 + 8 * j) = q4;
                         }
                     }
                 }
