@@ -237,7 +237,7 @@ class DecodeStep:
                                          partition_size)
         self.ws = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         self.kv_bytes = case.kv_bytes()
-        P = partition_size or (1024 if case.num_heads // case.num_kv_heads >= 4 else 512)
+        P = partition_size or pk.pa_decode_partition_size(B, case.num_heads, case.num_kv_heads, self.max_len)
         self.P_eff = P
         self.split = self.max_len > P
         self.launches_per_step = 2 + (1 if self.split else 0)

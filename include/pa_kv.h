@@ -147,9 +147,11 @@ pa_status pa_copy_blocks(const pa_kv_cache* cache, const int32_t* src_dst_pairs,
  *   <= max_blocks_per_seq*block_size, otherwise PA_ERR_INVALID_ARG is
  *   reported and the sequence's output is 0.
  * partition_size: tokens per context partition (a multiple of block_size),
- *   0 = automatic (512, or 1024 when num_heads / num_kv_heads >= 4; the
- *   workspace size query answers for 512, which covers both).  A sequence
- *   longer than one partition is split; the
+ *   0 = automatic (pa_decode_partition_size: 2048, or 1024 when num_heads /
+ *   num_kv_heads >= 4, halved down to 512 while the (sequence, KV head,
+ *   partition) work items would not fill the GPU twice over; the workspace
+ *   size query answers for 512, which covers every automatic choice).  A
+ *   sequence longer than one partition is split; the
  *   partitions' partial results go to `workspace` and a second kernel merges
  *   them by their log-sum-exp.
  * workspace: device scratch of at least pa_decode_workspace_size(...) bytes,
@@ -159,6 +161,11 @@ pa_status pa_copy_blocks(const pa_kv_cache* cache, const int32_t* src_dst_pairs,
  * ------------------------------------------------------------------------- */
 size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
                                 int32_t max_seq_len, int32_t block_size, int32_t partition_size);
+
+/* The partition size pa_decode takes for partition_size = 0 on the current
+ * device (host call, no launch); 0 for invalid arguments. */
+int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                 int32_t max_seq_len);
 
 pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
                     const int32_t* block_table, int32_t max_blocks_per_seq,

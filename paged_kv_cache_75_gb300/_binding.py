@@ -67,6 +67,7 @@ def library():
             "pa_decode_static_ws": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, vp],
                                     C.c_int),
             "pa_decode_cascade_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+            "pa_decode_partition_size": ([i32, i32, i32, i32], i32),
             "pa_decode_cascade": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, vp, vp, i32, i32, i32,
                                    i32, vp, sz, vp, vp], C.c_int),
         }
@@ -275,6 +276,11 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: t
                              block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), H, float(scale),
                              int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(q))
     _check(st, "pa_decode")
+
+
+def pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, max_seq_len) -> int:
+    """The partition size pa_decode chooses for partition_size = 0 on the current device."""
+    return int(library().pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, max_seq_len))
 
 
 def pa_decode_cascade_workspace_size(num_seqs, num_heads, head_size, max_seq_len, block_size,

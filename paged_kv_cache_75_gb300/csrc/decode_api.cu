@@ -6,17 +6,25 @@
 namespace pa {
 namespace {
 
-// Automatic partition: 512 tokens, or 1024 when a KV head serves 4 or more
-// query heads -- an item's fixed work (query load, merge and partial write of
-// every head) grows with the group, so longer items pay it less often.  A
-// workspace sized with group 1 (512) covers both.
-int resolve_partition(int partition_size, int block_size, int group) {
-    if (partition_size == 0) {
-        const int p = group >= 4 ? 1024 : 512;
-        return p % block_size == 0 ? p : block_size * ((p + block_size - 1) / block_size);
-    }
-    return partition_size;
+// Automatic partition: the longest of 2048 (1024 when a KV head serves four or
+// more query heads, whose items already carry more fixed work) halved down to
+// 512 tokens while the (sequence, KV head, partition) items would not fill two
+// rounds of resident blocks.  Fewer, longer items save the partials and the
+// merge; the balanced schedule keeps long items from leaving blocks idle.
+int auto_partition(int64_t num_seqs, int num_kv_heads, int max_seq_len, int group) {
+    int p = group >= 4 ? 1024 : 2048;
+    const int64_t want = 2ll * 3 * device_sm_count();
+    const int64_t pairs = num_seqs * num_kv_heads;
+    while (p > 512 && pairs * ((max_seq_len + p - 1) / p) < want) p >>= 1;
+    return p;  // a power of two >= 512: a multiple of every block size
 }
+
+int resolve_partition(int partition_size, int64_t num_seqs, int num_kv_heads, int max_seq_len, int group) {
+    return partition_size > 0 ? partition_size : auto_partition(num_seqs, num_kv_heads, max_seq_len, group);
+}
+
+// Workspace sizes hold for any automatic choice: it never goes below 512.
+int ws_partition(int partition_size) { return partition_size > 0 ? partition_size : 512; }
 
 int max_parts_of(int max_seq_len, int partition) {
     return max_seq_len <= partition ? 1 : (max_seq_len + partition - 1) / partition;
@@ -47,7 +55,7 @@ extern "C" size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, 
     if (num_seqs <= 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0 || block_size <= 0 ||
         partition_size < 0)
         return 0;
-    const int P = resolve_partition(partition_size, block_size, 1);
+    const int P = ws_partition(partition_size);
     return ws_layout(num_seqs, num_heads, head_size, max_parts_of(max_seq_len, P)).bytes;
 }
 
@@ -88,7 +96,7 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
         !(cache->k_scale > 0.f && std::isfinite(cache->k_scale) && cache->v_scale > 0.f &&
           std::isfinite(cache->v_scale)))
         return PA_ERR_INVALID_ARG;
-    const int P = resolve_partition(partition_size, bs, group);
+    const int P = resolve_partition(partition_size, num_seqs, cache->num_kv_heads, max_seq_len, group);
     if (P % bs != 0) return PA_ERR_INVALID_ARG;
     if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
     if (cu_groups != nullptr && (shared_lens == nullptr || num_groups <= 0 || k_new != nullptr))
@@ -170,13 +178,20 @@ extern "C" pa_status pa_decode_append(void* out, const void* q, const void* k_ne
                             stream, k_new, v_new);
 }
 
+extern "C" int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                            int32_t max_seq_len) {
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || max_seq_len < 0)
+        return 0;
+    return auto_partition(num_seqs, num_kv_heads, max_seq_len, num_heads / num_kv_heads);
+}
+
 extern "C" size_t pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
                                                    int32_t max_seq_len, int32_t block_size,
                                                    int32_t partition_size) {
     if (num_seqs <= 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0 || block_size <= 0 ||
         partition_size < 0)
         return 0;
-    const int P = resolve_partition(partition_size, block_size, 1);
+    const int P = ws_partition(partition_size);
     return ws_layout(num_seqs, num_heads, head_size, max_parts_of(max_seq_len, P) + 1).bytes;
 }
 
@@ -207,7 +222,7 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, pa_dtype q_dtyp
     if (max_group_size < 1 || max_group_size > 128 / group) return PA_ERR_UNSUPPORTED;
     if (max_shared_len < 0 || max_shared_len > max_seq_len || max_shared_len % bs != 0) return PA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 15u)) return PA_ERR_INVALID_ARG;
-    const int P = resolve_partition(partition_size, bs, group);
+    const int P = resolve_partition(partition_size, num_seqs, cache->num_kv_heads, max_seq_len, group);
     if (P <= 0 || P % bs != 0) return PA_ERR_INVALID_ARG;
     const int max_parts = max_parts_of(max_seq_len, P) + 1;
     const WsLayout w = ws_layout(num_seqs, num_heads, cache->head_size, max_parts);
