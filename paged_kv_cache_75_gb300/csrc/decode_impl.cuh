@@ -533,8 +533,13 @@ __device__ __forceinline__ uint32_t pack_pair(float lo, float hi) {
 //    them into V^T A fragments, whose rows (d) then follow the span order:
 //    m-tile mt, row r<8 is d = W*(r/2) + 4*mt + r%2 (with the chunk rotation
 //    below, the owner's chunk in place of mt/2), row r>=8 that d + 2;
-//  * bf16 weights go in as hi + lo (two MMAs) so they keep 16 bits; fp16
-//    weights (fp16 and E4M3 caches, V exact in fp16) take one MMA.
+//  * bf16 weights go in as hi + lo so they keep 16 bits; fp16 weights (fp16
+//    and E4M3 caches, V exact in fp16) take one MMA.  With four heads the
+//    queries fill columns 0..3 and again 4..7, so lanes ti >= 2 carry the
+//    same scores and softmax state as lanes ti - 2 and hand in the lo
+//    weights in columns 4..7: one MMA per tile takes hi and lo at once, and
+//    the two halves of O are added when the item ends.  Otherwise (eight
+//    heads) the lo weights take a second MMA.
 // Masked tokens (past the item or on a missing page) get weight 0 and their
 // V rows are zeroed before the MMA, so stale stage bytes never reach a sum.
 template <typename C, int QDT, int KVDT, int D, int G, int BS>
@@ -545,6 +550,7 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
                                                     volatile int* stage_mask, int warp, int lane) {
     constexpr int MT = C::KB == 2 ? KVDT : PA_F16;  // operand type of both products
     constexpr bool HILO = MT == PA_BF16;
+    constexpr bool PACK = HILO && G == 4;  // lo weights in the columns of heads 4..7
     constexpr int W = D / 4;   // d-span of a lane, elements
     constexpr int KS = D / 16; // QK k-steps = PV m-tiles
     constexpr int SL = C::SLICES;
@@ -569,12 +575,13 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
         uint32_t qb[KS][2];
         float qk_scale = p.qk_scale;
         {
-            const uint8_t* qs = qbuf + slot * QSLOT + (gi * D + W * ti) * C::QB;
+            const int qh = PACK ? (gi & 3) : gi;  // the head of MMA column gi
+            const uint8_t* qs = qbuf + slot * QSLOT + (qh * D + W * ti) * C::QB;
             if constexpr (C::KB == 2) {
 #pragma unroll
                 for (int c = 0; c < W / 8; ++c) {
                     uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                    if (gi < G) x = *reinterpret_cast<const uint4*>(qs + 16 * ((c + rot) & (NCH - 1)));
+                    if (PACK || gi < G) x = *reinterpret_cast<const uint4*>(qs + 16 * ((c + rot) & (NCH - 1)));
                     qb[2 * c][0] = x.x;
                     qb[2 * c][1] = x.y;
                     qb[2 * c + 1][0] = x.z;
@@ -667,13 +674,21 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
                     const float s1 = v0 ? (sa[1] + sb[1]) * qk_scale : -INFINITY;
                     const float s2 = v1 ? (sa[2] + sb[2]) * qk_scale : -INFINITY;
                     const float s3 = v1 ? (sa[3] + sb[3]) * qk_scale : -INFINITY;
-                    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                    // The reference max of a head moves only when one of its
+                    // scores passes it by more than tau; a lane tests its own
+                    // four and the warp votes, so the reduction over the slice's
+                    // tokens runs only then (an item's first slice, and rarely
+                    // after it)
+                    if (__any_sync(0xffffffffu, fmaxf(s0, s2) > m0 + kTau || fmaxf(s1, s3) > m1 + kTau)) {
+                        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                        // (with the lo columns, also over lanes ti and ti^2, whose
+                        // scores are the same products in two MMA columns: one
+                        // max, so both halves of O always share one reference)
 #pragma unroll
-                    for (int o2 = 4; o2 < 32; o2 <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
-                    }
-                    if (__any_sync(0xffffffffu, mx0 > m0 + kTau || mx1 > m1 + kTau)) {
+                        for (int o2 = PACK ? 2 : 4; o2 < 32; o2 <<= 1) {
+                            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+                            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+                        }
                         const bool r0 = mx0 > m0 + kTau, r1 = mx1 > m1 + kTau;
                         const float a0 = r0 ? fast_exp2(m0 - mx0) : 1.f, a1 = r1 ? fast_exp2(m1 - mx1) : 1.f;
                         m0 = r0 ? mx0 : m0;
@@ -693,8 +708,23 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
                     l0 += p0 + p2;
                     l1 += p1 + p3;
                     // ---- P^T fragments (token pair, head gi) ----
-                    uint32_t pb0, pb1, pl0 = 0u, pl1 = 0u;
-                    if constexpr (HILO) {
+                    uint32_t pb0, pb1;
+                    [[maybe_unused]] uint32_t pl0 = 0u, pl1 = 0u;
+                    if constexpr (PACK) {
+                        // columns 0..3 (lanes ti < 2): hi = the top 16 bits; columns
+                        // 4..7 (lanes ti >= 2, the same heads): lo = the rest in bf16
+                        const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+                        const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
+                        uint32_t w0 = __byte_perm(u0, u1, 0x7632), w1 = __byte_perm(u2, u3, 0x7632);
+                        if (ti >= 2) {
+                            w0 = pack_pair<PA_BF16>(p0 - __uint_as_float(u0 & 0xffff0000u),
+                                                    p1 - __uint_as_float(u1 & 0xffff0000u));
+                            w1 = pack_pair<PA_BF16>(p2 - __uint_as_float(u2 & 0xffff0000u),
+                                                    p3 - __uint_as_float(u3 & 0xffff0000u));
+                        }
+                        pb0 = movtrans(w0);
+                        pb1 = movtrans(w1);
+                    } else if constexpr (HILO) {
                         // hi = the top 16 bits (truncation), lo = the rest rounded to bf16
                         const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
                         const uint32_t u2 = __float_as_uint(p2), u3 = __float_as_uint(p3);
@@ -726,7 +756,7 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
                                            td1 = movtrans(y1.w);
                             mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pb0, pb1);
                             mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pb0, pb1);
-                            if constexpr (HILO) {
+                            if constexpr (HILO && !PACK) {
                                 mma16816<MT>(o[2 * c], ta0, tb0, ta1, tb1, pl0, pl1);
                                 mma16816<MT>(o[2 * c + 1], tc0, td0, tc1, td1, pl0, pl1);
                             }
@@ -760,6 +790,13 @@ __device__ __forceinline__ void decode_consumer_mma(const DecodeParams& p, uint8
         }
 
         // ---- this warp's partials to the merge area ----
+        if constexpr (PACK) {
+            // the lo half of each head's sum sits two lanes up (columns 4..7)
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) o[mt][r] += __shfl_xor_sync(0xffffffffu, o[mt][r], 2);
+        }
 #pragma unroll
         for (int o2 = 4; o2 < 32; o2 <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
