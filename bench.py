@@ -350,16 +350,35 @@ def build_workload(name, device, num_seqs=None, pool_blocks=None):
     raise ValueError(name)
 
 
+def kernel_pass(stream, steps, before, kernel, flush=None):
+    """Mean ms of `kernel` over `steps` launches, each bracketed by CUDA events
+    on `stream` with `before` (the step's other launches) ahead of it.  An
+    event between two launches ends their programmatic overlap, so this pass
+    runs after the timed steps, not inside them."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        before()
+        evs[i][0].record(stream)
+        kernel()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
 def timed_decode(step: DecodeStep, steps, warmup, world, flush):
     """Returns (total ms over the timed steps, mean decode-kernel ms, clocks).
-    With an L2 flush, every step is timed on its own (write + decode) and the
-    flush runs between the timed intervals."""
+    The timed steps (write + decode) carry no event between their launches;
+    with an L2 flush every step is timed on its own and the flush runs between
+    the timed intervals.  The decode kernel's own duration comes from a second
+    pass over the same steps with events around each decode launch; clocks are
+    sampled over both."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         step.write()
         step.decode()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     whole = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -367,18 +386,18 @@ def timed_decode(step: DecodeStep, steps, warmup, world, flush):
     with ClockSampler(torch.cuda.current_device()) as clk:
         start.record(stream)
         for i in range(steps):
-            flush()
-            whole[i][0].record(stream)
+            if flush.buf is not None:
+                flush()
+                whole[i][0].record(stream)
             step.write()
-            evs[i][0].record(stream)
             step.decode()
-            evs[i][1].record(stream)
-            whole[i][1].record(stream)
+            if flush.buf is not None:
+                whole[i][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
+        barrier(world)
+        decode_ms = kernel_pass(stream, steps, step.write, step.decode, flush if flush.buf is not None else None)
     total_ms = sum(a.elapsed_time(b) for a, b in whole) if flush.buf is not None else start.elapsed_time(end)
-    decode_ms = sum(a.elapsed_time(b) for a, b in evs) / steps
     st = int(step.status.item())
     if st != 0:
         raise RuntimeError("device status %d during the benchmark" % st)
@@ -448,12 +467,15 @@ def timed_graph(step: DecodeStep, steps, flush):
 
 
 def timed_prefill(step: PrefillStep, steps, warmup, world):
+    """Returns (total ms over the timed steps, mean varlen-kernel ms, clocks):
+    the timed steps (write + varlen call) carry no event between their
+    launches; the kernel's own duration comes from a second pass with events
+    around each varlen launch."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         step.write()
         step.main()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
@@ -461,49 +483,109 @@ def timed_prefill(step: PrefillStep, steps, warmup, world):
         start.record(stream)
         for i in range(steps):
             step.write()
-            evs[i][0].record(stream)
             step.main()
-            evs[i][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
-    barrier(world)
+        barrier(world)
+        kernel_ms = kernel_pass(stream, steps, step.write, step.main)
     st = int(step.status.item())
     if st != 0:
         raise RuntimeError("device status %d during the benchmark" % st)
-    return start.elapsed_time(end), sum(a.elapsed_time(b) for a, b in evs) / steps, clk.summary()
+    return start.elapsed_time(end), kernel_ms, clk.summary()
 
 
-def timed_prefill_e2e(step: PrefillStep, steps, warmup, world):
-    host = {n: t.cpu().pin_memory() for n, t in (("q", step.q), ("k", step.k_new), ("v", step.v_new),
-                                                 ("slots", step.slots), ("cu_q", step.cu_q), ("cu_k", step.cu_k),
-                                                 ("bt", step.bt))}
-    dev = {n: torch.empty_like(t, device=step.device) for n, t in host.items()}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
-    pk = step.pk
+E2E_NOTE = ("double-buffered: step i+1's inputs go up on one copy stream while step i computes, "
+            "step i's output comes back on another; the host waits for each step's output one step later; "
+            "every step's copies are inside the timed region")
 
-    def one():
-        for n, t in host.items():
-            dev[n].copy_(t, non_blocking=True)
-        pk.pa_kv_cache_write(step.cache, dev["k"], dev["v"], dev["slots"], step.status)
-        pk.pa_prefill_varlen(step.out, dev["q"], step.cache, dev["bt"], dev["cu_q"], dev["cu_k"], step.max_q,
-                             step.max_k, step.case.scale, True, step.status)
-        out_host.copy_(step.out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
 
-    for _ in range(warmup):
-        one()
+def pipelined_e2e(device, src, out_like, launch, steps, warmup, world):
+    """End-to-end steps through the public API with host buffers, as a serving
+    loop runs them: every step copies its inputs (`src`, packed into one
+    page-locked buffer of 16-byte-aligned pieces) to the device and its output
+    back to page-locked host memory.  Two device copies of the inputs and of
+    the output let step i+1's upload and step i-1's download overlap step i's
+    kernels; the host waits for each step's output one step later.
+    `launch(views, out)` issues a step's library calls on the current stream.
+    Returns (ms for `steps` steps, H2D bytes per step, D2H bytes per step)."""
+    offs, total = {}, 0
+    for n, t in src:
+        offs[n] = total
+        total += (t.numel() * t.element_size() + 15) // 16 * 16
+    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+
+    def view(buf, n, t):
+        nbytes = t.numel() * t.element_size()
+        return buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
+
+    for n, t in src:
+        view(host_buf, n, t).copy_(t.cpu())
+    dev_bufs = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(2)]
+    views = [{n: view(buf, n, t) for n, t in src} for buf in dev_bufs]
+    outs = [torch.empty_like(out_like) for _ in range(2)]
+    out_host = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
+    comp = torch.cuda.current_stream(device)
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def upload(i):
+        b = i % 2
+        up.wait_event(ev_done[b])  # step i-2 has finished with these inputs
+        with torch.cuda.stream(up):
+            dev_bufs[b].copy_(host_buf, non_blocking=True)
+        ev_in[b].record(up)
+
+    def run(n, start=None):
+        if start is not None:
+            up.wait_event(start)
+        upload(0)
+        for i in range(n):
+            b = i % 2
+            comp.wait_event(ev_in[b])
+            comp.wait_event(ev_out[b])  # step i-2's output has been read back
+            launch(views[b], outs[b])
+            ev_done[b].record(comp)
+            if i + 1 < n:
+                upload(i + 1)
+            down.wait_event(ev_done[b])
+            with torch.cuda.stream(down):
+                out_host[b].copy_(outs[b], non_blocking=True)
+            ev_out[b].record(down)
+            if i >= 1:
+                ev_out[(i - 1) % 2].synchronize()  # the host takes step i-1's output
+        comp.wait_event(ev_out[(n - 1) % 2])
+
+    run(warmup)
+    torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        one()
-    end.record()
+    start.record(comp)
+    run(steps, start)
+    end.record(comp)
+    end.synchronize()
     torch.cuda.synchronize()
     barrier(world)
+    h2d = total
+    d2h = out_like.numel() * out_like.element_size()
     return start.elapsed_time(end), h2d, d2h
+
+
+def timed_prefill_e2e(step: PrefillStep, steps, warmup, world):
+    """The mixed step end to end: q, the new K/V, slots, cumulative lengths and
+    block table up from page-locked host memory, the output back."""
+    src = (("q", step.q), ("k", step.k_new), ("v", step.v_new), ("slots", step.slots), ("cu_q", step.cu_q),
+           ("cu_k", step.cu_k), ("bt", step.bt))
+    pk = step.pk
+
+    def launch(dev, out):
+        pk.pa_kv_cache_write(step.cache, dev["k"], dev["v"], dev["slots"], step.status)
+        pk.pa_prefill_varlen(out, dev["q"], step.cache, dev["bt"], dev["cu_q"], dev["cu_k"], step.max_q,
+                             step.max_k, step.case.scale, True, step.status)
+
+    return pipelined_e2e(step.device, src, step.out, launch, steps, warmup, world)
 
 
 def timed_split(step: PrefillStep, steps, warmup):
@@ -569,7 +651,7 @@ def run_prefill(args, case, wname, dev, rank, world):
         "clocks": clocks,
         "e2e": {"value": round(flops_e2e / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "pipeline": E2E_NOTE},
         "gpu_launches": step.launches_per_step * args.steps,
         "split": None if split_ms is None else {
             "ms_per_step": round(split_ms, 5), "value": round(step.flops / (split_ms / 1e3) / 1e12, 2),
@@ -589,52 +671,17 @@ def run_prefill(args, case, wname, dev, rank, world):
 
 
 def timed_e2e(step: DecodeStep, steps, warmup, world):
-    """Same step through the public API with host buffers: each step copies
-    q, the new K/V, slots, block table and lengths from pinned host memory and
-    reads the output back."""
-    # the step's inputs packed into one page-locked buffer (16-byte aligned
-    # pieces), so a step takes one host-to-device copy; the library's
-    # arguments are views of its device copy
+    """The decode step end to end: q, the new K/V, slots, block table and
+    lengths up from page-locked host memory, the output back."""
     src = (("q", step.q), ("k", step.k_new), ("v", step.v_new), ("slots", step.slots), ("bt", step.bt),
            ("lens", step.lens))
-    offs, total = {}, 0
-    for n, t in src:
-        offs[n] = total
-        total += (t.numel() * t.element_size() + 15) // 16 * 16
-    host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
-    dev_buf = torch.empty(total, dtype=torch.uint8, device=step.device)
-
-    def view(buf, n, t):
-        nbytes = t.numel() * t.element_size()
-        return buf[offs[n]:offs[n] + nbytes].view(t.dtype).view(t.shape)
-
-    for n, t in src:
-        view(host_buf, n, t).copy_(t.cpu())
-    dev = {n: view(dev_buf, n, t) for n, t in src}
-    out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-    h2d = total
-    d2h = out_host.numel() * out_host.element_size()
     pk = step.pk
 
-    def one():
-        dev_buf.copy_(host_buf, non_blocking=True)
+    def launch(dev, out):
         pk.pa_kv_cache_write(step.cache, dev["k"], dev["v"], dev["slots"], step.status)
-        step.decode(q=dev["q"], out=step.out, bt=dev["bt"], lens=dev["lens"])
-        out_host.copy_(step.out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        step.decode(q=dev["q"], out=out, bt=dev["bt"], lens=dev["lens"])
 
-    for _ in range(warmup):
-        one()
-    barrier(world)
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        one()
-    end.record()
-    torch.cuda.synchronize()
-    barrier(world)
-    return start.elapsed_time(end), h2d, d2h
+    return pipelined_e2e(step.device, src, step.out, launch, steps, warmup, world)
 
 
 def oracle_decode_seconds(case: W.PagedCase, seq_idx, nthreads, q_bits, kc, vc, bt, lens):
@@ -889,7 +936,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": {"value": round(kv_e2e / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "pipeline": E2E_NOTE},
         "gpu_launches": step.launches_per_step * args.steps,
         "fused_append": {"ms_per_step": round(fused_ms, 5),
                          "value": round(step.kv_bytes / (fused_ms / 1e3) / 1e9, 2), "unit": "GB/s",
