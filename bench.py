@@ -62,6 +62,9 @@ NCU_TRAFFIC = {
     ("gqa", "7cb5cae478ced3ab"): 939_895_040,
     ("long", "7cb5cae478ced3ab"): 1_748_656_896,
     ("mixed", "530d95a1f63ff18c"): 1_556_752_896,
+    ("mha", "6c3aaacd1f8b3e95"): 944_406_528,
+    ("gqa", "6c3aaacd1f8b3e95"): 939_486_464,
+    ("long", "6c3aaacd1f8b3e95"): 1_748_525_824,
     ("mha", "11ea94ecf1cf01da"): 944_880_128,
     ("gqa", "11ea94ecf1cf01da"): 939_508_992,
     ("long", "11ea94ecf1cf01da"): 1_748_537_088,
