@@ -291,9 +291,10 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
  * computes exactly what pa_decode computes (the same softmax(q K^T scale) V per
  * sequence and head, up to fp32 rounding order) but reads a group's shared
  * blocks once for all of its members: a prefix pass (the varlen tensor-core
- * kernel, no causal mask) attends every member's query to the shared tokens,
- * a suffix pass (the decode kernel) attends each member's own tokens, and the
- * log-sum-exp merge of pa_decode combines the two.
+ * kernel, no causal mask) attends every member's query to the shared tokens in
+ * parts of the decode's partition length, a suffix pass (the decode kernel)
+ * attends each member's own tokens, and the log-sum-exp merge of pa_decode
+ * combines all parts.
  *
  * cu_groups: device int32 [num_groups+1], 0 = cu_groups[0] <= ... <=
  *   cu_groups[num_groups] = num_seqs; sequences cu_groups[g] .. cu_groups[g+1]-1

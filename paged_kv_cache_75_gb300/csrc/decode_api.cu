@@ -101,7 +101,8 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
     if (cu_groups != nullptr && (shared_lens == nullptr || num_groups <= 0 || k_new != nullptr))
         return PA_ERR_INVALID_ARG;
-    // cascade: one more part per (sequence, head) for the shared prefix's partial
+    // cascade: the prefix's parts (ceil(s0/P)) and the suffix's (parts_of(L-s0))
+    // never exceed parts_of(L) + 1
     const int max_parts = max_parts_of(max_seq_len, P) + (cu_groups != nullptr ? 1 : 0);
     const WsLayout w = ws_layout(num_seqs, num_heads, D, max_parts);
     if (w.bytes > 0 && (workspace == nullptr || workspace_bytes < w.bytes ||
@@ -232,7 +233,7 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, pa_dtype q_dtyp
     // 1) shared prefixes, once per group; 2) every member's own suffix; 3) the
     //    log-sum-exp merge of both (launched by the decode entry)
     st = cascade_prefix_partials(q, q_dtype, cache, block_table, max_blocks_per_seq, cu_groups, shared_lens,
-                                 num_groups, max_group_size, max_shared_len, num_heads, scale, ws_o, ws_lse,
+                                 num_groups, max_group_size, max_shared_len, P, num_heads, scale, ws_o, ws_lse,
                                  max_parts, dev_status, stream);
     if (st != PA_OK) return st;
     return decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,

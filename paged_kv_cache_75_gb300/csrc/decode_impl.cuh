@@ -64,10 +64,10 @@ struct DecodeParams {
     const void* v_new;
     float k_scale_w, v_scale_w;  // E4M3 cache: the write's scales
     // cascade suffix pass: sequences cu_groups[g] .. cu_groups[g+1]-1 form group
-    // g, whose first shared_lens[g] tokens (whole blocks, the same physical
-    // blocks in every member) a prefix pass has attended; this launch attends
-    // tokens [shared_lens[g], L) and writes every partial to the workspace from
-    // part 1 on (part 0 holds the prefix's)
+    // g, whose first s0 = shared_lens[g] tokens (whole blocks, the same physical
+    // blocks in every member) a prefix pass has attended in parts of
+    // `partition` tokens (workspace parts 0 .. ceil(s0/partition)-1); this
+    // launch attends tokens [s0, L) and writes its partials after those
     const int32_t* cu_groups;
     const int32_t* shared_lens;
     int32_t num_groups;
@@ -152,6 +152,11 @@ struct DecodeSmem {
 
 // number of partitions a sequence of length L splits into (>= 1)
 __device__ __forceinline__ int parts_of(int L, int P) { return L <= P ? 1 : (L + P - 1) / P; }
+
+// cascade: workspace parts the prefix pass filled for a shared length s0
+__device__ __forceinline__ int prefix_parts(const DecodeParams& p, int s0) {
+    return p.cu_groups != nullptr ? (s0 + p.partition - 1) / p.partition : 0;
+}
 
 // Cascade suffix pass: the group of sequence b (largest g with cu_groups[g] <= b).
 __device__ __forceinline__ int group_of(const DecodeParams& p, int b) {
@@ -435,7 +440,7 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
     {
         const int tid = threadIdx.x;  // 0 .. NCW*32-1
         const bool direct = it.nparts == 1 && p.cu_groups == nullptr;
-        const int part = it.part + (p.cu_groups != nullptr ? 1 : 0);  // cascade: part 0 is the prefix's
+        const int part = it.part + prefix_parts(p, it.s0);  // cascade: after the prefix's parts
         for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
             const int g = (2 * e) / D, d = (2 * e) % D;
             const int ghg = g / C::GW, gw = g % C::GW;
@@ -1407,10 +1412,13 @@ paged_decode_reduce_kernel(const DecodeParams p) {
         const int b = static_cast<int>(bh / p.num_heads);
         const int Lc = checked_len(p, b);
         const int L = Lc < 0 ? 0 : Lc;
-        // cascade: the prefix's partial (part 0), then the suffix's partitions
-        np = parts_of(L - seq_start(p, b, L), p.partition) + (p.cu_groups != nullptr ? 1 : 0);
+        // cascade: the prefix's parts, then the suffix's partitions
+        const int s0 = seq_start(p, b, L);
+        np = parts_of(L - s0, p.partition) + prefix_parts(p, s0);
     }
-    const bool work = np > 1;  // unsplit pairs were written by the decode kernel
+    // unsplit pairs were written by the decode kernel (a cascade's all go
+    // through the workspace)
+    const bool work = np > 1 || (np == 1 && p.cu_groups != nullptr);
     const float* lse = p.ws_lse + bh * p.max_parts;
     float M = -INFINITY;
     if (work) {
