@@ -353,6 +353,10 @@ def build_workload(name, device, num_seqs=None, pool_blocks=None):
     raise ValueError(name)
 
 
+def unique_bytes_of(case):
+    return case.unique_kv_bytes()
+
+
 def kernel_pass(stream, steps, before, kernel, flush=None):
     """Mean ms of `kernel` over `steps` launches, each bracketed by CUDA events
     on `stream` with `before` (the step's other launches) ahead of it.  An
@@ -909,6 +913,20 @@ def run_ours(args):
     graph_ms = timed_graph(step, args.steps, flush) if small else None
     fused_ms = timed_append(step, args.steps, args.warmup, flush)
     cascade_ms = timed_cascade(step, args.steps, args.warmup, flush) if step.has_groups else None
+    # a configuration that states its partition: the same step with the
+    # library's automatic choice beside it
+    auto = None
+    if partition:
+        astep = DecodeStep(case, dev, 0, wname)
+        if astep.P_eff != step.P_eff:
+            a_total, a_decode, _ = timed_decode(astep, args.steps, args.warmup, world, flush)
+            a_total, a_sum = aggregate(a_total, float(astep.kv_bytes) * args.steps, world)
+            auto = {"partition_size": astep.P_eff, "ms_per_step": round(a_total / args.steps, 5),
+                    "value": round(a_sum / (a_total / 1e3) / 1e9, 2), "unit": "GB/s",
+                    "kernel_achieved": round(unique_bytes_of(case) / (a_decode / 1e3) / 1e9, 1),
+                    "kernel_frac": round(unique_bytes_of(case) / (a_decode / 1e3) / 1e9 / measured_peaks()[0], 4),
+                    "note": "the same step with partition_size 0 (pa_decode_partition_size); not in value"}
+        del astep
     src_hash = kernel_source_hash()
     traffic = NCU_TRAFFIC.get((args.workload, src_hash))
     line = {
@@ -945,6 +963,7 @@ def run_ours(args):
                          "value": round(step.kv_bytes / (fused_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                          "note": "the same step (new token written, then attended) as one pa_decode_append launch; "
                                  "each step timed on its own"},
+        "auto_partition": auto,
         "cascade": None if cascade_ms is None else {
             "ms_per_step": round(cascade_ms, 5), "value": round(step.kv_bytes / (cascade_ms / 1e3) / 1e9, 2),
             "unit": "GB/s",

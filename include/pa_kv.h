@@ -148,9 +148,11 @@ pa_status pa_copy_blocks(const pa_kv_cache* cache, const int32_t* src_dst_pairs,
  *   reported and the sequence's output is 0.
  * partition_size: tokens per context partition (a multiple of block_size),
  *   0 = automatic (pa_decode_partition_size: 2048, or 1024 when num_heads /
- *   num_kv_heads >= 4, halved down to 512 while the (sequence, KV head,
- *   partition) work items would not fill the GPU twice over; the workspace
- *   size query answers for 512, which covers every automatic choice).  A
+ *   num_kv_heads >= 4; with fewer (sequence, KV head) pairs than resident
+ *   decode blocks, doubled up to 8192 while the work items of max_seq_len
+ *   still number four or more per block; then halved down to 512 while they
+ *   would not fill the GPU twice over; the workspace size query answers for
+ *   512, which covers every automatic choice).  A
  *   sequence longer than one partition is split; the
  *   partitions' partial results go to `workspace` and a second kernel merges
  *   them by their log-sum-exp.
