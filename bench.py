@@ -62,6 +62,10 @@ NCU_TRAFFIC = {
     ("gqa", "7cb5cae478ced3ab"): 939_895_040,
     ("long", "7cb5cae478ced3ab"): 1_748_656_896,
     ("mixed", "530d95a1f63ff18c"): 1_556_752_896,
+    ("mha", "982cdac6a2c10305"): 945_004_288,
+    ("gqa", "982cdac6a2c10305"): 939_515_904,
+    ("long", "982cdac6a2c10305"): 1_749_042_688,
+    ("mixed", "f803016c3ea7946c"): 1_545_752_320,
     ("mha", "6c3aaacd1f8b3e95"): 944_406_528,
     ("gqa", "6c3aaacd1f8b3e95"): 939_486_464,
     ("long", "6c3aaacd1f8b3e95"): 1_748_525_824,
