@@ -292,11 +292,11 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
  * decoding scenarios.  The pages give no kernel for it; this entry point
  * computes exactly what pa_decode computes (the same softmax(q K^T scale) V per
  * sequence and head, up to fp32 rounding order) but reads a group's shared
- * blocks once for all of its members: a prefix pass (the varlen tensor-core
- * kernel, no causal mask) attends every member's query to the shared tokens in
- * parts of the decode's partition length, a suffix pass (the decode kernel)
- * attends each member's own tokens, and the log-sum-exp merge of pa_decode
- * combines all parts.
+ * blocks once per 8 / (num_heads / num_kv_heads) members: a prefix pass (the
+ * decode kernel with those members' heads side by side as the eight query rows
+ * of one sequence) attends every member's query to the shared tokens in
+ * partitions, a suffix pass attends each member's own tokens, and the
+ * log-sum-exp merge of pa_decode combines all partitions.
  *
  * cu_groups: device int32 [num_groups+1], 0 = cu_groups[0] <= ... <=
  *   cu_groups[num_groups] = num_seqs; sequences cu_groups[g] .. cu_groups[g+1]-1
@@ -307,14 +307,14 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
  *   member's length).  The blocks are read through the group's first row; a
  *   member whose row differs there, or a shared length that breaks these rules,
  *   is reported as PA_ERR_INVALID_ARG in dev_status.
- * max_group_size: the largest group (host bound); at most 128 / (num_heads /
- *   num_kv_heads).  max_shared_len: host bound on shared_lens (a multiple of
- *   block_size, <= max_seq_len).
+ * max_group_size: the largest group (host bound, >= 1).  max_shared_len: host
+ *   bound on shared_lens (a multiple of block_size, <= max_seq_len).
  * workspace: pa_decode_cascade_workspace_size(...) bytes, 16-byte aligned (never
  *   0: every (sequence, head) keeps a prefix and a suffix partial).
- * Supported: fp16/bf16 caches with q of the same type, head_size 128, block
- *   sizes 16/32/64, num_heads / num_kv_heads in {1, 2, 4, 8}; other shapes return
- *   PA_ERR_UNSUPPORTED with nothing launched.  Everything else as pa_decode.
+ * Supported: the shapes and types of pa_decode (fp16/bf16 caches with q of the
+ *   same type, or E4M3 caches; head_size 64 or 128; block sizes 16/32/64;
+ *   num_heads / num_kv_heads in {1, 2, 4, 8}); others return PA_ERR_UNSUPPORTED
+ *   with nothing launched.  Everything else as pa_decode.
  * ------------------------------------------------------------------------- */
 size_t pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,
                                         int32_t max_seq_len, int32_t block_size, int32_t partition_size);

@@ -78,7 +78,8 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
                        int32_t partition_size, void* workspace, size_t workspace_bytes, int32_t* dev_status,
                        pa_stream_t stream, const void* k_new, const void* v_new,
                        const int32_t* cu_seq_lens_k = nullptr, const int32_t* cu_groups = nullptr,
-                       const int32_t* shared_lens = nullptr, int32_t num_groups = 0) {
+                       const int32_t* shared_lens = nullptr, int32_t num_groups = 0, bool group_mode = false,
+                       int32_t max_group_size = 0) {
     pa_status st = check_cache(cache);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
@@ -110,6 +111,12 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
     if (cu_groups != nullptr && (shared_lens == nullptr || num_groups <= 0 || k_new != nullptr))
         return PA_ERR_INVALID_ARG;
+    // group mode (the cascade's prefix pass): 8 / group members per launched
+    // sequence fill the eight query rows of the G = 8 kernel
+    const int vm = group_mode ? 8 / group : 0;
+    const int64_t vpg = group_mode ? (max_group_size + vm - 1) / vm : 0;
+    if (group_mode && (cu_groups == nullptr || max_group_size < 1)) return PA_ERR_INVALID_ARG;
+    if (group_mode && num_groups * vpg > 16384) return PA_ERR_UNSUPPORTED;
     // cascade: the prefix's parts (ceil(s0/P)) and the suffix's (parts_of(L-s0))
     // never exceed parts_of(L) + 1
     const int max_parts = max_parts_of(max_seq_len, P) + (cu_groups != nullptr ? 1 : 0);
@@ -148,11 +155,20 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     p.cu_groups = cu_groups;
     p.shared_lens = shared_lens;
     p.num_groups = num_groups;
+    p.num_members = num_seqs;
+    int kgroup = group;
+    if (group_mode) {
+        p.vm = vm;
+        p.vpg = static_cast<int32_t>(vpg);
+        p.g_real = group;
+        p.num_seqs = static_cast<int32_t>(num_groups * vpg);
+        kgroup = 8;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 #define PA_BS(KV)                                                       \
-    if (bs == 16) return launch_decode_##KV##_bs16(p, q_dtype, D, group, s); \
-    if (bs == 32) return launch_decode_##KV##_bs32(p, q_dtype, D, group, s); \
-    return launch_decode_##KV##_bs64(p, q_dtype, D, group, s);
+    if (bs == 16) return launch_decode_##KV##_bs16(p, q_dtype, D, kgroup, s); \
+    if (bs == 32) return launch_decode_##KV##_bs32(p, q_dtype, D, kgroup, s); \
+    return launch_decode_##KV##_bs64(p, q_dtype, D, kgroup, s);
     if (cache->kv_dtype == PA_F16) { PA_BS(f16) }
     if (cache->kv_dtype == PA_BF16) { PA_BS(bf16) }
     PA_BS(fp8)
@@ -224,12 +240,8 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, pa_dtype q_dtyp
     if (num_heads % cache->num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     const int group = num_heads / cache->num_kv_heads;
     const int bs = cache->block_size;
-    // the prefix pass runs on the varlen tensor-core kernel: 16-bit caches of
-    // head size 128, a group's members within one 128-row tile
-    if (cache->head_size != 128 || (q_dtype != PA_F16 && q_dtype != PA_BF16) || cache->kv_dtype != q_dtype)
-        return PA_ERR_UNSUPPORTED;
     if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
-    if (max_group_size < 1 || max_group_size > 128 / group) return PA_ERR_UNSUPPORTED;
+    if (max_group_size < 1) return PA_ERR_INVALID_ARG;
     if (max_shared_len < 0 || max_shared_len > max_seq_len || max_shared_len % bs != 0) return PA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 15u)) return PA_ERR_INVALID_ARG;
     const int P = resolve_partition(partition_size, num_seqs, cache->num_kv_heads, max_seq_len, group);
@@ -237,17 +249,18 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, pa_dtype q_dtyp
     const int max_parts = max_parts_of(max_seq_len, P) + 1;
     const WsLayout w = ws_layout(num_seqs, num_heads, cache->head_size, max_parts);
     if (workspace_bytes < w.bytes) return PA_ERR_INVALID_ARG;
-    float* ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.lse_off);
-    float* ws_o = reinterpret_cast<float*>(static_cast<char*>(workspace) + w.o_off);
-    // 1) shared prefixes, once per group; 2) every member's own suffix; 3) the
-    //    log-sum-exp merge of both (launched by the decode entry)
-    st = cascade_prefix_partials(q, q_dtype, cache, block_table, max_blocks_per_seq, cu_groups, shared_lens,
-                                 num_groups, max_group_size, max_shared_len, P, num_heads, scale, ws_o, ws_lse,
-                                 max_parts, dev_status, stream);
+    // 1) shared prefixes: the decode kernel in group mode, a group's members
+    //    side by side as the query rows of one sequence, each group's shared
+    //    blocks read once per 8 / group members, partials into parts
+    //    0 .. ceil(s0/P)-1; 2) every member's own tokens, partials after those,
+    //    and the log-sum-exp merge of all parts
+    st = decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                      num_heads, scale, P, workspace, workspace_bytes, dev_status, stream, nullptr, nullptr,
+                      nullptr, cu_groups, shared_lens, num_groups, true, max_group_size);
     if (st != PA_OK) return st;
     return decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
-                        num_heads, scale, partition_size, workspace, workspace_bytes, dev_status, stream, nullptr,
-                        nullptr, nullptr, cu_groups, shared_lens, num_groups);
+                        num_heads, scale, P, workspace, workspace_bytes, dev_status, stream, nullptr, nullptr,
+                        nullptr, cu_groups, shared_lens, num_groups);
 }
 
 extern "C" size_t pa_varlen_mixed_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,

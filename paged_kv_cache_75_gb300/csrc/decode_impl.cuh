@@ -71,6 +71,18 @@ struct DecodeParams {
     const int32_t* cu_groups;
     const int32_t* shared_lens;
     int32_t num_groups;
+    // cascade prefix pass ("group mode", vm > 0): sequence b of the launch is
+    // the members cu_groups[g] + j*vm .. + vm-1 (those that exist) of group
+    // g = b / vpg, j = b % vpg; the kernel's G = vm * g_real query rows of a
+    // KV head are those members' g_real heads, member after member; the
+    // sequence is the group's first shared_lens[g] tokens read through the
+    // group's first member's table row; every partial goes to the members'
+    // workspace slots from part 0 on (no output, no merge launch).
+    // num_members: the batch's real sequence count.
+    int32_t vm;
+    int32_t vpg;
+    int32_t g_real;
+    int32_t num_members;
 };
 
 template <int QDT, int KVDT, int D, int G, int BS>
@@ -169,11 +181,25 @@ __device__ __forceinline__ int group_of(const DecodeParams& p, int b) {
     return lo;
 }
 
+// Group mode: the group of sequence b and the members it stands for
+// (m0 .. m0+nm-1; nm = 0 past the group's end or for a malformed cu_groups).
+struct VSeq {
+    int g, m0, nm;
+};
+__device__ __forceinline__ VSeq vseq(const DecodeParams& p, int b) {
+    VSeq v;
+    v.g = b / p.vpg;
+    const int c0 = __ldg(p.cu_groups + v.g), c1 = min(__ldg(p.cu_groups + v.g + 1), p.num_members);
+    v.m0 = c0 + (b - v.g * p.vpg) * p.vm;
+    v.nm = c0 < 0 ? 0 : max(0, min(p.vm, c1 - v.m0));
+    return v;
+}
+
 // First token of sequence b (length L) this launch attends: its group's shared
 // length in a cascade suffix pass, else 0.  A shared length that is negative,
 // past L or not a whole number of blocks is reported and taken as 0.
 __device__ __forceinline__ int seq_start(const DecodeParams& p, int b, int L) {
-    if (p.cu_groups == nullptr) return 0;
+    if (p.cu_groups == nullptr || p.vm > 0) return 0;
     const int s0 = __ldg(p.shared_lens + group_of(p, b));
     if (s0 < 0 || s0 > L || s0 % p.block_size != 0) {
         report(p.status, PA_ERR_INVALID_ARG);
@@ -184,6 +210,16 @@ __device__ __forceinline__ int seq_start(const DecodeParams& p, int b, int L) {
 
 // A length is usable iff 0 <= L <= max_seq_len and L fits the table row.
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
+    if (p.vm > 0) {
+        // group mode: the group's shared blocks, for a sequence with members
+        const VSeq v = vseq(p, b);
+        if (v.nm == 0) return 0;
+        const int s0 = __ldg(p.shared_lens + v.g);
+        if (s0 < 0 || s0 > p.max_seq_len || s0 % p.block_size != 0 ||
+            static_cast<int64_t>(s0) > static_cast<int64_t>(p.max_blocks) * p.block_size)
+            return -1;
+        return s0;
+    }
     // lengths from seq_lens, or as differences of cumulative key lengths
     int L = p.cu_seq_lens_k != nullptr ? __ldg(p.cu_seq_lens_k + b + 1) - __ldg(p.cu_seq_lens_k + b)
                                        : __ldg(p.seq_lens + b);
@@ -441,6 +477,9 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
         const int tid = threadIdx.x;  // 0 .. NCW*32-1
         const bool direct = it.nparts == 1 && p.cu_groups == nullptr;
         const int part = it.part + prefix_parts(p, it.s0);  // cascade: after the prefix's parts
+        // group mode: query row g is head g % g_real of member m0 + g / g_real
+        VSeq v{0, it.b, 0};
+        if (p.vm > 0) v = vseq(p, it.b);
         for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
             const int g = (2 * e) / D, d = (2 * e) % D;
             const int ghg = g / C::GW, gw = g % C::GW;
@@ -461,8 +500,14 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
                 o0 *= inv;
                 o1 *= inv;
             }
-            const int h = it.kvh * G + g;
-            const int64_t bh = static_cast<int64_t>(it.b) * p.num_heads + h;
+            int h = it.kvh * G + g;
+            int64_t bh = static_cast<int64_t>(it.b) * p.num_heads + h;
+            if (p.vm > 0) {
+                const int mi = g / p.g_real;
+                if (mi >= v.nm) continue;
+                h = it.kvh * p.g_real + (g - mi * p.g_real);
+                bh = static_cast<int64_t>(v.m0 + mi) * p.num_heads + h;
+            }
             if (direct) {
                 using T = typename dtype_traits<QDT>::storage;
                 T* out = static_cast<T*>(p.out) + bh * D + d;
@@ -955,7 +1000,21 @@ paged_decode_kernel(const DecodeParams p) {
             if (lane == 0) {
                 const uint32_t slot = qn & 1u;
                 if (qn >= 2) ok = mbar_wait(qempty0 + 8u * slot, ((qn >> 1) - 1) & 1u, p.status, abort_flag);
-                if (ok) {
+                if (ok && p.vm > 0) {
+                    // group mode: each member's g_real heads, zeros for absent members
+                    const VSeq v = vseq(p, it.b);
+                    const uint32_t mb = static_cast<uint32_t>(p.g_real) * D * C::QB;
+                    uint8_t* dst = qbuf + slot * QSLOT;
+                    for (uint32_t o = static_cast<uint32_t>(v.nm) * mb; o < C::QBYTES; o += 16)
+                        *reinterpret_cast<uint4*>(dst + o) = make_uint4(0u, 0u, 0u, 0u);
+                    mbar_expect_tx(qfull0 + 8u * slot, static_cast<uint32_t>(v.nm) * mb);
+                    for (int mi = 0; mi < v.nm; ++mi) {
+                        const uint8_t* src =
+                            static_cast<const uint8_t*>(p.q) +
+                            (static_cast<int64_t>(v.m0 + mi) * p.num_heads + it.kvh * p.g_real) * D * C::QB;
+                        bulk_g2s(smem_addr(dst + mi * mb), src, mb, qfull0 + 8u * slot);
+                    }
+                } else if (ok) {
                     const uint8_t* src = static_cast<const uint8_t*>(p.q) +
                                          (static_cast<int64_t>(it.b) * p.num_heads + it.kvh * G) * D * C::QB;
                     mbar_expect_tx(qfull0 + 8u * slot, C::QBYTES);
@@ -969,7 +1028,9 @@ paged_decode_kernel(const DecodeParams p) {
             if constexpr (APPEND) {
                 if (it.L > 0 && it.t1 == it.L) xnew = append_prefetch<C, QDT>(p, it, lane);
             }
-            const int32_t* row = p.block_table + static_cast<int64_t>(it.b) * p.max_blocks;
+            // (group mode: the group's first member's row)
+            const int trow = p.vm > 0 ? __ldg(p.cu_groups + it.b / p.vpg) : it.b;
+            const int32_t* row = p.block_table + static_cast<int64_t>(trow) * p.max_blocks;
             // cascade: the prefix pass read the shared blocks through the group's
             // first row; a member whose row names other blocks there is reported
             if (p.cu_groups != nullptr && it.part == 0 && it.kvh == 0 && it.s0 > 0) {

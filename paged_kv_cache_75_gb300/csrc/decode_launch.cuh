@@ -43,7 +43,7 @@ pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);
     if (grid <= 0) return PA_OK;
     if (launch_pdl(kern, grid, C::THREADS, smem, stream, p) != cudaSuccess) return PA_ERR_CUDA;
-    if (p.max_parts > 1) {
+    if (p.max_parts > 1 && p.vm == 0) {  // (group mode leaves its partials to a later merge)
         // warps per (sequence, head): more when pairs have many partitions
         const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_heads;
         const int wpp = p.max_parts >= 32 ? 8 : p.max_parts >= 8 ? 4 : p.max_parts >= 3 ? 2 : 1;

@@ -61,17 +61,6 @@ int blocks_per_sm(Kernel kern, int threads, int smem, LaunchCache& c) {
     return n;
 }
 
-// Prefix pass of pa_decode_cascade (prefill.cu): every group's members against
-// the group's shared prefix keys in parts of part_len keys, part j written as
-// fp32 partials and log-sum-exp into part j of the decode workspace
-// (ws_o [rows][ws_parts][128], ws_lse [rows][ws_parts], rows = (sequence,
-// head)); a group with shared length s0 fills parts 0 .. ceil(s0/part_len)-1.
-pa_status cascade_prefix_partials(const void* q, pa_dtype dtype, const pa_kv_cache* cache,
-                                  const int32_t* block_table, int32_t max_blocks, const int32_t* cu_groups,
-                                  const int32_t* shared_lens, int32_t num_groups, int32_t max_group_size,
-                                  int32_t max_shared_len, int32_t part_len, int32_t num_heads, float scale,
-                                  float* ws_o, float* ws_lse, int32_t ws_parts, int32_t* dev_status,
-                                  pa_stream_t stream);
 
 // Launch with programmatic stream serialization: the kernel's blocks may be
 // scheduled while the previous kernel on the stream drains, which hides the

@@ -90,20 +90,6 @@ struct PrefillParams {
     float scale_log2;  // scale * log2(e)
     int64_t total_k;   // packed K/V: rows of K and V (Σ key lengths); -1 for the paged cache
     int32_t order_cap; // query tiles the shared-memory work order holds (set by the launch)
-    // Shared-prefix pass of the cascade decode: group g's shared keys
-    // [0, k_lens[g]) are cut into parts of kpart_len keys, and sequence
-    // b = g*kparts + j of the launch is part j of group g: the group's query
-    // rows cu_q[g] .. cu_q[g+1]-1 (none once j*kpart_len reaches k_lens[g])
-    // against keys [j*kpart_len, ...) read through block-table row cu_q[g] (the
-    // first member's row); every query row writes its fp32 O / l and
-    // log-sum-exp (log2 units) into part j of its decode workspace slot
-    // (query row, head) instead of `out`.  cu_k is unused.
-    const int32_t* k_lens;
-    float* ws_o;
-    float* ws_lse;
-    int32_t ws_parts;
-    int32_t kparts;     // key parts per group (cascade)
-    int32_t kpart_len;  // keys per part, a multiple of block_size (cascade)
 };
 
 // ---------------------------------------------------------------------------
@@ -292,16 +278,6 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 // lengths of sequence b; false if they break the stated bounds
 __device__ __forceinline__ bool seq_lens_ok(const PrefillParams& p, int b, int& lq, int& lk) {
-    if (p.k_lens != nullptr) {
-        // cascade prefix pass: key part j of group g
-        const int g = b / p.kparts, j = b - g * p.kparts;
-        const int s0 = __ldg(p.k_lens + g), k_off = j * p.kpart_len;
-        lk = min(max(s0 - k_off, 0), p.kpart_len);
-        lq = k_off < s0 ? __ldg(p.cu_q + g + 1) - __ldg(p.cu_q + g) : 0;
-        return s0 >= 0 && static_cast<int64_t>(s0) <= static_cast<int64_t>(p.kparts) * p.kpart_len &&
-               static_cast<int64_t>(s0) <= static_cast<int64_t>(p.max_blocks) * p.block_size && lq >= 0 &&
-               lq <= p.max_q;
-    }
     const int q0 = __ldg(p.cu_q + b), q1 = __ldg(p.cu_q + b + 1);
     const int k0 = __ldg(p.cu_k + b);
     const int k1 = __ldg(p.cu_k + b + 1);
@@ -570,15 +546,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
             for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
                 const Work w = work_item(p, prefix, order, item);
-                // (cascade: the group's first member's row, from the part's first page)
-                int64_t trow = w.b;
-                int page0 = 0;
-                if (p.k_lens != nullptr) {
-                    const int g = w.b / p.kparts;
-                    trow = __ldg(p.cu_q + g);
-                    page0 = (w.b - g * p.kparts) * (p.kpart_len / p.block_size);
-                }
-                const int32_t* bt_row = p.block_table + trow * p.max_blocks + page0;
+                const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
                 // page ids come in batches of 32 (one per lane, -1: past Lk, -2:
                 // bad id), so the table's latency is paid once per batch
                 const int pages = (w.ntiles * kBN + p.block_size - 1) / p.block_size;
@@ -766,25 +734,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const int qi = w.i0 + t_row;  // query index of this row in its sequence
             const bool row_valid = qi < w.lq;
             const int lim = p.causal ? min(w.lk, shift + qi + 1) : w.lk;  // keys [0, lim) visible
-            // this row's (query row, head); its place in q / out and (cascade
-            // prefix pass) its workspace slot follow from these two
-            const int qrow = __ldg(p.cu_q + (p.k_lens != nullptr ? w.b / p.kparts : w.b)) + qi;
+            // this row's (query row, head): its place in q and out
+            const int qrow = __ldg(p.cu_q + w.b) + qi;
             const int head = w.kvh * p.group + g_row;
             const int64_t row_off = (static_cast<int64_t>(qrow) * p.num_heads + head) * kD;
             uint16_t* dst = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
-            const int64_t ws_slot = (static_cast<int64_t>(qrow) * p.num_heads + head) * p.ws_parts +
-                                    (p.k_lens != nullptr ? w.b % p.kparts : 0);
             if (w.ntiles == 0) {
                 // no visible key for any row of the item: output 0
                 if (row_valid) {
-                    if (p.ws_o != nullptr) {
-                        float4* wo = reinterpret_cast<float4*>(p.ws_o + ws_slot * kD + 64 * x);
-                        for (int c = 0; c < 16; ++c) wo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (x == 0) p.ws_lse[ws_slot] = -INFINITY;
-                    } else {
-                        for (int c = 0; c < 64; c += 8)
-                            *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    for (int c = 0; c < 64; c += 8)
+                        *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 continue;
             }
@@ -996,23 +955,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 tc_fence_after();
                 const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
                 const float inv = L > 0.f ? 1.f / L : 0.f;
-                const int64_t ws_e = (static_cast<int64_t>(qrow) * p.num_heads + head) * p.ws_parts +
-                                     (p.k_lens != nullptr ? w.b % p.kparts : 0);
                 uint16_t* dst_e = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_heads + head) * kD +
                                   64 * x;
-                if (p.ws_o != nullptr && row_valid && x == 0)
-                    p.ws_lse[ws_e] = L > 0.f ? m + __log2f(L) : -INFINITY;
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     float o[32];
                     tmem_ld32(tmem_o + c0, o);
-                    if (row_valid && p.ws_o != nullptr) {
-                        float4* wo = reinterpret_cast<float4*>(p.ws_o + ws_e * kD + 64 * x + c0);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            wo[j] = make_float4(o[4 * j] * inv, o[4 * j + 1] * inv, o[4 * j + 2] * inv,
-                                                o[4 * j + 3] * inv);
-                    } else if (row_valid) {
+                    if (row_valid) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             uint4 q4;
@@ -1178,65 +1127,6 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
         return PA_ERR_CUDA;
     return launch_prefill<false>(p, q_dtype, map_k, map_v, stream);
 }
-
-namespace pa {
-
-// Prefix pass of pa_decode_cascade: group g's members (decode rows
-// cu_groups[g] .. cu_groups[g+1]-1, consecutive in q) attend the group's first
-// shared_lens[g] keys, read through the first member's block-table row, without
-// a causal mask (every member's query comes after the shared prompt).  The
-// shared keys are cut into parts of part_len keys (the decode's partition), so
-// a long prompt spreads over as many work items; part j of a (member, head)
-// row goes to part j of its decode workspace slot as fp32 O / l and its
-// log-sum-exp.  The caller (pa_decode_cascade) has checked the cache, the types
-// (16-bit, q and cache alike), head size 128, the group size bound and that
-// part_len is a positive multiple of the block size.
-pa_status cascade_prefix_partials(const void* q, pa_dtype dtype, const pa_kv_cache* cache,
-                                  const int32_t* block_table, int32_t max_blocks, const int32_t* cu_groups,
-                                  const int32_t* shared_lens, int32_t num_groups, int32_t max_group_size,
-                                  int32_t max_shared_len, int32_t part_len, int32_t num_heads, float scale,
-                                  float* ws_o, float* ws_lse, int32_t ws_parts, int32_t* dev_status,
-                                  pa_stream_t stream) {
-    if (part_len <= 0) return PA_ERR_INVALID_ARG;
-    const int kparts = max_shared_len > part_len ? (max_shared_len + part_len - 1) / part_len : 1;
-    if (static_cast<int64_t>(num_groups) * kparts > kMaxSeqs) return PA_ERR_UNSUPPORTED;
-    const int bs = cache->block_size;
-    const int64_t rows = cache->num_blocks * cache->num_kv_heads * bs;
-    if (rows > INT32_MAX) return PA_ERR_UNSUPPORTED;
-    PrefillParams p{};
-    p.out = nullptr;
-    p.q = static_cast<const uint16_t*>(q);
-    p.block_table = block_table;
-    p.cu_q = cu_groups;
-    p.cu_k = nullptr;
-    p.k_lens = shared_lens;
-    p.status = dev_status;
-    p.num_blocks = cache->num_blocks;
-    p.block_size = bs;
-    p.num_kv_heads = cache->num_kv_heads;
-    p.num_heads = num_heads;
-    p.group = num_heads / cache->num_kv_heads;
-    p.tq = kRows / p.group;
-    p.num_seqs = num_groups * kparts;
-    p.max_blocks = max_blocks;
-    p.max_q = max_group_size;
-    p.max_k = max_shared_len < part_len ? max_shared_len : part_len;
-    p.causal = 0;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.total_k = -1;
-    p.ws_o = ws_o;
-    p.ws_lse = ws_lse;
-    p.ws_parts = ws_parts;
-    p.kparts = kparts;
-    p.kpart_len = part_len;
-    CUtensorMap map_k, map_v;
-    if (!make_cache_map(&map_k, cache->k_cache, rows, dtype, bs) ||
-        !make_cache_map(&map_v, cache->v_cache, rows, dtype, bs))
-        return PA_ERR_CUDA;
-    return launch_prefill<false>(p, dtype, map_k, map_v, stream);
-}
-
-}  // namespace pa
 
 extern "C" pa_status pa_prefill_varlen_packed(void* out, const void* q, const void* k, const void* v,
                                               pa_dtype dtype, const int32_t* cu_seq_lens_q,

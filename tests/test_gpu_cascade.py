@@ -128,19 +128,33 @@ def test_shared_length_off_a_block_boundary_is_reported():
 
 
 @pytest.mark.parametrize("kind", ["e4m3", "d64", "big_group"])
-def test_unsupported_shapes_launch_nothing(kind):
+def test_cascade_other_shapes(kind):
+    # E4M3 cache (bf16 queries), head size 64, and a group of 40 members
     D = 64 if kind == "d64" else 128
     kd = W.E4M3 if kind == "e4m3" else W.F16
     qd = W.BF16 if kind == "e4m3" else W.F16
-    case = W.make_decode_case(3, [40, 40], 8, 2, D, 16, 10, qd, kd)
+    sizes, shared = ([40], [3]) if kind == "big_group" else ([3, 2], [4, 1])
+    extras = list(range(5, 5 + 7 * sum(sizes), 7))
+    case, cu, sl = group_case(13, sizes, shared, extras, 8, 2, 16, qd, D=D)
+    if kd == W.E4M3:
+        case.k_cache = W.random_values(torch.Generator().manual_seed(1), case.k_cache.shape, W.E4M3)
+        case.v_cache = W.random_values(torch.Generator().manual_seed(2), case.v_cache.shape, W.E4M3)
+        case.kv_dtype = W.E4M3
+    out, st = run_cascade(case, cu, sl)
+    assert st == 0
+    assert_close(out, oracle_ref(case), qd, kd, "cascade " + kind)
+
+
+def test_unsupported_group_launches_nothing():
+    # 16 query heads per KV head: no decode kernel for it
+    case = W.make_decode_case(3, [40, 40], 16, 1, 128, 16, 10, W.F16, W.F16)
     cu = np.array([0, 2], np.int32)
     sl = np.array([32], np.int32)
     q = case.q.to(DEV)
     out = torch.empty_like(q)
-    ws = torch.empty(pk.pa_decode_cascade_workspace_size(2, 8, D, 40, 16), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(pk.pa_decode_cascade_workspace_size(2, 16, 128, 40, 16), dtype=torch.uint8, device=DEV)
     cache = pk.KVCache(case.k_cache.to(DEV), case.v_cache.to(DEV), case.k_scale, case.v_scale)
-    max_group = 64 if kind == "big_group" else 2  # G = 4: at most 32 members
     with pytest.raises(pk.PaError) as e:
         pk.pa_decode_cascade(out, q, cache, case.block_table.to(DEV), case.seq_lens.to(DEV), 40, case.scale,
-                             torch.as_tensor(cu).to(DEV), torch.as_tensor(sl).to(DEV), max_group, 32, ws)
+                             torch.as_tensor(cu).to(DEV), torch.as_tensor(sl).to(DEV), 2, 32, ws)
     assert e.value.status == 2  # PA_ERR_UNSUPPORTED
