@@ -62,6 +62,10 @@ NCU_TRAFFIC = {
     ("gqa", "7cb5cae478ced3ab"): 939_895_040,
     ("long", "7cb5cae478ced3ab"): 1_748_656_896,
     ("mixed", "530d95a1f63ff18c"): 1_556_752_896,
+    ("mha", "4facb81714f61645"): 944_771_072,
+    ("gqa", "4facb81714f61645"): 939_407_360,
+    ("long", "4facb81714f61645"): 1_748_968_448,
+    ("mixed", "a2e53b228aac2fea"): 1_554_160_640,
     ("mha", "982cdac6a2c10305"): 945_004_288,
     ("gqa", "982cdac6a2c10305"): 939_515_904,
     ("long", "982cdac6a2c10305"): 1_749_042_688,
