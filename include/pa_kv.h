@@ -292,11 +292,11 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
  * decoding scenarios.  The pages give no kernel for it; this entry point
  * computes exactly what pa_decode computes (the same softmax(q K^T scale) V per
  * sequence and head, up to fp32 rounding order) but reads a group's shared
- * blocks once per 8 / (num_heads / num_kv_heads) members: a prefix pass (the
- * decode kernel with those members' heads side by side as the eight query rows
- * of one sequence) attends every member's query to the shared tokens in
- * partitions, a suffix pass attends each member's own tokens, and the
- * log-sum-exp merge of pa_decode combines all partitions.
+ * blocks once per 8 / (num_heads / num_kv_heads) members: one decode launch
+ * attends every member's query to the shared tokens (those members' heads side
+ * by side as the eight query rows of one sequence) and each member's own
+ * tokens, all in partitions of one work list, and the log-sum-exp merge of
+ * pa_decode combines all partitions.
  *
  * cu_groups: device int32 [num_groups+1], 0 = cu_groups[0] <= ... <=
  *   cu_groups[num_groups] = num_seqs; sequences cu_groups[g] .. cu_groups[g+1]-1

@@ -111,12 +111,13 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     if (num_seqs > 16384) return PA_ERR_UNSUPPORTED;
     if (cu_groups != nullptr && (shared_lens == nullptr || num_groups <= 0 || k_new != nullptr))
         return PA_ERR_INVALID_ARG;
-    // group mode (the cascade's prefix pass): 8 / group members per launched
-    // sequence fill the eight query rows of the G = 8 kernel
+    // group mode (the cascade in one launch): 8 / group members per launched
+    // sequence fill the eight query rows of the G = 8 kernel over their group's
+    // shared tokens, then every member's own tokens as sequences of their own
     const int vm = group_mode ? 8 / group : 0;
     const int64_t vpg = group_mode ? (max_group_size + vm - 1) / vm : 0;
     if (group_mode && (cu_groups == nullptr || max_group_size < 1)) return PA_ERR_INVALID_ARG;
-    if (group_mode && num_groups * vpg > 16384) return PA_ERR_UNSUPPORTED;
+    if (group_mode && num_groups * vpg + num_seqs > 16384) return PA_ERR_UNSUPPORTED;
     // cascade: the prefix's parts (ceil(s0/P)) and the suffix's (parts_of(L-s0))
     // never exceed parts_of(L) + 1
     const int max_parts = max_parts_of(max_seq_len, P) + (cu_groups != nullptr ? 1 : 0);
@@ -160,8 +161,9 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     if (group_mode) {
         p.vm = vm;
         p.vpg = static_cast<int32_t>(vpg);
+        p.vcount = static_cast<int32_t>(num_groups * vpg);
         p.g_real = group;
-        p.num_seqs = static_cast<int32_t>(num_groups * vpg);
+        p.num_seqs = p.vcount + num_seqs;
         kgroup = 8;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -249,18 +251,14 @@ extern "C" pa_status pa_decode_cascade(void* out, const void* q, pa_dtype q_dtyp
     const int max_parts = max_parts_of(max_seq_len, P) + 1;
     const WsLayout w = ws_layout(num_seqs, num_heads, cache->head_size, max_parts);
     if (workspace_bytes < w.bytes) return PA_ERR_INVALID_ARG;
-    // 1) shared prefixes: the decode kernel in group mode, a group's members
-    //    side by side as the query rows of one sequence, each group's shared
-    //    blocks read once per 8 / group members, partials into parts
-    //    0 .. ceil(s0/P)-1; 2) every member's own tokens, partials after those,
-    //    and the log-sum-exp merge of all parts
-    st = decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
-                      num_heads, scale, P, workspace, workspace_bytes, dev_status, stream, nullptr, nullptr,
-                      nullptr, cu_groups, shared_lens, num_groups, true, max_group_size);
-    if (st != PA_OK) return st;
+    // One decode launch in group mode: a group's members side by side as the
+    // query rows of one sequence over the group's shared blocks (read once per
+    // 8 / group members, partials into parts 0 .. ceil(s0/P)-1) and every
+    // member's own tokens (partials after those) share one work list; then the
+    // log-sum-exp merge of all parts
     return decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                         num_heads, scale, P, workspace, workspace_bytes, dev_status, stream, nullptr, nullptr,
-                        nullptr, cu_groups, shared_lens, num_groups);
+                        nullptr, cu_groups, shared_lens, num_groups, true, max_group_size);
 }
 
 extern "C" size_t pa_varlen_mixed_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t head_size,

@@ -71,16 +71,19 @@ struct DecodeParams {
     const int32_t* cu_groups;
     const int32_t* shared_lens;
     int32_t num_groups;
-    // cascade prefix pass ("group mode", vm > 0): sequence b of the launch is
-    // the members cu_groups[g] + j*vm .. + vm-1 (those that exist) of group
-    // g = b / vpg, j = b % vpg; the kernel's G = vm * g_real query rows of a
-    // KV head are those members' g_real heads, member after member; the
-    // sequence is the group's first shared_lens[g] tokens read through the
-    // group's first member's table row; every partial goes to the members'
-    // workspace slots from part 0 on (no output, no merge launch).
+    // cascade decode in one launch ("group mode", vm > 0).  Sequence b <
+    // vcount of the launch is the members cu_groups[g] + j*vm .. + vm-1 (those
+    // that exist) of group g = b / vpg, j = b % vpg, over the group's first
+    // shared_lens[g] tokens read through the group's first member's table row:
+    // the kernel's G = vm * g_real query rows of a KV head are those members'
+    // g_real heads, member after member, and the partials go to the members'
+    // workspace parts 0 .. ceil(s0/partition)-1.  Sequence vcount + m is
+    // member m alone over its own tokens [s0, L) (query rows past g_real
+    // empty), partials after the prefix's.  A merge launch follows.
     // num_members: the batch's real sequence count.
     int32_t vm;
     int32_t vpg;
+    int32_t vcount;
     int32_t g_real;
     int32_t num_members;
 };
@@ -181,13 +184,22 @@ __device__ __forceinline__ int group_of(const DecodeParams& p, int b) {
     return lo;
 }
 
-// Group mode: the group of sequence b and the members it stands for
-// (m0 .. m0+nm-1; nm = 0 past the group's end or for a malformed cu_groups).
+// Group mode: the members sequence b stands for (m0 .. m0+nm-1; nm = 0 past
+// a group's end or for a malformed cu_groups) and whether it is a member's own
+// tokens (b >= vcount) rather than its group's shared ones.
 struct VSeq {
     int g, m0, nm;
+    bool own;
 };
 __device__ __forceinline__ VSeq vseq(const DecodeParams& p, int b) {
     VSeq v;
+    v.own = b >= p.vcount;
+    if (v.own) {
+        v.g = 0;  // (not needed by the callers)
+        v.m0 = b - p.vcount;
+        v.nm = 1;
+        return v;
+    }
     v.g = b / p.vpg;
     const int c0 = __ldg(p.cu_groups + v.g), c1 = min(__ldg(p.cu_groups + v.g + 1), p.num_members);
     v.m0 = c0 + (b - v.g * p.vpg) * p.vm;
@@ -199,7 +211,11 @@ __device__ __forceinline__ VSeq vseq(const DecodeParams& p, int b) {
 // length in a cascade suffix pass, else 0.  A shared length that is negative,
 // past L or not a whole number of blocks is reported and taken as 0.
 __device__ __forceinline__ int seq_start(const DecodeParams& p, int b, int L) {
-    if (p.cu_groups == nullptr || p.vm > 0) return 0;
+    if (p.cu_groups == nullptr) return 0;
+    if (p.vm > 0) {
+        if (b < p.vcount) return 0;  // group mode: a group's shared tokens
+        b -= p.vcount;               // a member's own tokens
+    }
     const int s0 = __ldg(p.shared_lens + group_of(p, b));
     if (s0 < 0 || s0 > L || s0 % p.block_size != 0) {
         report(p.status, PA_ERR_INVALID_ARG);
@@ -210,7 +226,8 @@ __device__ __forceinline__ int seq_start(const DecodeParams& p, int b, int L) {
 
 // A length is usable iff 0 <= L <= max_seq_len and L fits the table row.
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int b) {
-    if (p.vm > 0) {
+    if (p.vm > 0 && b >= p.vcount) b -= p.vcount;  // group mode: a member's own tokens
+    else if (p.vm > 0) {
         // group mode: the group's shared blocks, for a sequence with members
         const VSeq v = vseq(p, b);
         if (v.nm == 0) return 0;
@@ -478,8 +495,13 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
         const bool direct = it.nparts == 1 && p.cu_groups == nullptr;
         const int part = it.part + prefix_parts(p, it.s0);  // cascade: after the prefix's parts
         // group mode: query row g is head g % g_real of member m0 + g / g_real
-        VSeq v{0, it.b, 0};
-        if (p.vm > 0) v = vseq(p, it.b);
+        VSeq v{0, it.b, 0, false};
+        if (p.vm > 0) {
+            v = vseq(p, it.b);
+            // a group without shared tokens leaves its members' parts to
+            // their own sequences (the same parts, written in this launch)
+            if (!v.own && it.L == 0) v.nm = 0;
+        }
         for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
             const int g = (2 * e) / D, d = (2 * e) % D;
             const int ghg = g / C::GW, gw = g % C::GW;
@@ -1028,14 +1050,15 @@ paged_decode_kernel(const DecodeParams p) {
             if constexpr (APPEND) {
                 if (it.L > 0 && it.t1 == it.L) xnew = append_prefetch<C, QDT>(p, it, lane);
             }
-            // (group mode: the group's first member's row)
-            const int trow = p.vm > 0 ? __ldg(p.cu_groups + it.b / p.vpg) : it.b;
+            // (group mode: the group's first member's row, or the member's own)
+            const int member = p.vm > 0 && it.b >= p.vcount ? it.b - p.vcount : it.b;
+            const int trow = p.vm > 0 && it.b < p.vcount ? __ldg(p.cu_groups + it.b / p.vpg) : member;
             const int32_t* row = p.block_table + static_cast<int64_t>(trow) * p.max_blocks;
             // cascade: the prefix pass read the shared blocks through the group's
             // first row; a member whose row names other blocks there is reported
             if (p.cu_groups != nullptr && it.part == 0 && it.kvh == 0 && it.s0 > 0) {
-                const int b0 = __ldg(p.cu_groups + group_of(p, it.b));
-                if (b0 != it.b) {
+                const int b0 = __ldg(p.cu_groups + group_of(p, member));
+                if (b0 != member) {
                     const int32_t* row0 = p.block_table + static_cast<int64_t>(b0) * p.max_blocks;
                     bool bad = false;
                     for (int j = lane; j < it.s0 / BS; j += 32) bad |= __ldg(row0 + j) != __ldg(row + j);

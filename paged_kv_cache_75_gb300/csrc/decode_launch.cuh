@@ -43,16 +43,22 @@ pa_status launch_decode_t(DecodeParams p, cudaStream_t stream) {
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);
     if (grid <= 0) return PA_OK;
     if (launch_pdl(kern, grid, C::THREADS, smem, stream, p) != cudaSuccess) return PA_ERR_CUDA;
-    if (p.max_parts > 1 && p.vm == 0) {  // (group mode leaves its partials to a later merge)
+    if (p.max_parts > 1) {
+        // group mode: the merge runs over the batch's members
+        DecodeParams r = p;
+        if (r.vm > 0) {
+            r.vm = 0;
+            r.num_seqs = r.num_members;
+        }
         // warps per (sequence, head): more when pairs have many partitions
-        const int64_t pairs = static_cast<int64_t>(p.num_seqs) * p.num_heads;
+        const int64_t pairs = static_cast<int64_t>(r.num_seqs) * r.num_heads;
         const int wpp = p.max_parts >= 32 ? 8 : p.max_parts >= 8 ? 4 : p.max_parts >= 3 ? 2 : 1;
         const int rgrid = static_cast<int>((pairs * wpp + 7) / 8);
         cudaError_t e;
-        if (wpp == 8) e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 8>, rgrid, 256, 0, stream, p);
-        else if (wpp == 4) e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 4>, rgrid, 256, 0, stream, p);
-        else if (wpp == 2) e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 2>, rgrid, 256, 0, stream, p);
-        else e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 1>, rgrid, 256, 0, stream, p);
+        if (wpp == 8) e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 8>, rgrid, 256, 0, stream, r);
+        else if (wpp == 4) e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 4>, rgrid, 256, 0, stream, r);
+        else if (wpp == 2) e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 2>, rgrid, 256, 0, stream, r);
+        else e = launch_pdl(paged_decode_reduce_kernel<QDT, D, 1>, rgrid, 256, 0, stream, r);
         if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     return PA_OK;
