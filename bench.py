@@ -62,6 +62,9 @@ NCU_TRAFFIC = {
     ("gqa", "7cb5cae478ced3ab"): 939_895_040,
     ("long", "7cb5cae478ced3ab"): 1_748_656_896,
     ("mixed", "530d95a1f63ff18c"): 1_556_752_896,
+    ("mha", "7779adaa5cbb9b71"): 944_760_064,
+    ("gqa", "7779adaa5cbb9b71"): 939_720_448,
+    ("long", "7779adaa5cbb9b71"): 1_749_494_528,
     ("mha", "4facb81714f61645"): 944_771_072,
     ("gqa", "4facb81714f61645"): 939_407_360,
     ("long", "4facb81714f61645"): 1_748_968_448,
