@@ -23,9 +23,14 @@
 //    mbarriers;
 //  * four consumer warps split each stage's tokens; all G query heads of a KV
 //    head are handled together, so a page is read once per KV head (GQA);
-//  * each 8-lane token group keeps its own online softmax in fp32 (exp2
-//    domain, lazy rescale), QK with warp-shuffle reductions, and groups and
-//    warps are merged once per work item;
+//  * with one or two query heads per KV head, each 8-lane token group keeps
+//    its own online softmax in fp32 (exp2 domain, lazy rescale), QK with
+//    warp-shuffle reductions; with four or eight, 16-token slices go through
+//    tensor-core MMAs (mma.sync, fp32 accumulate) with one softmax state per
+//    head; groups and warps are merged once per work item;
+//  * the shared-prefix (cascade) decode is this kernel in "group mode": a
+//    group's members side by side as one sequence's query rows over their
+//    shared blocks, beside every member's own tokens, in one work list;
 //  * every mbarrier wait is bounded (PA_ERR_TIMEOUT, no hang).
 #pragma once
 
