@@ -194,10 +194,26 @@ def test_full_gqa_shared_decode_sampled():
     _sampled_check(case, sample)
 
 
-def test_full_long_fp8_decode_sampled():
+@pytest.mark.parametrize("P", [512, 0])
+def test_full_long_fp8_decode_sampled(P):
+    # the stated 512-token partitions, and the automatic choice (4096 here)
     case = W.long_fp8_decode(device=DEV)
     lens = case.seq_lens.cpu().numpy()
-    _sampled_check(case, [int(np.argmax(lens))], P=512)
+    _sampled_check(case, [int(np.argmax(lens))], P=P)
+
+
+def test_automatic_partition_for_the_bench_shapes():
+    # few long sequences grow it, many sequences keep 2048 (1024 for four or
+    # more query heads per KV head), and it never goes below 512
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip("the expected values assume 152 SMs")
+    assert pk.pa_decode_partition_size(64, 32, 32, 2048) == 2048      # MHA
+    assert pk.pa_decode_partition_size(256, 32, 8, 8192) == 1024      # GQA
+    assert pk.pa_decode_partition_size(8, 64, 8, 131072) == 4096      # long context
+    assert pk.pa_decode_partition_size(3, 4, 4, 71) == 512            # tiny: shrunk to fill
+    assert pk.pa_decode_partition_size(1, 8, 8, 10 ** 6) == 4096      # 8 pairs x 245 parts at 4096
+    assert pk.pa_decode_partition_size(1, 8, 8, 2 * 10 ** 6) == 8192  # and 8 x 245 at 8192: the cap
 
 
 @pytest.mark.parametrize("G", [1, 4])
