@@ -150,7 +150,8 @@ pa_status pa_copy_blocks(const pa_kv_cache* cache, const int32_t* src_dst_pairs,
  *   0 = automatic (pa_decode_partition_size: 2048, or 1024 when num_heads /
  *   num_kv_heads >= 4; with fewer (sequence, KV head) pairs than resident
  *   decode blocks, doubled up to 8192 while the work items of max_seq_len
- *   still number four or more per block; then halved down to 512 while they
+ *   still number four or more per block; with more pairs and num_heads /
+ *   num_kv_heads >= 4, 1536; then halved, not below 512, while the items
  *   would not fill the GPU twice over; the workspace size query answers for
  *   512, which covers every automatic choice).  A
  *   sequence longer than one partition is split; the

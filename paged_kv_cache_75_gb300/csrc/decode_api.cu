@@ -21,11 +21,18 @@ int auto_partition(int64_t num_seqs, int num_kv_heads, int max_seq_len, int grou
     // faster while the items still give each resident block four or more (the
     // E4M3 decode of 8 sequences of 32k-128k tokens moved 0.77 of the copy rate
     // with 512-token partitions, 0.86 with 1024 and 0.92 with 4096).
-    if (pairs < ctas)
-        while (p < 8192 && items(2 * p) >= 4 * ctas) p <<= 1;
-    // Otherwise shorter ones while the items would not fill the GPU twice.
-    while (p > 512 && items(p) < 2 * ctas) p >>= 1;
-    return p;  // a power of two >= 512: a multiple of every block size
+    if (pairs < ctas) {
+        while (2 * p <= 8192 && items(2 * p) >= 4 * ctas) p <<= 1;
+    } else if (group >= 4) {
+        // many pairs through the tensor-core consumer: 1536 tokens (the GQA
+        // decode of 256 sequences, lengths log-normal around 1000, moved 0.71
+        // of the copy rate at 768, 0.74 at 1024, 0.75 at 1536, 0.74 at 2048)
+        p = 1536;
+    }
+    // Shorter ones while the items would not fill the GPU twice, never below
+    // 512 (the workspace size query answers for 512).
+    while (p / 2 >= 512 && items(p) < 2 * ctas) p >>= 1;
+    return p;  // 512 .. 8192, a multiple of every block size
 }
 
 int resolve_partition(int partition_size, int64_t num_seqs, int num_kv_heads, int max_seq_len, int group) {

@@ -203,13 +203,14 @@ def test_full_long_fp8_decode_sampled(P):
 
 
 def test_automatic_partition_for_the_bench_shapes():
-    # few long sequences grow it, many sequences keep 2048 (1024 for four or
+    # few long sequences grow it, many sequences keep 2048 (1536 for four or
     # more query heads per KV head), and it never goes below 512
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     if sms != 152:
         pytest.skip("the expected values assume 152 SMs")
     assert pk.pa_decode_partition_size(64, 32, 32, 2048) == 2048      # MHA
-    assert pk.pa_decode_partition_size(256, 32, 8, 8192) == 1024      # GQA
+    assert pk.pa_decode_partition_size(256, 32, 8, 8192) == 1536      # GQA
+    assert pk.pa_decode_partition_size(100, 32, 8, 700) == 768        # 800 pairs x 1 part: halved once
     assert pk.pa_decode_partition_size(8, 64, 8, 131072) == 4096      # long context
     assert pk.pa_decode_partition_size(3, 4, 4, 71) == 512            # tiny: shrunk to fill
     assert pk.pa_decode_partition_size(1, 8, 8, 10 ** 6) == 4096      # 8 pairs x 245 parts at 4096
