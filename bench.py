@@ -62,6 +62,9 @@ NCU_TRAFFIC = {
     ("gqa", "7cb5cae478ced3ab"): 939_895_040,
     ("long", "7cb5cae478ced3ab"): 1_748_656_896,
     ("mixed", "530d95a1f63ff18c"): 1_556_752_896,
+    ("mha", "a632445778d43fd8"): 944_534_528,
+    ("gqa", "a632445778d43fd8"): 939_881_984,
+    ("long", "a632445778d43fd8"): 1_749_401_856,
     ("mha", "6eae42cdb4f82c16"): 944_916_480,
     ("gqa", "6eae42cdb4f82c16"): 939_575_040,
     ("long", "6eae42cdb4f82c16"): 1_749_021_696,
