@@ -180,26 +180,24 @@ def _sampled_check(case, sample, P=0):
     assert_close(out[idx], ref, case.q_dtype, case.kv_dtype, "sampled")
 
 
-def test_full_mha_decode_sampled():
+def test_full_mha_decode_all_sequences():
+    # every one of the 64 sequences against the oracle
     case = W.mha_decode(device=DEV)
-    lens = case.seq_lens.cpu().numpy()
-    sample = [int(np.argmin(lens)), int(np.argmax(lens))] + list(range(0, 64, 9))
-    _sampled_check(case, sample)
+    _sampled_check(case, list(range(64)))
 
 
-def test_full_gqa_shared_decode_sampled():
+def test_full_gqa_shared_decode_all_sequences():
+    # every one of the 256 sequences (64 sampling groups of 4) against the oracle
     case = W.gqa_shared_decode(device=DEV)
-    lens = case.seq_lens.cpu().numpy()
-    sample = [int(np.argmax(lens)), int(np.argmin(lens))] + list(range(1, 256, 37))
-    _sampled_check(case, sample)
+    _sampled_check(case, list(range(256)))
 
 
 @pytest.mark.parametrize("P", [512, 0])
-def test_full_long_fp8_decode_sampled(P):
-    # the stated 512-token partitions, and the automatic choice (4096 here)
+def test_full_long_fp8_decode_all_sequences(P):
+    # all 8 sequences (32k-128k tokens, E4M3) at the stated 512-token
+    # partitions, and at the automatic choice (4096 here)
     case = W.long_fp8_decode(device=DEV)
-    lens = case.seq_lens.cpu().numpy()
-    _sampled_check(case, [int(np.argmax(lens))], P=P)
+    _sampled_check(case, list(range(8)), P=P)
 
 
 def test_automatic_partition_for_the_bench_shapes():

@@ -65,7 +65,7 @@ def test_p2_varlen_example(causal):
 
 @pytest.mark.parametrize("dtype", [W.BF16, W.F16])
 @pytest.mark.parametrize("bs", [16, 32, 64])
-@pytest.mark.parametrize("G", [1, 4])
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
 @pytest.mark.parametrize("causal", [True, False])
 def test_prefill_ragged(dtype, bs, G, causal):
     lq = [1, 64, 65, 130, 0, 17, 200, 3]
@@ -103,10 +103,13 @@ def test_status_on_bad_block_and_length():
 
 
 def test_full_mixed_varlen_sampled():
-    """The mixed batch (8 prefill + 120 decode sequences) in one call; the
-    oracle checks the first and last 16 query rows of every prefill sequence
-    (bottom-right alignment makes a row subset a valid sub-batch) and 20
-    decode rows."""
+    """The mixed batch (8 prefill + 120 decode sequences) in one call.  The
+    oracle checks, for every prefill sequence, its first and last 16 query
+    rows and a window of 128 query rows from its middle (four whole 32-token
+    query tiles at four query heads per KV head), and every decode row.
+    Bottom-right alignment makes each such run of rows a valid sub-batch: rows
+    a .. a+n-1 of a sequence with Lq queries over Lk keys are n queries over
+    the first Lk - Lq + a + n keys."""
     case = W.mixed_varlen(device=DEV)
     lq = np.array(case.meta["query_lens"])
     lk = np.array(case.meta["key_lens"])
@@ -122,13 +125,25 @@ def test_full_mixed_varlen_sampled():
     kc, vc = W.as_bits(case.k_cache), W.as_bits(case.v_cache)
     bt = case.block_table.cpu().numpy()
     rows, sub_q, sub_k, seqs = [], [], [], []
-    for b in list(range(8)) + list(range(8, 128, 6)):
-        r = min(16, lq[b])
-        prior = lk[b] - lq[b]
-        # first r rows: a sequence of r queries over prior + r keys
-        rows.append(np.arange(cu_q[b], cu_q[b] + r)); sub_q.append(r); sub_k.append(prior + r); seqs.append(b)
-        if lq[b] > r:  # last r rows: r queries over all keys
-            rows.append(np.arange(cu_q[b + 1] - r, cu_q[b + 1])); sub_q.append(r); sub_k.append(lk[b]); seqs.append(b)
+
+    def take(b, a, n):
+        rows.append(np.arange(cu_q[b] + a, cu_q[b] + a + n))
+        sub_q.append(n)
+        sub_k.append(lk[b] - lq[b] + a + n)
+        seqs.append(b)
+
+    n_pre = int(case.meta["n_prefill"])
+    for b in range(len(lq)):
+        if b >= n_pre:
+            take(b, 0, int(lq[b]))  # a decode row: one query over all keys
+            continue
+        r = min(16, int(lq[b]))
+        take(b, 0, r)
+        mid = max(r, (int(lq[b]) // 2 // 32) * 32 - 64)
+        if lq[b] >= mid + 128 + r:
+            take(b, mid, 128)
+        if lq[b] > r:
+            take(b, int(lq[b]) - r, r)
     rows = np.concatenate(rows)
     cq = np.concatenate([[0], np.cumsum(sub_q)]).astype(np.int32)
     ck = np.concatenate([[0], np.cumsum(sub_k)]).astype(np.int32)
