@@ -187,12 +187,17 @@ pa_status pa_decode(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cach
  * workspace: the split-K partial results go to a scratch array of
  * PA_DECODE_STATIC_WS_BYTES that is built into the library and held by every
  * GPU that loads it until the process exits.  It allocates nothing.
- *   - A call whose pa_decode_workspace_size(...) exceeds
+ *   - partition_size 0 is resolved first (pa_decode_partition_size) and the
+ *     resolved partition is the one both the size check and the launch use.
+ *   - A call whose pa_decode_workspace_size(..., resolved partition) exceeds
  *     PA_DECODE_STATIC_WS_BYTES returns PA_ERR_UNSUPPORTED and launches
  *     nothing (use pa_decode with a workspace of your own instead).
  *   - The first call on a device looks up the scratch's device address
- *     (cudaGetSymbolAddress, with that device current) and remembers it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and remembers it
+ *     together with the context then current; a call that finds another
+ *     context current (after cudaDeviceReset, or in a context the caller
+ *     created) looks it up again.  Make the first call on a device, and in
+ *     each such new context, before any stream capture.
  *   - Every call on a device shares the one array and finds the previous
  *     call's data in it; nothing needs clearing, but calls whose kernels
  *     overlap on the GPU (e.g. on two unordered streams) race and give wrong
@@ -425,6 +430,25 @@ pa_status pa_pool_block_table(void* pool, const int64_t* seq_ids, int32_t n, int
 int64_t pa_pool_num_free(void* pool);
 int32_t pa_pool_ref_count(void* pool, int64_t block);
 int32_t pa_pool_seq_len(void* pool, int64_t seq_id);
+
+/* ---------------------------------------------------------------------------
+ * Test hook for the decode's wait timeout.  (Not on the pages: every wait of
+ * the library's kernels is bounded, so that a stalled copy ends in an error
+ * status instead of a hung GPU.)
+ *
+ * Same arguments and host checks as pa_decode, but the launched decode's
+ * producer warp issues no copy at all: no page and no query ever lands, so
+ * every consumer wait runs out after the library's wait limit (2 s) with
+ * nothing in flight, PA_ERR_TIMEOUT (5) is written to *dev_status, and the
+ * kernel returns.  The output and workspace contents are unspecified
+ * afterwards (within their stated sizes); the device stays usable.  For the
+ * library's own tests; a serving path has no use for it.
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode_test_wait_timeout(void* out, const void* q, pa_dtype q_dtype, const pa_kv_cache* cache,
+                                      const int32_t* block_table, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                      int32_t num_heads, float scale, int32_t partition_size, void* workspace,
+                                      size_t workspace_bytes, int32_t* dev_status, pa_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -66,6 +66,8 @@ def library():
                                           i32, vp, vp], C.c_int),
             "pa_decode_static_ws": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, vp],
                                     C.c_int),
+            "pa_decode_test_wait_timeout": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, i32, vp, sz, vp,
+                                             vp], C.c_int),
             "pa_decode_cascade_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
             "pa_decode_partition_size": ([i32, i32, i32, i32], i32),
             "pa_decode_cascade": ([vp, vp, C.c_int, pc, vp, i32, vp, i32, i32, i32, f32, vp, vp, i32, i32, i32,
@@ -276,6 +278,23 @@ def pa_decode(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: t
                              block_table.shape[1], _ptr(seq_lens), B, int(max_seq_len), H, float(scale),
                              int(partition_size), _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(q))
     _check(st, "pa_decode")
+
+
+def pa_decode_test_wait_timeout(out: torch.Tensor, q: torch.Tensor, cache: KVCache, block_table: torch.Tensor,
+                                seq_lens: torch.Tensor, max_seq_len: int, scale: float, partition_size: int = 0,
+                                workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None):
+    """Test hook: pa_decode whose copies are never issued, so every wait of
+    the kernel runs out (PA_ERR_TIMEOUT in dev_status after about 2 s)."""
+    _need(q, "q")
+    _need(out, "out", q.dtype)
+    B, H, D = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    cs = cache.c_struct()
+    st = library().pa_decode_test_wait_timeout(_ptr(out), _ptr(q), torch_dtype_code(q.dtype), C.byref(cs),
+                                               _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B,
+                                               int(max_seq_len), H, float(scale), int(partition_size),
+                                               _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(q))
+    _check(st, "pa_decode_test_wait_timeout")
 
 
 def pa_decode_partition_size(num_seqs, num_heads, num_kv_heads, max_seq_len) -> int:

@@ -86,7 +86,7 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
                        pa_stream_t stream, const void* k_new, const void* v_new,
                        const int32_t* cu_seq_lens_k = nullptr, const int32_t* cu_groups = nullptr,
                        const int32_t* shared_lens = nullptr, int32_t num_groups = 0, bool group_mode = false,
-                       int32_t max_group_size = 0) {
+                       int32_t max_group_size = 0, bool no_copies = false) {
     pa_status st = check_cache(cache);
     if (st != PA_OK) return st;
     if (num_seqs < 0 || num_heads <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 ||
@@ -164,6 +164,7 @@ pa_status decode_entry(void* out, const void* q, pa_dtype q_dtype, const pa_kv_c
     p.shared_lens = shared_lens;
     p.num_groups = num_groups;
     p.num_members = num_seqs;
+    p.no_copies = no_copies ? 1 : 0;
     int kgroup = group;
     if (group_mode) {
         p.vm = vm;
@@ -211,6 +212,17 @@ extern "C" pa_status pa_decode_append(void* out, const void* q, const void* k_ne
     return pa::decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                             max_seq_len, num_heads, scale, partition_size, workspace, workspace_bytes, dev_status,
                             stream, k_new, v_new);
+}
+
+extern "C" pa_status pa_decode_test_wait_timeout(void* out, const void* q, pa_dtype q_dtype,
+                                                 const pa_kv_cache* cache, const int32_t* block_table,
+                                                 int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                                 int32_t num_seqs, int32_t max_seq_len, int32_t num_heads,
+                                                 float scale, int32_t partition_size, void* workspace,
+                                                 size_t workspace_bytes, int32_t* dev_status, pa_stream_t stream) {
+    return pa::decode_entry(out, q, q_dtype, cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                            max_seq_len, num_heads, scale, partition_size, workspace, workspace_bytes, dev_status,
+                            stream, nullptr, nullptr, nullptr, nullptr, nullptr, 0, false, 0, true);
 }
 
 extern "C" int32_t pa_decode_partition_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,

@@ -91,6 +91,10 @@ struct DecodeParams {
     int32_t vcount;
     int32_t g_real;
     int32_t num_members;
+    // test hook (pa_decode_test_wait_timeout; 0 on every other path): the
+    // producer warp issues no copy at all, so every consumer wait runs out
+    // with nothing in flight, reports PA_ERR_TIMEOUT and the block returns
+    int32_t no_copies;
 };
 
 template <int QDT, int KVDT, int D, int G, int BS>
@@ -1015,6 +1019,7 @@ paged_decode_kernel(const DecodeParams p) {
 
     if (warp == C::NCW) {
         // ------------------------------ producer ------------------------------
+        if (p.no_copies) return;
         const uint64_t policy = policy_evict_first();
         uint32_t fill = 0;    // ring stages used so far by this CTA
         uint32_t stage = 0;   // fill % S
