@@ -1,23 +1,33 @@
 #!/usr/bin/env python3
-"""Benchmark of the paged KV-cache decode path on GB300.
+"""Benchmark of the paged KV-cache attention path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload mha|gqa|long|mixed|tiny]
+                    [--workload all|mha|gqa|long|mixed|tiny|swap]
 
-One step = one pass of the whole decode hot path over one batch: the new
-token's K/V of every sequence is written through its slot (slots come from
-the host block pool), then single-query paged attention runs over every
-sequence (and the partition merge where a sequence was split).  The default
-workload is the 7B-shaped MHA decode layer: 64 sequences, 32 heads, head size
-128, block size 16, fp16, attended lengths uniform in [1, 2048], physical
-blocks drawn from a seeded permutation of a 10,000-block pool.
+One step = one pass of the whole hot path over one batch: the new token's
+K/V of every sequence is written through its slot (slots from
+pa_slot_mapping over the batch's block table), then single-query paged
+attention runs over every sequence (and the partition merge where a sequence
+was split); for the mixed batch, every new token's K/V is written, then one
+varlen call attends all query rows.
+
+The default (--workload all) prints ONE JSON line: the headline workload, the
+7B-shaped MHA decode layer (64 sequences, 32 heads, head size 128, block size
+16, fp16, attended lengths uniform in [1, 2048], physical blocks drawn from a
+seeded permutation of a 10,000-block pool), and under "configs" one record
+per other workload -- the worked example ("tiny"), the GQA parallel-sampling
+batch built through the library's block pool, fork and copy-on-write ("gqa"),
+the long-context E4M3 split-K decode ("long") and the mixed varlen prefill +
+decode batch ("mixed") -- each with its own value, roofline, e2e, clocks and
+CPU baseline.
 
 `value` is the algorithmic K/V bytes the step reads (sum over sequences of
 L * num_kv_heads * head_size * 2 * element size) per second of device time,
-summed over ranks, with all inputs resident in HBM.  `e2e` is the same metric
-when every step also copies its inputs from pinned host memory and reads the
-outputs back.  With N > 1 (torchrun) every rank runs its own replica: the path
-has no exchange step, so there is no collective in the timed work.
+summed over ranks, with all inputs resident in HBM (the mixed batch: causal
+FLOPs per second).  `e2e` is the same metric when every step also copies its
+inputs from pinned host memory and reads the outputs back.  With N > 1
+(torchrun) every rank runs its own replica: the path has no exchange step, so
+there is no collective in the timed work.
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores
 on a bounded sample of the same workload.
@@ -45,49 +55,28 @@ METRIC = "paged-attn decode KV-read GB/s (% of GB300 HBM peak); decode seqs/s pe
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture (`--set full`, one launch after 3 warm-up steps), keyed by workload
-# and the hash of the kernel source it was taken on; reported only while that
-# source is unchanged.
-NCU_TRAFFIC = {
-    ("mha", "07c6a73572c19639"): 945_729_792,
-    ("gqa", "07c6a73572c19639"): 1_003_785_472,
-    ("long", "07c6a73572c19639"): 1_748_673_610,
-    ("mixed", "0932f6a3353bb5b1"): 1_314_560_216,
-    ("mixed", "e5e1d4af739c4631"): 1_554_890_240,
-    ("mha", "c47a7983c3cb25e9"): 945_337_856,
-    ("gqa", "c47a7983c3cb25e9"): 939_493_120,
-    ("long", "c47a7983c3cb25e9"): 1_748_532_224,
-    ("mha", "7cb5cae478ced3ab"): 945_331_968,
-    ("gqa", "7cb5cae478ced3ab"): 939_895_040,
-    ("long", "7cb5cae478ced3ab"): 1_748_656_896,
-    ("mixed", "530d95a1f63ff18c"): 1_556_752_896,
-    ("mha", "a632445778d43fd8"): 944_534_528,
-    ("gqa", "a632445778d43fd8"): 939_881_984,
-    ("long", "a632445778d43fd8"): 1_749_401_856,
-    ("mha", "6eae42cdb4f82c16"): 944_916_480,
-    ("gqa", "6eae42cdb4f82c16"): 939_575_040,
-    ("long", "6eae42cdb4f82c16"): 1_749_021_696,
-    ("mha", "7779adaa5cbb9b71"): 944_760_064,
-    ("gqa", "7779adaa5cbb9b71"): 939_720_448,
-    ("long", "7779adaa5cbb9b71"): 1_749_494_528,
-    ("mha", "4facb81714f61645"): 944_771_072,
-    ("gqa", "4facb81714f61645"): 939_407_360,
-    ("long", "4facb81714f61645"): 1_748_968_448,
-    ("mixed", "a2e53b228aac2fea"): 1_554_160_640,
-    ("mha", "982cdac6a2c10305"): 945_004_288,
-    ("gqa", "982cdac6a2c10305"): 939_515_904,
-    ("long", "982cdac6a2c10305"): 1_749_042_688,
-    ("mixed", "f803016c3ea7946c"): 1_545_752_320,
-    ("mha", "6c3aaacd1f8b3e95"): 944_406_528,
-    ("gqa", "6c3aaacd1f8b3e95"): 939_486_464,
-    ("long", "6c3aaacd1f8b3e95"): 1_748_525_824,
-    ("mha", "11ea94ecf1cf01da"): 944_880_128,
-    ("gqa", "11ea94ecf1cf01da"): 939_508_992,
-    ("long", "11ea94ecf1cf01da"): 1_748_537_088,
-    ("mixed", "bbcf4a857c344141"): 1_557_721_856,
-}
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture per workload, listed in profiles/ncu_traffic.md as table rows
+# "| workload | kernel source hash | bytes | ..."; a figure is reported only
+# while the kernel source it was taken on is unchanged.
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "ncu_traffic.md")
+
+
+def ncu_traffic(workload, src_hash):
+    try:
+        with open(TRAFFIC_TABLE) as f:
+            for line in f:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                if len(cells) >= 3 and cells[0] == workload and cells[1] == src_hash:
+                    return int(cells[2].replace(",", "").replace("_", ""))
+    except OSError:
+        pass
+    return None
+
+
 L2_BYTES = 129 * 1024 * 1024
+# nominal host link of a Grace-Blackwell superchip (NVLink-C2C), per direction
+C2C_GBS_PER_DIRECTION = 450.0
 DECODE_SOURCES = ("decode_impl.cuh", "decode_launch.cuh", "decode_api.cu", "common.cuh")
 PREFILL_SOURCES = ("prefill.cu", "common.cuh", "launch.h")
 
@@ -355,9 +344,14 @@ def build_workload(name, device, num_seqs=None, pool_blocks=None):
         tag = "mha_decode_%dseq_32h_d128_bs16_fp16_len_u1_2048_pool%d" % (B, nb)
         return W.mha_decode(device=device, B=B, num_blocks=nb), tag
     if name == "gqa":
+        from paged_kv_cache_75_gb300 import sampling
         groups = (num_seqs or 256) // 4
-        return (W.gqa_shared_decode(device=device, groups=groups),
-                "gqa_decode_%dseq_32q8kv_d128_bs16_bf16_lognormal1000_shared4" % (4 * groups))
+        case = sampling.build_sampled_batch(W.gqa_sampling_inputs(device=device, groups=groups), device)
+        torch.cuda.synchronize()
+        if int(case.meta["dev_status"].item()) != 0:
+            raise RuntimeError("device status %d while building the sampled batch"
+                               % int(case.meta["dev_status"].item()))
+        return case, build_workload_name("gqa", groups)
     if name == "long":
         B = num_seqs or 8
         return W.long_fp8_decode(device=device, B=B), "long_decode_%dseq_64q8kv_d128_bs32_e4m3_len_u32k_128k_p512" % B
@@ -643,7 +637,7 @@ def timed_split(step: PrefillStep, steps, warmup):
     return start.elapsed_time(end) / steps
 
 
-def run_prefill(args, case, wname, dev, rank, world):
+def run_prefill(args, case, wname, dev, rank, world, cpu_budget=10.0):
     step = PrefillStep(case, dev, wname)
     total_ms, main_ms, clocks = timed_prefill(step, args.steps, args.warmup, world)
     total_ms, flops_sum = aggregate(total_ms, float(step.flops) * args.steps, world)
@@ -651,6 +645,8 @@ def run_prefill(args, case, wname, dev, rank, world):
     split_ms = timed_split(step, args.steps, args.warmup)
     e2e_ms, flops_e2e = aggregate(e2e_ms, float(step.flops) * args.steps, world)
     _, tflops_peak, tflops_sustained, peak_kind = measured_peaks()
+    # the varlen kernel is timed per launch in steps of well under a
+    # millisecond, not inside a seconds-long loop: the burst peak applies
     achieved = step.flops / (main_ms / 1e3) / 1e12
     line = {
         "metric": "paged-attn varlen prefill TFLOP/s (causal, % of GB300 bf16 tensor peak)",
@@ -683,15 +679,15 @@ def run_prefill(args, case, wname, dev, rank, world):
             "note": "the same step through pa_varlen_mixed: the varlen kernel on the prefill sequences, "
                     "the decode kernel on the trailing one-token sequences (same FLOPs counted)"},
         "roofline": {"bound": "tensor", "kernel": "pa_prefill_varlen", "achieved": round(achieved, 2),
-                     "peak": tflops_sustained, "unit": "TFLOP/s", "frac": round(achieved / tflops_sustained, 4),
-                     "peak_kind": "of %s (bf16 dense, sustained)" % peak_kind,
-                     "traffic": NCU_TRAFFIC.get(("mixed", kernel_source_hash(PREFILL_SOURCES))),
+                     "peak": tflops_peak, "unit": "TFLOP/s", "frac": round(achieved / tflops_peak, 4),
+                     "peak_kind": "of %s (bf16 dense, burst)" % peak_kind,
+                     "frac_of_sustained": round(achieved / tflops_sustained, 4),
+                     "traffic": ncu_traffic("mixed", kernel_source_hash(PREFILL_SOURCES)),
                      "prefill_ms": round(main_ms, 5), "kernel_src": kernel_source_hash(PREFILL_SOURCES)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_prefill(case)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+        line["cpu_baseline"] = cpu_baseline_prefill(case, cpu_budget)
+    return line
 
 
 def timed_e2e(step: DecodeStep, steps, warmup, world):
@@ -875,40 +871,27 @@ def run_swap(args, dev, rank, world):
         "swap_out_gbs": round(gbs(t_out), 2), "swap_in_gbs": round(gbs(t_in), 2),
         "gpu_launches": 2 * steps,
         "roofline": {"bound": "link", "kernel": "swap_blocks_kernel", "achieved": round(gbs(t_out), 2),
-                     "peak": round(gbs(t_d2h), 2), "unit": "GB/s", "frac": round(t_d2h / t_out, 4),
-                     "peak_kind": "of a contiguous device->host copy of the same bytes, measured live",
-                     "swap_in_frac": round(t_h2d / t_in, 4), "h2d_copy_gbs": round(gbs(t_h2d), 2),
+                     "peak": C2C_GBS_PER_DIRECTION, "unit": "GB/s",
+                     "frac": round(gbs(t_out) / C2C_GBS_PER_DIRECTION, 4),
+                     "peak_kind": "of nominal (NVLink-C2C between the Grace host and the GPU: 900 GB/s both "
+                                  "directions together, 450 GB/s each way)",
+                     "swap_in_frac": round(gbs(t_in) / C2C_GBS_PER_DIRECTION, 4),
+                     "d2h_copy_engine_gbs": round(gbs(t_d2h), 2), "h2d_copy_engine_gbs": round(gbs(t_h2d), 2),
+                     "copy_engine_note": "one contiguous cudaMemcpyAsync of the same bytes each way (torch copy_), "
+                                         "measured in the same run: context, not the peak",
                      "traffic": None},
-        "cpu_baseline": {"value": round(cpu_gbs, 2), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(cpu_gbs, 2), "unit": "GB/s", "cores": 1, "kind": "numpy_gather",
                          "sample": "numpy gather of 1024 of 2048 host blocks of 256 KiB, %d passes" % reps},
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    return line
 
 
 # ---------------------------------------------------------------------------
-def run_ours(args):
-    rank, local_rank, world = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    if args.workload == "swap":
-        run_swap(args, dev, rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
-    case, wname = build_workload(args.workload, dev, args.num_seqs, args.pool_blocks)
-    if args.workload == "mixed":
-        run_prefill(args, case, wname, dev, rank, world)
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
+def run_decode(args, workload, dev, rank, world, cpu_budget=10.0):
+    """One decode workload's record (not printed)."""
+    case, wname = build_workload(workload, dev, args.num_seqs, args.pool_blocks)
     # the long-context configuration states its partition (512 tokens)
-    partition = args.partition_size or (512 if args.workload == "long" else 0)
+    partition = args.partition_size or (512 if workload == "long" else 0)
     step = DecodeStep(case, dev, partition, wname)
     # the K/V a step reads, plus everything else it touches
     small = step.kv_bytes + case.q.numel() * case.q.element_size() * 2 < L2_BYTES
@@ -940,12 +923,11 @@ def run_ours(args):
             a_total, a_sum = aggregate(a_total, float(astep.kv_bytes) * args.steps, world)
             auto = {"partition_size": astep.P_eff, "ms_per_step": round(a_total / args.steps, 5),
                     "value": round(a_sum / (a_total / 1e3) / 1e9, 2), "unit": "GB/s",
-                    "kernel_achieved": round(unique_bytes_of(case) / (a_decode / 1e3) / 1e9, 1),
-                    "kernel_frac": round(unique_bytes_of(case) / (a_decode / 1e3) / 1e9 / measured_peaks()[0], 4),
+                    "kernel_achieved": round(unique_bytes / (a_decode / 1e3) / 1e9, 1),
+                    "kernel_frac": round(unique_bytes / (a_decode / 1e3) / 1e9 / hbm, 4),
                     "note": "the same step with partition_size 0 (pa_decode_partition_size); not in value"}
         del astep
     src_hash = kernel_source_hash()
-    traffic = NCU_TRAFFIC.get((args.workload, src_hash))
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -971,6 +953,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single"},
         "seqs_per_s_per_layer": round(seqs_sum / (total_ms / 1e3), 1),
         "hbm_frac_of_8000": round(value / world / 8000.0, 4),
+        "hbm_frac_of_8000_distinct": round(value / world / 8000.0 * unique_bytes / step.kv_bytes, 4),
         "clocks": clocks,
         "e2e": {"value": round(kv_e2e / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
@@ -994,15 +977,92 @@ def run_ours(args):
                      "frac": round(achieved / hbm, 4), "peak_kind": "of %s" % peak_kind,
                      "bytes": "distinct K/V rows read (unique_kv_bytes_per_step)",
                      "achieved_logical": round(achieved_logical, 1),
-                     "traffic": traffic, "decode_ms": round(decode_ms, 5), "kernel_src": src_hash},
+                     "traffic": ncu_traffic(workload, src_hash), "decode_ms": round(decode_ms, 5),
+                     "kernel_src": src_hash},
     }
+    if small:
+        line["us_per_step"] = round(ms_per_step * 1e3, 2)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case)
+        line["cpu_baseline"] = cpu_baseline(case, cpu_budget)
+    del step, case
+    return line
+
+
+SUB_KEYS = ("n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data")
+
+
+def run_ours(args):
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    def one(workload, cpu_budget=10.0):
+        if workload == "swap":
+            return run_swap(args, dev, rank, world)
+        if workload == "mixed":
+            case, wname = build_workload("mixed", dev)
+            line = run_prefill(args, case, wname, dev, rank, world, cpu_budget)
+            del case
+            return line
+        return run_decode(args, workload, dev, rank, world, cpu_budget)
+
+    if args.workload == "all":
+        # the headline line (the MHA decode layer) carries every other
+        # configuration's record under "configs"
+        line = one("mha")
+        configs = {}
+        for w in ("tiny", "gqa", "long", "mixed"):
+            torch.cuda.empty_cache()
+            sub = one(w, cpu_budget=5.0)
+            for k in SUB_KEYS:
+                sub.pop(k, None)
+            configs[w] = sub
+        line["configs"] = configs
+    else:
+        line = one(args.workload)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def build_workload_name(name, groups=64):
+    return "gqa_decode_%dseq_32q8kv_d128_bs16_bf16_lognormal1000_shared4_pool_cow" % (4 * groups)
+
+
+def oracle_sampled_case(inp):
+    """The parallel-sampling batch built on the host for the reference arm:
+    the pool's reference model in the library's order of operations, then the
+    oracle's cache write and block copy (no GPU involved)."""
+    import oracle
+    from oracle.pool_model import BlockPoolModel
+    m = BlockPoolModel(inp.num_blocks, inp.block_size, inp.free_order.tolist())
+    ps, gsl, pr = [], [], []
+    gs = inp.group_size
+    for g, (L, P) in enumerate(zip(inp.group_lens.tolist(), inp.prompt_lens.tolist())):
+        m.add_seq(g * gs)
+        ps += m.append(g * gs, P)[0]
+        for k in range(1, gs):
+            m.fork(g * gs, g * gs + k)
+        for k in range(gs):
+            s_, c_ = m.append(g * gs + k, L - P)
+            gsl += s_
+            pr += c_
+    kc, vc = W.as_bits(inp.k_cache_init), W.as_bits(inp.v_cache_init)
+    oracle.cache_write(kc, vc, W.BF16, W.as_bits(inp.prompt_k), W.as_bits(inp.prompt_v), W.BF16,
+                       np.asarray(ps, np.int64))
+    oracle.copy_blocks(kc, vc, W.BF16, np.asarray(pr, np.int32).reshape(-1, 2))
+    oracle.cache_write(kc, vc, W.BF16, W.as_bits(inp.gen_k), W.as_bits(inp.gen_v), W.BF16, np.asarray(gsl, np.int64))
+    table, lens = m.block_table(list(range(inp.num_seqs)), inp.max_blocks)
+    as_t = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    return W.PagedCase(q=inp.q, k_cache=as_t(kc), v_cache=as_t(vc), block_table=torch.tensor(table, dtype=torch.int32),
+                       seq_lens=torch.tensor(lens, dtype=torch.int32), q_dtype=W.BF16, kv_dtype=W.BF16,
+                       num_heads=inp.num_heads, num_kv_heads=inp.num_kv_heads, head_size=inp.head_size,
+                       block_size=inp.block_size, scale=inp.scale)
 
 
 def run_reference(args):
@@ -1036,10 +1096,14 @@ def run_reference(args):
         }), flush=True)
         return
     import oracle
-    case, wname = build_workload(args.workload, "cpu")
+    workload = "mha" if args.workload == "all" else args.workload  # the headline line's workload
+    if workload == "gqa":
+        case, wname = oracle_sampled_case(W.gqa_sampling_inputs(device="cpu")), build_workload_name("gqa")
+    else:
+        case, wname = build_workload(workload, "cpu")
     cores = os.cpu_count() or 1
     n = oracle.num_threads(cores)
-    if args.workload == "mixed":
+    if workload == "mixed":
         kc, vc = W.as_bits(case.k_cache), W.as_bits(case.v_cache)
         sample = prefill_sample(case, rows_per_prefill=1, decode_every=12)
         flops = 4 * case.head_size * case.num_heads * sample[4]
@@ -1090,7 +1154,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mha", "gqa", "long", "tiny", "mixed", "swap"], default="mha")
+    ap.add_argument("--workload", choices=["all", "mha", "gqa", "long", "tiny", "mixed", "swap"], default="all")
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--num-seqs", type=int, default=None, help="sequences (smaller profiling cases)")

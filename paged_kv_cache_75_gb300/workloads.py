@@ -173,57 +173,81 @@ def gqa_group_lengths(seed=3000, groups=64, median=1000.0, sigma=1.0, lo=16, hi=
     return np.clip(L, lo, hi)
 
 
-def gqa_shared_decode(seed=3000, device="cpu", groups=64, group_size=4, block_size=16,
-                      pool_factor=1.25, max_len=8192) -> PagedCase:
+@dataclass
+class SamplingInputs:
+    """Raw inputs of a parallel-sampling decode batch: groups of members that
+    share a prompt and then each generated tokens of their own.  Only values,
+    lengths and the pool's initial free order; the block pool, forks,
+    copy-on-write and cache writes that turn them into a paged cache are the
+    library's (paged_kv_cache_75_gb300.sampling) and, for the tests, the
+    oracle's."""
+    group_lens: np.ndarray     # int64 [groups]: every member attends this many tokens
+    prompt_lens: np.ndarray    # int64 [groups]: the shared prompt's tokens
+    group_size: int
+    num_blocks: int            # pool size
+    free_order: np.ndarray     # int32 [num_blocks]: the pool's initial free list
+    prompt_k: torch.Tensor     # [sum prompt_lens, Hkv, D], groups in order
+    prompt_v: torch.Tensor
+    gen_k: torch.Tensor        # [sum over members of (L - P), Hkv, D], members in order
+    gen_v: torch.Tensor
+    q: torch.Tensor            # [groups * group_size, H, D]
+    k_cache_init: torch.Tensor  # [num_blocks, Hkv, bs, D]: contents before anything is written
+    v_cache_init: torch.Tensor
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    dtype: int
+    scale: float
+    max_blocks: int
+
+    @property
+    def num_seqs(self):
+        return len(self.group_lens) * self.group_size
+
+
+def gqa_sampling_inputs(seed=3000, device="cpu", groups=64, group_size=4, block_size=16, pool_factor=1.25,
+                        max_len=8192, with_values=True) -> SamplingInputs:
     """256 seqs in 64 parallel-sampling groups of 4; 32 query / 8 KV heads,
     head size 128, block size 16, bf16.  Group length L ~ LogNormal(median
-    1000, sigma 1) clipped to [16, 8192]; all members share L.  The prompt
-    (floor(L/2) tokens) is shared: its full blocks are the same physical
-    blocks in every member (reference count 4); the partially filled prompt
-    block is a private copy for members 1..3 (copy-on-write); generated
-    blocks are private.  Pool = 1.25 x the unique blocks, shuffled."""
+    1000, sigma 1) clipped to [16, 8192]; all members attend L tokens: the
+    prompt's floor(L/2), shared, then L - floor(L/2) generated tokens of their
+    own.  The pool holds 1.25 x the blocks the batch ends up using (its full
+    prompt blocks once, the partially filled prompt block and the generated
+    blocks once per member), in a seeded random free order.  with_values=False
+    leaves every tensor out (None): lengths and the pool's order only."""
     g = np.random.default_rng(seed + 1)
     L = gqa_group_lengths(seed, groups, hi=max_len)
+    P = L // 2
     bs = block_size
-    tables, lens, shared_rows, cow_pairs = [], [], [], []
-    counts = []
-    for Lg in L:
-        P = int(Lg) // 2
-        n_shared = P // bs
-        n_total = pages_for(int(Lg), bs)
-        counts.append((n_shared, n_total))
-    unique = sum(ns + group_size * (nt - ns) for ns, nt in counts)
+    unique = 0
+    for Lg, Pg in zip(L, P):
+        ns, nt = int(Pg) // bs, pages_for(int(Lg), bs)
+        unique += ns + group_size * (nt - ns)
     num_blocks = int(np.ceil(pool_factor * unique))
-    ids = g.permutation(num_blocks)
-    mb = pages_for(max_len, bs)
-    k = 0
-    for gi, (ns, nt) in enumerate(counts):
-        shared = ids[k:k + ns]
-        k += ns
-        first_private = None
-        for m in range(group_size):
-            row = np.full(mb, -1, np.int32)
-            row[:ns] = shared
-            priv = ids[k:k + nt - ns]
-            k += nt - ns
-            row[ns:nt] = priv
-            if m == 0 and nt > ns:
-                first_private = priv[0]
-            elif nt > ns and (int(L[gi]) // 2) % bs != 0:
-                cow_pairs.append((int(first_private), int(priv[0])))
-            tables.append(row)
-            lens.append(int(L[gi]))
-    case = make_decode_case(seed + 2, lens, 32, 8, 128, bs, num_blocks, BF16, BF16,
-                            block_table=np.stack(tables), device=device)
-    case.meta["unique_blocks"] = unique
-    case.meta["group_size"] = group_size
-    # the sampling groups as a cascade decode sees them: members are
-    # consecutive rows; the shared length is the prompt's whole blocks
-    case.meta["cu_groups"] = np.arange(0, groups * group_size + 1, group_size, dtype=np.int32)
-    case.meta["shared_lens"] = np.array([ns * bs for ns, _ in counts], np.int32)
-    # copy-on-write pairs (source = member 0's partial prompt block)
-    case.meta["cow_pairs"] = np.array(cow_pairs, np.int32).reshape(-1, 2)
-    return case
+    free_order = g.permutation(num_blocks).astype(np.int32)
+    H, Hkv, D = 32, 8, 128
+    gen_t = torch.Generator(device=device)
+    gen_t.manual_seed(seed + 2)
+    n_gen = int(group_size * (L - P).sum())
+    if not with_values:
+        return SamplingInputs(group_lens=L.astype(np.int64), prompt_lens=P.astype(np.int64), group_size=group_size,
+                              num_blocks=num_blocks, free_order=free_order, prompt_k=None, prompt_v=None,
+                              gen_k=None, gen_v=None, q=None, k_cache_init=None, v_cache_init=None, num_heads=H,
+                              num_kv_heads=Hkv, head_size=D, block_size=bs, dtype=BF16, scale=1.0 / D ** 0.5,
+                              max_blocks=pages_for(max_len, bs))
+    q = random_values(gen_t, (groups * group_size, H, D), BF16, device)
+    pk_ = random_values(gen_t, (int(P.sum()), Hkv, D), BF16, device)
+    pv_ = random_values(gen_t, (int(P.sum()), Hkv, D), BF16, device)
+    gk_ = random_values(gen_t, (n_gen, Hkv, D), BF16, device)
+    gv_ = random_values(gen_t, (n_gen, Hkv, D), BF16, device)
+    kc = _fill_cache(gen_t, num_blocks, Hkv, bs, D, BF16, device)
+    vc = _fill_cache(gen_t, num_blocks, Hkv, bs, D, BF16, device)
+    return SamplingInputs(group_lens=L.astype(np.int64), prompt_lens=P.astype(np.int64), group_size=group_size,
+                          num_blocks=num_blocks, free_order=free_order, prompt_k=pk_, prompt_v=pv_, gen_k=gk_,
+                          gen_v=gv_, q=q, k_cache_init=kc, v_cache_init=vc, num_heads=H, num_kv_heads=Hkv,
+                          head_size=D, block_size=bs, dtype=BF16, scale=1.0 / D ** 0.5,
+                          max_blocks=pages_for(max_len, bs))
 
 
 def long_context_lengths(seed=4000, B=8, lo=32768, hi=131072):

@@ -13,6 +13,7 @@ import torch.multiprocessing as mp
 import bench
 import oracle
 from paged_kv_cache_75_gb300 import build as pkg_build
+from paged_kv_cache_75_gb300 import sampling
 from paged_kv_cache_75_gb300 import workloads as W
 
 
@@ -87,16 +88,36 @@ def test_unique_bytes_count_shared_blocks_once():
     assert case.unique_kv_bytes() == (16 + 4) * row
     # the bench's GQA workload: the groups' shared prompt blocks make the
     # distinct rows a strict subset of the logical ones
-    g = W.gqa_shared_decode()
+    _, g, _ = _sampling_plan()
     assert 0 < g.unique_kv_bytes() < g.kv_bytes()
-    m = W.mha_decode()
+    # private blocks only (the MHA workload's table): distinct = logical
+    lens = W.mha_decode_lengths()
+    table = W.assign_blocks(np.random.default_rng(1), lens, 16, 10_000, 128)
+    m = W.PagedCase(q=torch.empty(0), k_cache=torch.empty(0), v_cache=torch.empty(0),
+                    block_table=torch.from_numpy(table), seq_lens=torch.tensor(lens, dtype=torch.int32),
+                    q_dtype=W.F16, kv_dtype=W.F16, num_heads=32, num_kv_heads=32, head_size=128, block_size=16,
+                    scale=1.0)
     assert m.unique_kv_bytes() == m.kv_bytes()
+
+
+def _sampling_plan():
+    """The GQA workload's pool operations on the native pool (host only)."""
+    inp = W.gqa_sampling_inputs(with_values=False)
+    pool, table, lens, prompt_slots, gen_slots, pairs = sampling.plan_sampled_batch(inp)
+    case = W.PagedCase(q=torch.empty(0), k_cache=torch.empty(0), v_cache=torch.empty(0),
+                       block_table=torch.tensor(table, dtype=torch.int32),
+                       seq_lens=torch.tensor(lens, dtype=torch.int32), q_dtype=W.BF16, kv_dtype=W.BF16,
+                       num_heads=inp.num_heads, num_kv_heads=inp.num_kv_heads, head_size=inp.head_size,
+                       block_size=inp.block_size, scale=inp.scale)
+    case.meta["cu_groups"] = np.arange(0, inp.num_seqs + 1, inp.group_size, dtype=np.int32)
+    case.meta["shared_lens"] = ((inp.prompt_lens // inp.block_size) * inp.block_size).astype(np.int32)
+    return inp, case, (pool, prompt_slots, gen_slots, pairs)
 
 
 def test_gqa_groups_share_their_prompt_blocks():
     # the cascade metadata of the GQA workload: consecutive groups of four whose
     # rows name the same blocks over the shared length, and differ right after
-    g = W.gqa_shared_decode()
+    _, g, _ = _sampling_plan()
     cu, sl = g.meta["cu_groups"], g.meta["shared_lens"]
     bt = g.block_table.numpy()
     lens = g.seq_lens.numpy()
@@ -108,3 +129,41 @@ def test_gqa_groups_share_their_prompt_blocks():
         assert np.all(rows[:, :nb] == rows[0, :nb])
         if cu[k + 1] - cu[k] > 1 and lens[cu[k]] > sl[k]:
             assert len(set(rows[:, nb].tolist())) == cu[k + 1] - cu[k]
+
+
+def test_sampling_plan_matches_the_pool_model():
+    """The GQA workload's cache layout comes from the native pool: add_seq and
+    append of each group's prompt, fork of the other members, append of every
+    member's generated tokens.  The same operations on the pool's reference
+    model give the same slots, copy-on-write pairs, block table, lengths,
+    reference counts and free list size."""
+    from oracle.pool_model import BlockPoolModel
+    inp, case, (pool, prompt_slots, gen_slots, pairs) = _sampling_plan()
+    m = BlockPoolModel(inp.num_blocks, inp.block_size, inp.free_order.tolist())
+    ps, gsl, pr = [], [], []
+    gs = inp.group_size
+    for g, (L, P) in enumerate(zip(inp.group_lens.tolist(), inp.prompt_lens.tolist())):
+        first = g * gs
+        m.add_seq(first)
+        s, c = m.append(first, P)
+        ps += s
+        for k in range(1, gs):
+            m.fork(first, first + k)
+        for k in range(gs):
+            s, c = m.append(first + k, L - P)
+            gsl += s
+            pr += c
+    assert list(prompt_slots) == ps and list(gen_slots) == gsl
+    assert [tuple(x) for x in pairs.tolist()] == pr
+    # one copy per member but the last whose prompt ends inside a block
+    partial = int(np.sum(inp.prompt_lens % inp.block_size != 0))
+    assert len(pr) == (gs - 1) * partial
+    table, lens = m.block_table(list(range(inp.num_seqs)), inp.max_blocks)
+    assert np.array_equal(case.block_table.numpy(), np.array(table, np.int32))
+    assert list(case.seq_lens.numpy()) == lens == list(np.repeat(inp.group_lens, gs))
+    assert pool.num_free() == m.num_free()
+    assert all(pool.ref_count(b) == m.ref[b] for b in range(inp.num_blocks))
+    # full prompt blocks are shared by the whole group
+    ns = int(inp.prompt_lens[0]) // inp.block_size
+    if ns:
+        assert pool.ref_count(int(case.block_table[0, 0])) == gs

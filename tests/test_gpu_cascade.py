@@ -100,16 +100,6 @@ def test_cascade_with_partitions(P):
     assert_close(out, oracle_ref(case), W.BF16, W.BF16, "cascade P=%d" % P)
 
 
-def test_cascade_equals_decode_and_oracle_on_the_gqa_workload():
-    case = W.gqa_shared_decode(device="cpu")
-    cu, sl = case.meta["cu_groups"], case.meta["shared_lens"]
-    out, st = run_cascade(case, cu, sl)
-    assert st == 0
-    lens = case.seq_lens.cpu().numpy()
-    sample = [int(np.argmax(lens)), int(np.argmin(lens))] + list(range(1, 256, 29))
-    assert_close(out[sample], oracle_ref(case, sample), W.BF16, W.BF16, "cascade, sampled")
-
-
 def test_mismatched_shared_blocks_are_reported():
     case, cu, sl = group_case(9, [3], [4], [5, 6, 7], 8, 2, 16, W.F16)
     bt = case.block_table.clone()

@@ -186,12 +186,6 @@ def test_full_mha_decode_all_sequences():
     _sampled_check(case, list(range(64)))
 
 
-def test_full_gqa_shared_decode_all_sequences():
-    # every one of the 256 sequences (64 sampling groups of 4) against the oracle
-    case = W.gqa_shared_decode(device=DEV)
-    _sampled_check(case, list(range(256)))
-
-
 @pytest.mark.parametrize("P", [512, 0])
 def test_full_long_fp8_decode_all_sequences(P):
     # all 8 sequences (32k-128k tokens, E4M3) at the stated 512-token
