@@ -19,7 +19,9 @@ per other workload -- the worked example ("tiny"), the GQA parallel-sampling
 batch built through the library's block pool, fork and copy-on-write ("gqa"),
 the long-context E4M3 split-K decode ("long") and the mixed varlen prefill +
 decode batch ("mixed") -- each with its own value, roofline, e2e, clocks and
-CPU baseline.
+CPU baseline.  The GQA batch's attention call is pa_decode_cascade (its
+groups share their prompt blocks); the plain pa_decode step is reported
+beside it.
 
 `value` is the algorithmic K/V bytes the step reads (sum over sequences of
 L * num_kv_heads * head_size * 2 * element size) per second of device time,
@@ -257,6 +259,8 @@ class DecodeStep:
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
         self.has_groups = "cu_groups" in case.meta
         if self.has_groups:
+            self.launches_per_step = 3  # write, the group-mode decode, the merge
+        if self.has_groups:
             cu, sl = case.meta["cu_groups"], case.meta["shared_lens"]
             self.cu_groups = torch.as_tensor(cu).to(device)
             self.shared_lens = torch.as_tensor(sl).to(device)
@@ -285,6 +289,18 @@ class DecodeStep:
         self.pk.pa_decode(self.out if out is None else out, self.q if q is None else q, self.cache,
                           self.bt if bt is None else bt, self.lens if lens is None else lens, self.max_len,
                           self.case.scale, self.P, self.ws, self.status)
+
+    def attend(self, q=None, out=None, bt=None, lens=None, cu_groups=None, shared_lens=None):
+        """The step's attention call: pa_decode_cascade for a batch of sampling
+        groups that share their prompt blocks (the library's call for such a
+        batch), pa_decode otherwise."""
+        if not self.has_groups:
+            return self.decode(q, out, bt, lens)
+        self.pk.pa_decode_cascade(self.out if out is None else out, self.q if q is None else q, self.cache,
+                                  self.bt if bt is None else bt, self.lens if lens is None else lens, self.max_len,
+                                  self.case.scale, self.cu_groups if cu_groups is None else cu_groups,
+                                  self.shared_lens if shared_lens is None else shared_lens, self.max_group,
+                                  self.max_shared, self.ws_cascade, self.P, self.status)
 
 
 class PrefillStep:
@@ -385,7 +401,7 @@ def kernel_pass(stream, steps, before, kernel, flush=None):
     return sum(a.elapsed_time(b) for a, b in evs) / steps
 
 
-def timed_decode(step: DecodeStep, steps, warmup, world, flush):
+def timed_decode(step: DecodeStep, steps, warmup, world, flush, attend=None):
     """Returns (total ms over the timed steps, mean decode-kernel ms, clocks).
     The timed steps (write + decode) carry no event between their launches;
     with an L2 flush every step is timed on its own and the flush runs between
@@ -393,9 +409,10 @@ def timed_decode(step: DecodeStep, steps, warmup, world, flush):
     pass over the same steps with events around each decode launch; clocks are
     sampled over both."""
     stream = torch.cuda.current_stream()
+    attend = step.attend if attend is None else attend
     for _ in range(warmup):
         step.write()
-        step.decode()
+        attend()
     torch.cuda.synchronize()
     whole = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -408,13 +425,13 @@ def timed_decode(step: DecodeStep, steps, warmup, world, flush):
                 flush()
                 whole[i][0].record(stream)
             step.write()
-            step.decode()
+            attend()
             if flush.buf is not None:
                 whole[i][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        decode_ms = kernel_pass(stream, steps, step.write, step.decode, flush if flush.buf is not None else None)
+        decode_ms = kernel_pass(stream, steps, step.write, attend, flush if flush.buf is not None else None)
     total_ms = sum(a.elapsed_time(b) for a, b in whole) if flush.buf is not None else start.elapsed_time(end)
     st = int(step.status.item())
     if st != 0:
@@ -441,27 +458,6 @@ def timed_append(step: DecodeStep, steps, warmup, flush):
     return sum(a.elapsed_time(b) for a, b in evs) / steps
 
 
-def timed_cascade(step: DecodeStep, steps, warmup, flush):
-    """Mean ms of the step (new token written, then pa_decode_cascade), each
-    step timed on its own with the L2 flush (if any) outside the interval."""
-    stream = torch.cuda.current_stream()
-    for _ in range(warmup):
-        step.write()
-        step.cascade()
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for i in range(steps):
-        flush()
-        evs[i][0].record(stream)
-        step.write()
-        step.cascade()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    if int(step.status.item()) != 0:
-        raise RuntimeError("device status %d in the cascade step" % int(step.status.item()))
-    return sum(a.elapsed_time(b) for a, b in evs) / steps
-
-
 def timed_graph(step: DecodeStep, steps, flush):
     """One step (write + decode) captured as a CUDA graph and replayed: the
     device-side latency without host launch overhead.  Each replay is timed on
@@ -470,7 +466,7 @@ def timed_graph(step: DecodeStep, steps, flush):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
         step.write()
-        step.decode()
+        step.attend()
     for _ in range(3):
         graph.replay()
     torch.cuda.synchronize()
@@ -693,13 +689,16 @@ def run_prefill(args, case, wname, dev, rank, world, cpu_budget=10.0):
 def timed_e2e(step: DecodeStep, steps, warmup, world):
     """The decode step end to end: q, the new K/V, slots, block table and
     lengths up from page-locked host memory, the output back."""
-    src = (("q", step.q), ("k", step.k_new), ("v", step.v_new), ("slots", step.slots), ("bt", step.bt),
-           ("lens", step.lens))
+    src = [("q", step.q), ("k", step.k_new), ("v", step.v_new), ("slots", step.slots), ("bt", step.bt),
+           ("lens", step.lens)]
+    if step.has_groups:
+        src += [("cu_groups", step.cu_groups), ("shared_lens", step.shared_lens)]
     pk = step.pk
 
     def launch(dev, out):
         pk.pa_kv_cache_write(step.cache, dev["k"], dev["v"], dev["slots"], step.status)
-        step.decode(q=dev["q"], out=out, bt=dev["bt"], lens=dev["lens"])
+        step.attend(q=dev["q"], out=out, bt=dev["bt"], lens=dev["lens"], cu_groups=dev.get("cu_groups"),
+                    shared_lens=dev.get("shared_lens"))
 
     return pipelined_e2e(step.device, src, step.out, launch, steps, warmup, world)
 
@@ -912,7 +911,16 @@ def run_decode(args, workload, dev, rank, world, cpu_budget=10.0):
     achieved_logical = step.kv_bytes / (decode_ms / 1e3) / 1e9
     graph_ms = timed_graph(step, args.steps, flush) if small else None
     fused_ms = timed_append(step, args.steps, args.warmup, flush)
-    cascade_ms = timed_cascade(step, args.steps, args.warmup, flush) if step.has_groups else None
+    plain = None
+    if step.has_groups:
+        # the same step with the plain decode (each member reads the shared
+        # prompt blocks itself; the re-reads are L2 hits)
+        p_total, p_decode, _ = timed_decode(step, args.steps, args.warmup, world, flush, attend=step.decode)
+        p_total, p_sum = aggregate(p_total, float(step.kv_bytes) * args.steps, world)
+        plain = {"ms_per_step": round(p_total / args.steps, 5), "value": round(p_sum / (p_total / 1e3) / 1e9, 2),
+                 "unit": "GB/s", "kernel_achieved": round(unique_bytes / (p_decode / 1e3) / 1e9, 1),
+                 "kernel_frac": round(unique_bytes / (p_decode / 1e3) / 1e9 / hbm, 4),
+                 "note": "the same step with the attention through pa_decode (no shared-prefix pass); not in value"}
     # a configuration that states its partition: the same step with the
     # library's automatic choice beside it
     auto = None
@@ -964,15 +972,14 @@ def run_decode(args, workload, dev, rank, world, cpu_budget=10.0):
                          "note": "the same step (new token written, then attended) as one pa_decode_append launch; "
                                  "each step timed on its own"},
         "auto_partition": auto,
-        "cascade": None if cascade_ms is None else {
-            "ms_per_step": round(cascade_ms, 5), "value": round(step.kv_bytes / (cascade_ms / 1e3) / 1e9, 2),
-            "unit": "GB/s",
-            "note": "the same step with the attention through pa_decode_cascade: each sampling group's shared "
-                    "prompt blocks attended once for all members (logical bytes counted as in value)"},
+        "plain_decode": plain,
         "graph": None if graph_ms is None else {
             "us_per_step": round(graph_ms * 1e3, 2), "value": round(step.kv_bytes / (graph_ms / 1e3) / 1e9, 2),
             "unit": "GB/s", "note": "the same step captured once as a CUDA graph and replayed (not in value)"},
-        "roofline": {"bound": "hbm", "kernel": "pa_decode (paged_decode_kernel + partition merge)",
+        "attention_call": "pa_decode_cascade" if step.has_groups else "pa_decode",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("pa_decode_cascade (paged_decode_kernel in group mode + partition merge)"
+                                if step.has_groups else "pa_decode (paged_decode_kernel + partition merge)"),
                      "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_kind": "of %s" % peak_kind,
                      "bytes": "distinct K/V rows read (unique_kv_bytes_per_step)",

@@ -1077,9 +1077,16 @@ paged_decode_kernel(const DecodeParams p) {
             }
             const int64_t head_off = static_cast<int64_t>(it.kvh) * C::PAGE;
             const int64_t blk_stride = static_cast<int64_t>(p.num_kv_heads) * C::PAGE;
+            // block ids come 32 at a time, one per lane; the next batch's load
+            // is issued before this batch's stages are filled, so its latency
+            // hides behind them
+            // block ids come 32 at a time, one per lane; the next batch's load
+            // is issued before this batch's stages are filled, so its latency
+            // hides behind them
+            int32_t id_next = it.j0 + lane < it.j1 ? __ldg(row + it.j0 + lane) : -1;
             for (int jb = it.j0; jb < it.j1 && ok; jb += 32) {
-                const int j = jb + lane;
-                const int32_t id = j < it.j1 ? __ldg(row + j) : -1;
+                const int32_t id = id_next;
+                id_next = jb + 32 + lane < it.j1 ? __ldg(row + jb + 32 + lane) : -1;
                 const int cnt = min(32, it.j1 - jb);
                 for (int k0 = 0; k0 < cnt; k0 += C::SPAGES) {
                     int32_t ids[C::SPAGES];
