@@ -511,26 +511,27 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
             // their own sequences (the same parts, written in this launch)
             if (!v.own && it.L == 0) v.nm = 0;
         }
-        for (int e = tid; e < G * D / 2; e += C::NCW * 32) {
-            const int g = (2 * e) / D, d = (2 * e) % D;
+        // Thread tid takes pairs of one head: g = tid / TPH, columns 2j for j =
+        // tid % TPH, + TPH, ...; the head's max over the slots, the slots'
+        // weights and the normaliser are taken once per thread.
+        constexpr int NT = C::NCW * 32;
+        constexpr int TPH = NT / G < 1 ? 1 : NT / G;  // threads per head
+        for (int g = tid / TPH; g < G; g += NT / TPH) {
             const int ghg = g / C::GW, gw = g % C::GW;
             float M = -INFINITY;
 #pragma unroll
             for (int t = 0; t < C::TW; ++t) M = fmaxf(M, merge[((ghg * C::TW + t) * C::GW + gw) * (D + 2) + D]);
-            float o0 = 0.f, o1 = 0.f, lsum = 0.f;
-            if (M != -INFINITY) {
+            float wt[C::TW];
+            float lsum = 0.f;
 #pragma unroll
-                for (int t = 0; t < C::TW; ++t) {
-                    const float* mw = merge + ((ghg * C::TW + t) * C::GW + gw) * (D + 2);
-                    const float a = fast_exp2(mw[D] - M);
-                    lsum = fmaf(a, mw[D + 1], lsum);
-                    o0 = fmaf(a, mw[d], o0);
-                    o1 = fmaf(a, mw[d + 1], o1);
-                }
-                const float inv = p.v_scale / lsum;
-                o0 *= inv;
-                o1 *= inv;
+            for (int t = 0; t < C::TW; ++t) {
+                const float* mw = merge + ((ghg * C::TW + t) * C::GW + gw) * (D + 2);
+                wt[t] = M == -INFINITY ? 0.f : fast_exp2(mw[D] - M);
+                lsum = fmaf(wt[t], mw[D + 1], lsum);
             }
+            const float inv = M == -INFINITY ? 0.f : p.v_scale / lsum;
+#pragma unroll
+            for (int t = 0; t < C::TW; ++t) wt[t] *= inv;
             int h = it.kvh * G + g;
             int64_t bh = static_cast<int64_t>(it.b) * p.num_heads + h;
             if (p.vm > 0) {
@@ -539,15 +540,26 @@ __device__ __forceinline__ void store_item(const DecodeParams& p, const Item& it
                 h = it.kvh * p.g_real + (g - mi * p.g_real);
                 bh = static_cast<int64_t>(v.m0 + mi) * p.num_heads + h;
             }
-            if (direct) {
-                using T = typename dtype_traits<QDT>::storage;
-                T* out = static_cast<T*>(p.out) + bh * D + d;
-                out[0] = dtype_traits<QDT>::from_f(o0);
-                out[1] = dtype_traits<QDT>::from_f(o1);
-            } else {
-                const int64_t r = bh * p.max_parts + part;
-                *reinterpret_cast<float2*>(p.ws_o + r * D + d) = make_float2(o0, o1);
-                if (d == 0) p.ws_lse[r] = M == -INFINITY ? -INFINITY : M + __log2f(lsum);
+            const int64_t r = bh * p.max_parts + part;
+            if (!direct && tid % TPH == 0) p.ws_lse[r] = M == -INFINITY ? -INFINITY : M + __log2f(lsum);
+            for (int j = tid % TPH; j < D / 2; j += TPH) {
+                const int d = 2 * j;
+                float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+                for (int t = 0; t < C::TW; ++t) {
+                    const float2 x = *reinterpret_cast<const float2*>(
+                        merge + ((ghg * C::TW + t) * C::GW + gw) * (D + 2) + d);
+                    o0 = fmaf(wt[t], x.x, o0);
+                    o1 = fmaf(wt[t], x.y, o1);
+                }
+                if (direct) {
+                    using T = typename dtype_traits<QDT>::storage;
+                    T* out = static_cast<T*>(p.out) + bh * D + d;
+                    out[0] = dtype_traits<QDT>::from_f(o0);
+                    out[1] = dtype_traits<QDT>::from_f(o1);
+                } else {
+                    *reinterpret_cast<float2*>(p.ws_o + r * D + d) = make_float2(o0, o1);
+                }
             }
         }
     }
