@@ -8,8 +8,10 @@ One step = one pass of the whole hot path over one batch: the new token's
 K/V of every sequence is written through its slot (slots from
 pa_slot_mapping over the batch's block table), then single-query paged
 attention runs over every sequence (and the partition merge where a sequence
-was split); for the mixed batch, every new token's K/V is written, then one
-varlen call attends all query rows.
+was split); for the mixed batch, every new token's K/V is written, then
+pa_varlen_mixed attends all query rows (its prefill sequences through the
+varlen tensor-core kernel, its trailing one-token sequences through the
+decode kernel; the one-call pa_prefill_varlen form is reported beside).
 
 The default (--workload all) prints ONE JSON line: the headline workload, the
 7B-shaped MHA decode layer (64 sequences, 32 heads, head size 128, block size
@@ -305,7 +307,10 @@ class DecodeStep:
 
 class PrefillStep:
     """Inputs of one mixed varlen step (new tokens' K/V written through their
-    slots, then one varlen prefill call over all sequences), on the device."""
+    slots, then attention over all sequences: through pa_varlen_mixed, which
+    sends the prefill sequences to the varlen kernel and the trailing
+    one-token sequences to the decode kernel, or as one pa_prefill_varlen
+    call over all of them), on the device."""
 
     def __init__(self, case: W.PagedCase, device, name=""):
         import paged_kv_cache_75_gb300 as pk
@@ -342,15 +347,51 @@ class PrefillStep:
             pairs += int(np.minimum(k, k - q + i + 1).clip(min=0).sum())
         self.flops = 4 * case.head_size * case.num_heads * pairs
         self.pairs = pairs
-        self.launches_per_step = 2
+        # the mixed dispatcher: the trailing run of one-token sequences goes
+        # to the decode kernel, the rest to the varlen kernel
+        self.host_cu_q = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+        n_dec = 0
+        while n_dec < self.B and lq[self.B - 1 - n_dec] == 1:
+            n_dec += 1
+        self.n_pre = self.B - n_dec
+        pre_pairs = 0
+        for q, k in zip(lq[:self.n_pre], lk[:self.n_pre]):
+            i = np.arange(q)
+            pre_pairs += int(np.minimum(k, k - q + i + 1).clip(min=0).sum())
+        self.prefill_flops = 4 * case.head_size * case.num_heads * pre_pairs
+        self.max_q_pre = int(lq[:self.n_pre].max()) if self.n_pre else 0
+        self.max_k_pre = int(lk[:self.n_pre].max()) if self.n_pre else 0
+        ws_n = pk.pa_varlen_mixed_workspace_size(self.B, case.num_heads, case.head_size, self.max_k,
+                                                 case.block_size)
+        self.ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
+        dec_P = pk.pa_decode_partition_size(max(n_dec, 1), case.num_heads, case.num_kv_heads, self.max_k)
+        # write, the varlen kernel, the decode kernel (and its merge when a
+        # one-token sequence spans several partitions)
+        self.launches_per_step = 1 + (1 if self.n_pre else 0) + (
+            (2 if self.max_k > dec_P else 1) if n_dec else 0)
 
     def write(self):
         self.pk.pa_kv_cache_write(self.cache, self.k_new, self.v_new, self.slots, self.status)
 
+    def mixed(self, q=None, out=None, cu_q=None, cu_k=None, bt=None):
+        """The step's attention: pa_varlen_mixed."""
+        self.pk.pa_varlen_mixed(self.out if out is None else out, self.q if q is None else q, self.cache,
+                                self.bt if bt is None else bt, self.cu_q if cu_q is None else cu_q,
+                                self.cu_k if cu_k is None else cu_k, self.host_cu_q, self.max_q, self.max_k,
+                                self.case.scale, True, self.ws, self.status)
+
     def main(self, q=None, out=None):
+        """One pa_prefill_varlen call over every sequence."""
         self.pk.pa_prefill_varlen(self.out if out is None else out, self.q if q is None else q, self.cache,
                                   self.bt, self.cu_q, self.cu_k, self.max_q, self.max_k, self.case.scale, True,
                                   self.status)
+
+    def prefill_rows(self):
+        """The varlen kernel alone on the prefill sequences (the launch
+        pa_varlen_mixed makes for them)."""
+        n = self.n_pre
+        self.pk.pa_prefill_varlen(self.out, self.q, self.cache, self.bt[:n], self.cu_q[:n + 1], self.cu_k[:n + 1],
+                                  self.max_q_pre, self.max_k_pre, self.case.scale, True, self.status)
 
 
 def build_workload(name, device, num_seqs=None, pool_blocks=None):
@@ -480,15 +521,15 @@ def timed_graph(step: DecodeStep, steps, flush):
     return sum(a.elapsed_time(b) for a, b in evs) / steps
 
 
-def timed_prefill(step: PrefillStep, steps, warmup, world):
+def timed_prefill(step: PrefillStep, steps, warmup, world, attend, kernel):
     """Returns (total ms over the timed steps, mean varlen-kernel ms, clocks):
-    the timed steps (write + varlen call) carry no event between their
-    launches; the kernel's own duration comes from a second pass with events
-    around each varlen launch."""
+    the timed steps (write + `attend`) carry no event between their launches;
+    the varlen kernel's own duration comes from a second pass with events
+    around each `kernel` call."""
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
         step.write()
-        step.main()
+        attend()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -497,11 +538,11 @@ def timed_prefill(step: PrefillStep, steps, warmup, world):
         start.record(stream)
         for i in range(steps):
             step.write()
-            step.main()
+            attend()
         end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        kernel_ms = kernel_pass(stream, steps, step.write, step.main)
+        kernel_ms = kernel_pass(stream, steps, step.write, kernel)
     st = int(step.status.item())
     if st != 0:
         raise RuntimeError("device status %d during the benchmark" % st)
@@ -596,54 +637,27 @@ def timed_prefill_e2e(step: PrefillStep, steps, warmup, world):
 
     def launch(dev, out):
         pk.pa_kv_cache_write(step.cache, dev["k"], dev["v"], dev["slots"], step.status)
-        pk.pa_prefill_varlen(out, dev["q"], step.cache, dev["bt"], dev["cu_q"], dev["cu_k"], step.max_q,
-                             step.max_k, step.case.scale, True, step.status)
+        step.mixed(q=dev["q"], out=out, cu_q=dev["cu_q"], cu_k=dev["cu_k"], bt=dev["bt"])
 
     return pipelined_e2e(step.device, src, step.out, launch, steps, warmup, world)
 
 
-def timed_split(step: PrefillStep, steps, warmup):
-    """The mixed batch through pa_varlen_mixed: the varlen kernel takes the
-    prefill sequences, the decode kernel the trailing one-token sequences.
-    Returns mean ms per step (write + attention)."""
-    import paged_kv_cache_75_gb300 as pk
-    B = len(step.lq)
-    host_cu_q = np.concatenate([[0], np.cumsum(step.lq)]).astype(np.int32)
-    ws_n = pk.pa_varlen_mixed_workspace_size(B, step.case.num_heads, step.case.head_size, step.max_k,
-                                             step.case.block_size)
-    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=step.device)
-    stream = torch.cuda.current_stream()
-
-    def one():
-        step.write()
-        pk.pa_varlen_mixed(step.out, step.q, step.cache, step.bt, step.cu_q, step.cu_k, host_cu_q, step.max_q,
-                           step.max_k, step.case.scale, True, ws, step.status)
-
-    for _ in range(warmup):
-        one()
-    torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for _ in range(steps):
-        one()
-    end.record(stream)
-    torch.cuda.synchronize()
-    if int(step.status.item()) != 0:
-        raise RuntimeError("device status %d in the dispatched step" % int(step.status.item()))
-    return start.elapsed_time(end) / steps
-
-
 def run_prefill(args, case, wname, dev, rank, world, cpu_budget=10.0):
     step = PrefillStep(case, dev, wname)
-    total_ms, main_ms, clocks = timed_prefill(step, args.steps, args.warmup, world)
+    # the step: new K/V written, then pa_varlen_mixed; the dominant kernel is
+    # the varlen kernel on the prefill sequences
+    total_ms, main_ms, clocks = timed_prefill(step, args.steps, args.warmup, world, step.mixed, step.prefill_rows)
     total_ms, flops_sum = aggregate(total_ms, float(step.flops) * args.steps, world)
     e2e_ms, h2d, d2h = timed_prefill_e2e(step, args.steps, args.warmup, world)
-    split_ms = timed_split(step, args.steps, args.warmup)
     e2e_ms, flops_e2e = aggregate(e2e_ms, float(step.flops) * args.steps, world)
+    # the same step as one pa_prefill_varlen call over all 128 sequences
+    one_ms, one_kernel_ms, _ = timed_prefill(step, args.steps, args.warmup, world, step.main, step.main)
+    one_ms, one_sum = aggregate(one_ms, float(step.flops) * args.steps, world)
     _, tflops_peak, tflops_sustained, peak_kind = measured_peaks()
     # the varlen kernel is timed per launch in steps of well under a
     # millisecond, not inside a seconds-long loop: the burst peak applies
-    achieved = step.flops / (main_ms / 1e3) / 1e12
+    achieved = step.prefill_flops / (main_ms / 1e3) / 1e12
+    one_achieved = step.flops / (one_kernel_ms / 1e3) / 1e12
     line = {
         "metric": "paged-attn varlen prefill TFLOP/s (causal, % of GB300 bf16 tensor peak)",
         "value": round(flops_sum / (total_ms / 1e3) / 1e12, 2),
@@ -661,24 +675,30 @@ def run_prefill(args, case, wname, dev, rank, world, cpu_budget=10.0):
         "config": {"workload": wname, "num_seqs": step.B, "num_heads": case.num_heads,
                    "num_kv_heads": case.num_kv_heads, "head_size": case.head_size, "block_size": case.block_size,
                    "total_q": int(step.lq.sum()), "visible_pairs": step.pairs, "flops_per_step": step.flops,
+                   "prefill_seqs": step.n_pre, "prefill_flops_per_step": step.prefill_flops,
                    "l2": "inputs larger than L2 (%.2f GB of K/V cache)" % (
                        2 * case.k_cache.numel() * case.k_cache.element_size() / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
+        "attention_call": "pa_varlen_mixed",
         "clocks": clocks,
         "e2e": {"value": round(flops_e2e / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms / args.steps, 5), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "pipeline": E2E_NOTE},
         "gpu_launches": step.launches_per_step * args.steps,
-        "split": None if split_ms is None else {
-            "ms_per_step": round(split_ms, 5), "value": round(step.flops / (split_ms / 1e3) / 1e12, 2),
-            "unit": "TFLOP/s",
-            "note": "the same step through pa_varlen_mixed: the varlen kernel on the prefill sequences, "
-                    "the decode kernel on the trailing one-token sequences (same FLOPs counted)"},
-        "roofline": {"bound": "tensor", "kernel": "pa_prefill_varlen", "achieved": round(achieved, 2),
-                     "peak": tflops_peak, "unit": "TFLOP/s", "frac": round(achieved / tflops_peak, 4),
+        "one_varlen_call": {
+            "ms_per_step": round(one_ms / args.steps, 5), "value": round(one_sum / (one_ms / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s", "kernel_achieved": round(one_achieved, 2),
+            "kernel_frac": round(one_achieved / tflops_peak, 4),
+            "note": "the same step with the attention as one pa_prefill_varlen call over all 128 sequences (the "
+                    "one-token rows as 128-row tiles with four live rows); not in value"},
+        "roofline": {"bound": "tensor",
+                     "kernel": "paged_prefill_tc_kernel (pa_varlen_mixed's launch over the 8 prefill sequences)",
+                     "achieved": round(achieved, 2), "peak": tflops_peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / tflops_peak, 4),
+                     "flops": "causal FLOPs of the prefill sequences (prefill_flops_per_step)",
                      "peak_kind": "of %s (bf16 dense, burst)" % peak_kind,
                      "frac_of_sustained": round(achieved / tflops_sustained, 4),
-                     "traffic": ncu_traffic("mixed", kernel_source_hash(PREFILL_SOURCES)),
+                     "traffic": ncu_traffic("mixed_prefill_rows", kernel_source_hash(PREFILL_SOURCES)),
                      "prefill_ms": round(main_ms, 5), "kernel_src": kernel_source_hash(PREFILL_SOURCES)},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
