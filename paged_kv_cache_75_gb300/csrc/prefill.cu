@@ -727,17 +727,44 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             return stop != 0;
         };
         bool stop = false;
+        // this row's query row and head in q / out for item w
+        auto row_of = [&](const Work& w, bool& valid) -> int64_t {
+            const int t_row = r / p.group, g_row = r - t_row * p.group;
+            const int qi = w.i0 + t_row;  // query index of this row in its sequence
+            valid = qi < w.lq;
+            const int qrow = __ldg(p.cu_q + w.b) + qi;
+            const int head = w.kvh * p.group + g_row;
+            return (static_cast<int64_t>(qrow) * p.num_heads + head) * kD;
+        };
+        // ---- Q row -> tensor memory (warpgroup x: elements 64x .. 64x+63), zero past Lq ----
+        auto store_q = [&](int64_t off, bool valid) {
+            uint32_t qw[32];
+            const uint4* src = reinterpret_cast<const uint4*>(p.q + off + 64 * x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 v = valid ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
+                qw[4 * j] = v.x;
+                qw[4 * j + 1] = v.y;
+                qw[4 * j + 2] = v.z;
+                qw[4 * j + 3] = v.w;
+            }
+            const uint32_t qcol = tmem + kColQ + 32 * x + lane_base;
+            tmem_st16(qcol, *reinterpret_cast<const uint32_t(*)[16]>(qw));
+            tmem_st16(qcol + 16, *reinterpret_cast<const uint32_t(*)[16]>(qw + 16));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        };
+        bool q_ready = false;  // this item's Q already in tensor memory (stored after the previous item's last tile)
         for (int rnd = 0, item; !stop && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
             const Work w = work_item(p, prefix, order, item);
             const int shift = w.lk - w.lq;
-            const int t_row = r / p.group, g_row = r - t_row * p.group;
+            const int t_row = r / p.group;
             const int qi = w.i0 + t_row;  // query index of this row in its sequence
-            const bool row_valid = qi < w.lq;
+            bool row_valid;
+            const int64_t row_off = row_of(w, row_valid);
             const int lim = p.causal ? min(w.lk, shift + qi + 1) : w.lk;  // keys [0, lim) visible
-            // this row's (query row, head): its place in q and out
-            const int qrow = __ldg(p.cu_q + w.b) + qi;
-            const int head = w.kvh * p.group + g_row;
-            const int64_t row_off = (static_cast<int64_t>(qrow) * p.num_heads + head) * kD;
             uint16_t* dst = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
             if (w.ntiles == 0) {
                 // no visible key for any row of the item: output 0
@@ -747,26 +774,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 }
                 continue;
             }
-            // ---- Q row -> tensor memory (warpgroup x: elements 64x .. 64x+63), zero past Lq ----
-            {
-                uint32_t qw[32];
-                const uint4* src = reinterpret_cast<const uint4*>(p.q + row_off + 64 * x);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 v = row_valid ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
-                    qw[4 * j] = v.x;
-                    qw[4 * j + 1] = v.y;
-                    qw[4 * j + 2] = v.z;
-                    qw[4 * j + 3] = v.w;
-                }
-                const uint32_t qcol = tmem + kColQ + 32 * x + lane_base;
-                tmem_st16(qcol, *reinterpret_cast<const uint32_t(*)[16]>(qw));
-                tmem_st16(qcol + 16, *reinterpret_cast<const uint32_t(*)[16]>(qw + 16));
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(q_full);
-            }
+            if (!q_ready) store_q(row_off, row_valid);
+            q_ready = false;
             float m = -INFINITY, l = 0.f;  // reference max (same in both warpgroups), own partial sum
             bool ok = true;
             const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
@@ -940,6 +949,23 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             }
             if (stop) break;
             tiles += w.ntiles;
+            // The next item's Q goes to tensor memory now, before this item's
+            // epilogue: every QK of this item is complete (this thread saw its
+            // last S), so the MMA thread can start the next item's first QKs
+            // while the epilogue runs.  Its first PV, which overwrites O, waits
+            // for the weights of its first tile, written after the epilogue.
+            if (ok) {
+                const int item2 = snake_item(rnd + 1, n_items);
+                if (item2 >= 0) {
+                    const Work w2 = work_item(p, prefix, order, item2);
+                    if (w2.ntiles > 0) {
+                        bool valid2;
+                        const int64_t off2 = row_of(w2, valid2);
+                        store_q(off2, valid2);
+                        q_ready = true;
+                    }
+                }
+            }
             // ---- epilogue: the last PV done, row sums combined, O / l ----
             // both warpgroups saw QK(n-1), so PV(n-3) -- the previous phase of
             // the last PV's barrier -- is complete and the wait cannot alias
@@ -955,8 +981,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 tc_fence_after();
                 const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
                 const float inv = L > 0.f ? 1.f / L : 0.f;
-                uint16_t* dst_e = static_cast<uint16_t*>(p.out) + (static_cast<int64_t>(qrow) * p.num_heads + head) * kD +
-                                  64 * x;
+                uint16_t* dst_e = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     float o[32];
