@@ -122,7 +122,10 @@ struct DecodeCfg {
     static constexpr int PL = EPL / 2;                // element pairs per lane
     static constexpr int ROWB = D * KB;               // bytes per token row
     static constexpr int PAGE = BS * ROWB;            // bytes of one (block, KV head) page
-    static constexpr int SPAGES = BS >= 32 ? 1 : 32 / BS;  // pages per ring stage
+    // pages per ring stage: 32 tokens, except 64 for the tensor-core consumer
+    // at block size 32, so that each stage holds a 16-token slice for each of
+    // the four warps and they finish an item together
+    static constexpr int SPAGES = BS >= 64 ? 1 : (BS == 32 ? (MMA ? 2 : 1) : 32 / BS);
     static constexpr int STOK = SPAGES * BS;          // tokens per ring stage
     static constexpr int SUB = STOK / TPI;            // block steps per stage
     static constexpr int STAGE_BYTES = 2 * SPAGES * PAGE;  // K pages, then V pages
