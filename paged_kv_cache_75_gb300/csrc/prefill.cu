@@ -16,8 +16,9 @@
 // one key/value tile serves the whole GQA group.  Items are sorted by their
 // key-tile count and dealt to the persistent blocks in snake order.  Per
 // item, key tiles of 128 keys stream through separate 3-stage K and V rings:
-//   warp 0      loads pages with TMA tensor copies (128B swizzle), through the
-//               block table (or 3-D boxes of packed K/V);
+//   warps 0, 2  load pages with TMA tensor copies (128B swizzle), through the
+//               block table (or 3-D boxes of packed K/V): warp 0 the K ring,
+//               warp 2 the V ring;
 //   warp 1      allocates tensor memory and issues every MMA from one thread:
 //               S[t & 1] = Q K(t)^T with Q in tensor memory, then
 //               O += P V(t) with the weights P written over S[t & 1];
@@ -505,10 +506,18 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     }
     const uint32_t tmem = *tmem_slot;
     const int n_items = prefix[B] * p.num_kv_heads;
-    if (warp == 0) {
-        // ------------------------------- loader -------------------------------
-        // K and V have rings of their own: a K stage is free again once its QK
-        // is done, long before the PV of the same tile has used V.
+    if (warp == 0 || warp == 2) {
+        // ------------------------------- loaders -------------------------------
+        // K (warp 0) and V (warp 2) have rings and loader warps of their own: a
+        // K stage is free again once its QK is done, long before the PV of the
+        // same tile has used V, and each warp issues only half of a tile's
+        // copies (a tile of block-size-16 pages is 16 copies of K and 16 of V,
+        // issued lane by lane).
+        const int kv = warp == 0 ? 0 : 1;
+        const uint32_t full0 = kv == 0 ? k_full : v_full;
+        const uint32_t empty0 = kv == 0 ? k_empty : v_empty;
+        const uint32_t ring = smem_addr(kv == 0 ? sK : sV);
+        const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
         uint32_t fill = 0, stage = 0, phase = 0;
         bool ok = true;
         if constexpr (PACKED) {
@@ -519,22 +528,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 const Work w = work_item(p, prefix, order, item);
                 const int row0 = __ldg(p.cu_k + w.b);
                 for (int t = 0; t < w.ntiles && ok; ++t) {
-#pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint32_t full = (kv == 0 ? k_full : v_full) + 8 * stage;
-                        const uint32_t empty = (kv == 0 ? k_empty : v_empty) + 8 * stage;
-                        if (lane == 0) ok = ok && mbar_wait(empty, phase ^ 1u, p.status, abort_flag);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) break;
-                        if (lane == 0) {
-                            mbar_expect_tx(full, kTileBytes);
-                            const uint32_t dst = smem_addr((kv == 0 ? sK : sV) + stage * kTileBytes);
-                            const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
-                            tma_load_3d(dst, map, 0, w.kvh, row0 + t * kBN, full);
-                            tma_load_3d(dst + kBlkBytes, map, 64, w.kvh, row0 + t * kBN, full);
-                        }
-                        __syncwarp();
+                    const uint32_t full = full0 + 8 * stage;
+                    if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status, abort_flag);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mbar_expect_tx(full, kTileBytes);
+                        const uint32_t dst = ring + stage * kTileBytes;
+                        tma_load_3d(dst, map, 0, w.kvh, row0 + t * kBN, full);
+                        tma_load_3d(dst + kBlkBytes, map, 64, w.kvh, row0 + t * kBN, full);
                     }
+                    __syncwarp();
                     ++fill;
                     if (++stage == kStages) {
                         stage = 0;
@@ -543,7 +547,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 }
             }
         } else {
-        const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
+            const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
             for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
                 const Work w = work_item(p, prefix, order, item);
                 const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
@@ -559,7 +563,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         if (pg < pages && pg * p.block_size < w.lk) {
                             id = __ldg(bt_row + pg);
                             if (id < 0 || id >= p.num_blocks) {
-                                report(p.status, PA_ERR_BAD_BLOCK);
+                                // both loader warps read the id; one reports it
+                                if (kv == 0) report(p.status, PA_ERR_BAD_BLOCK);
                                 id = -2;
                             }
                         }
@@ -571,24 +576,19 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         static_cast<uint32_t>(__popc(__ballot_sync(0xffffffffu, have))) * 2u * p.block_size * kD;
                     const int row = (my_id * p.num_kv_heads + w.kvh) * p.block_size;
                     const uint32_t off = lane * p.block_size * 128;  // page lane's rows in a 64-column block
-    #pragma unroll
-                    for (int kv = 0; kv < 2; ++kv) {
-                        const uint32_t full = (kv == 0 ? k_full : v_full) + 8 * stage;
-                        const uint32_t empty = (kv == 0 ? k_empty : v_empty) + 8 * stage;
-                        if (lane == 0) ok = ok && mbar_wait(empty, phase ^ 1u, p.status, abort_flag);
-                        ok = __shfl_sync(0xffffffffu, ok, 0);
-                        if (!ok) break;
-                        if (lane == 0) {
-                            if (bytes) mbar_expect_tx(full, bytes);
-                            else mbar_arrive(full);
-                        }
-                        __syncwarp();
-                        if (have) {
-                            const uint32_t dst = smem_addr((kv == 0 ? sK : sV) + stage * kTileBytes) + off;
-                            const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
-                            tma_load_2d(dst, map, 0, row, full);
-                            tma_load_2d(dst + kBlkBytes, map, 64, row, full);
-                        }
+                    const uint32_t full = full0 + 8 * stage;
+                    if (lane == 0) ok = mbar_wait(empty0 + 8 * stage, phase ^ 1u, p.status, abort_flag);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        if (bytes) mbar_expect_tx(full, bytes);
+                        else mbar_arrive(full);
+                    }
+                    __syncwarp();
+                    if (have) {
+                        const uint32_t dst = ring + stage * kTileBytes + off;
+                        tma_load_2d(dst, map, 0, row, full);
+                        tma_load_2d(dst + kBlkBytes, map, 64, row, full);
                     }
                     ++fill;
                     if (++stage == kStages) {
@@ -598,14 +598,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 }
             }
         }
-        // after an abort, wait (bounded) for the copies still landing
+        // after an abort, wait (bounded) for this ring's copies still landing
         if (lane == 0 && *abort_flag) {
             const uint64_t t0 = global_timer_ns();
             const uint32_t first = fill > kStages ? fill - kStages : 0u;
             for (uint32_t f = first; f < fill; ++f)
-                for (int kv = 0; kv < 2; ++kv)
-                    while (!mbar_try_wait((kv == 0 ? k_full : v_full) + 8 * (f % kStages), (f / kStages) & 1u))
-                        if (global_timer_ns() - t0 > kWaitLimitNs) break;
+                while (!mbar_try_wait(full0 + 8 * (f % kStages), (f / kStages) & 1u))
+                    if (global_timer_ns() - t0 > kWaitLimitNs) break;
         }
     } else if (warp == 1) {
         // -------------------------------- MMA ---------------------------------
