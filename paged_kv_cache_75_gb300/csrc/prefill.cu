@@ -245,6 +245,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// one 32-byte global store (dst 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(reinterpret_cast<uint64_t>(dst)),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a
+// multiple of 16)
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+                 : "memory");
+}
+
 // 3-D tiled TMA load (packed K/V: {element, KV head, token})
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                                             uint32_t bar) {
@@ -775,6 +789,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             }
             if (!q_ready) store_q(row_off, row_valid);
             q_ready = false;
+            // the next item's queries to L2 now, an item ahead of their load:
+            // one bulk prefetch per token of the G rows (heads) it shares
+            if (x == 0 && r % p.group == 0) {
+                const int item2 = snake_item(rnd + 1, n_items);
+                if (item2 >= 0) {
+                    const Work w2 = work_item(p, prefix, order, item2);
+                    bool valid2;
+                    const int64_t off2 = row_of(w2, valid2);
+                    if (valid2 && w2.ntiles > 0) prefetch_l2(p.q + off2, static_cast<uint32_t>(p.group * kD * 2));
+                }
+            }
             float m = -INFINITY, l = 0.f;  // reference max (same in both warpgroups), own partial sum
             bool ok = true;
             const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
@@ -981,19 +1006,25 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
                 const float inv = L > 0.f ? 1.f / L : 0.f;
                 uint16_t* dst_e = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
+                // 32-byte stores (whole sectors) when out allows them: a row's
+                // 16 columns start at a multiple of 32 bytes from out
+                const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
 #pragma unroll
                 for (int c0 = 0; c0 < 64; c0 += 32) {
                     float o[32];
                     tmem_ld32(tmem_o + c0, o);
                     if (row_valid) {
+                        uint32_t w[16];
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            uint4 q4;
-                            q4.x = pack2<DT>(o[8 * j] * inv, o[8 * j + 1] * inv);
-                            q4.y = pack2<DT>(o[8 * j + 2] * inv, o[8 * j + 3] * inv);
-                            q4.z = pack2<DT>(o[8 * j + 4] * inv, o[8 * j + 5] * inv);
-                            q4.w = pack2<DT>(o[8 * j + 6] * inv, o[8 * j + 7] * inv);
-                            *reinterpret_cast<uint4*>(dst_e + c0 + 8 * j) = q4;
+                        for (int j = 0; j < 16; ++j) w[j] = pack2<DT>(o[2 * j] * inv, o[2 * j + 1] * inv);
+                        if (wide) {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) st_global_v8(dst_e + c0 + 16 * j, w + 8 * j);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                *reinterpret_cast<uint4*>(dst_e + c0 + 8 * j) =
+                                    make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                         }
                     }
                 }

@@ -79,6 +79,31 @@ def test_prefill_ragged(dtype, bs, G, causal):
     assert_close(out, ref, dtype, dtype)
 
 
+@pytest.mark.parametrize("dtype", [W.BF16, W.F16])
+def test_output_16_byte_aligned_only(dtype):
+    """out 16 bytes past a 32-byte boundary (the epilogue's 16-byte store
+    path): the same bits as an aligned out, and nothing around it touched."""
+    lq = [1, 64, 130, 17, 200]
+    lk = [5, 64, 300, 17, 329]
+    q, kc, vc, bt, cu_q, cu_k = make(77, lq, lk, 8, 2, 16, dtype)
+    ref_bits, st = run_gpu(q, kc, vc, bt, cu_q, cu_k, 0.1, True, dtype)
+    assert st == 0
+    n = q.numel()
+    big = torch.full((n + 64,), 0x5A5A, dtype=torch.int16, device=DEV).view(q.dtype)
+    out = big[8:8 + n].view(q.shape)  # 16 bytes past the allocation's start
+    assert out.data_ptr() % 32 == 16
+    st = dev_status()
+    pk.pa_prefill_varlen(out, q.to(DEV), pk.KVCache(kc.to(DEV), vc.to(DEV)), torch.as_tensor(bt).to(DEV),
+                         torch.as_tensor(cu_q).to(DEV), torch.as_tensor(cu_k).to(DEV), max(lq), max(lk), 0.1, True,
+                         st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(W.as_bits(out), ref_bits)
+    rest = torch.cat([big[:8], big[8 + n:]]).view(torch.int16).cpu().numpy()
+    assert np.all(rest == 0x5A5A)
+    assert_close(ref_bits, run_oracle(q, kc, vc, bt, cu_q, cu_k, 0.1, True, dtype), dtype, dtype)
+
+
 def test_single_query_rows_match_decode():
     lens = [33, 1, 700, 64]
     case = W.make_decode_case(3, lens, 8, 2, 128, 16, 60, W.BF16, W.BF16)
