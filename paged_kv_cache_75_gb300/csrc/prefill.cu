@@ -15,13 +15,19 @@
 // rows are the G query heads of the KV head for TQ tokens (row = t*G + g), so
 // one key/value tile serves the whole GQA group.  Items are sorted by their
 // key-tile count and dealt to the persistent blocks in snake order.  Per
-// item, key tiles of 128 keys stream through separate 3-stage K and V rings:
+// item, key tiles of 128 keys stream through a 3-stage K ring and a 2-stage
+// V ring:
 //   warps 0, 2  load pages with TMA tensor copies (128B swizzle), through the
 //               block table (or 3-D boxes of packed K/V): warp 0 the K ring,
 //               warp 2 the V ring;
+//   warp 3      loads each item's 128 query rows into shared memory in the
+//               layout of a K tile (16-byte asynchronous copies, zero past
+//               the sequence) once the previous item's last QK is done;
 //   warp 1      allocates tensor memory and issues every MMA from one thread:
-//               S[t & 1] = Q K(t)^T with Q in tensor memory, then
-//               O += P V(t) with the weights P written over S[t & 1];
+//               S[t & 1] = Q K(t)^T from shared memory, then
+//               O[c] += P V(t) with the weights P written over S[t & 1]; two
+//               O buffers (c alternates per item) let one item's epilogue run
+//               beside the next item's first PV;
 //   warps 4..7, two softmax warpgroups that split the 128 key columns of each
 //   8..11       tile (a thread: 64 columns of one row, its tensor-memory
 //               lane).  They take weights against a shared reference max and
@@ -30,7 +36,8 @@
 //               exchanged through shared memory, O rescaled in tensor memory
 //               and the weights recomputed.  Weights go to tensor memory as
 //               bf16 hi + lo (both truncated, ~16 bits together; two PV
-//               passes) or one fp16.  The epilogue writes O / l.
+//               passes) or one fp16.  An item's epilogue (O / l) is written
+//               once the next item's first weights are out.
 // Causal alignment is bottom-right: query i of a sequence with Lq queries and
 // Lk keys sits at position Lk - Lq + i.  Every wait is bounded.
 #include <cuda.h>
@@ -47,27 +54,30 @@ namespace {
 constexpr int kD = 128;              // head size
 constexpr int kBN = 128;             // keys per tile
 constexpr int kRows = 128;           // MMA M: query rows per item
-constexpr int kStages = 3;           // depth of the K ring and of the V ring
+constexpr int kStages = 3;           // depth of the K ring
+constexpr int kStagesV = 2;          // depth of the V ring
 constexpr int kThreads = 384;        // 12 warps
 constexpr int kSoftWarp0 = 4;        // softmax warpgroups = warps 4..7 and 8..11
 constexpr uint32_t kTmemCols = 512;
 // tensor-memory columns: S[b] (fp32 scores of the key tiles t with t & 1 = b,
-// later overwritten by the 16-bit weights P), O (fp32 accumulator), Q (16-bit,
-// two per column)
+// later overwritten by the 16-bit weights P) and O[c] (fp32 accumulators of
+// the items with key tiles, c = their count & 1: one item's O is written out
+// while the next item's first PV goes to the other)
 constexpr uint32_t kColS = 0;    // S[b] at b * kBN
-constexpr uint32_t kColO = 256;  // 128 columns
-constexpr uint32_t kColQ = 384;  // 64 columns
+constexpr uint32_t kColO = 256;  // O[c] at kColO + c * kD
 
 // shared memory layout (bytes from the 1 KB-aligned base)
 constexpr int kBlkBytes = kBN * 128;           // 16 KB: one 64-column block of a K or V tile
 constexpr int kTileBytes = 2 * kBlkBytes;      // 32 KB: a K or a V tile
 constexpr int kOffK = 0;                       // K ring
 constexpr int kOffV = kOffK + kStages * kTileBytes;  // V ring
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
-constexpr int kNumBars = 4 * kStages + 3 * 2 + 2;
+constexpr int kOffQ = kOffV + kStagesV * kTileBytes; // the item's 128 query rows, laid out like a K tile
+constexpr int kOffBar = kOffQ + kTileBytes;
+constexpr int kNumBars = 2 * kStages + 2 * kStagesV + 3 * 2 + 3;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffXch = kOffMisc + 64;                   // [2 slots][2 warpgroups][128 rows] floats
-constexpr int kSmemBytes = kOffXch + 2 * 2 * kRows * 4;
+constexpr int kOffPend = kOffXch + 2 * 2 * kRows * 4;  // [256] int64 row offsets, then [256] float row sums
+constexpr int kSmemBytes = kOffPend + 256 * 12;
 constexpr int kMaxSeqs = 6144;                           // prefix of query tiles: (B + 1) ints
 
 struct PrefillParams {
@@ -118,6 +128,13 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t tmem_d, uint32_t tmem_a, uin
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
         "r"(tmem_a), "l"(db), "r"(idesc), "r"(acc));
+}
+// A and B from shared memory
+__device__ __forceinline__ void mma_f16_ss(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(da), "l"(db), "r"(idesc), "r"(acc));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -245,17 +262,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes 0 writes zeros and
+// reads nothing
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // one 32-byte global store (dst 32-byte aligned)
 __device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(reinterpret_cast<uint64_t>(dst)),
                  "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
-}
-
-// bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a
-// multiple of 16)
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                  : "memory");
 }
 
@@ -420,26 +439,31 @@ __device__ __forceinline__ Work work_item(const PrefillParams& p, const int32_t*
 template <int DT, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                        const __grid_constant__ CUtensorMap map_q,
                         const PrefillParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 128B-swizzled tiles need 1 KB alignment; the launch adds 1 KB of slack
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sK = smem + kOffK;
     uint8_t* sV = smem + kOffV;
+    uint8_t* sQ = smem + kOffQ;
     const uint32_t bar0 = smem_addr(smem + kOffBar);
-    const uint32_t k_full = bar0;                  // [kStages] TMA bytes of a K tile
-    const uint32_t k_empty = bar0 + 8 * kStages;   // [kStages] MMA commit after QK
-    const uint32_t v_full = bar0 + 16 * kStages;   // [kStages] TMA bytes of a V tile
-    const uint32_t v_empty = bar0 + 24 * kStages;  // [kStages] MMA commit after PV
-    const uint32_t s_full = bar0 + 32 * kStages;   // [2] MMA commit after QK into S[b]
+    const uint32_t k_full = bar0;                       // [kStages] TMA bytes of a K tile
+    const uint32_t k_empty = k_full + 8 * kStages;      // [kStages] MMA commit after QK
+    const uint32_t v_full = k_empty + 8 * kStages;      // [kStagesV] TMA bytes of a V tile
+    const uint32_t v_empty = v_full + 8 * kStagesV;     // [kStagesV] MMA commit after PV
+    const uint32_t s_full = v_empty + 8 * kStagesV;     // [2] MMA commit after QK into S[b]
     const uint32_t p_full = s_full + 16;           // [2] the 8 softmax warps: P[b] written
     const uint32_t o_done = p_full + 16;           // [2] MMA commit after PV number g, on o_done[g & 1]
-    const uint32_t q_full = o_done + 16;           // 8 softmax warps: Q in tensor memory
-    const uint32_t mma_done = q_full + 8;          // MMA commit at the very end
+    const uint32_t q_full = o_done + 16;           // the query loader warp: an item's Q in shared memory
+    const uint32_t q_empty = q_full + 8;           // MMA commit after an item's last QK
+    const uint32_t mma_done = q_empty + 8;         // MMA commit at the very end
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
     volatile int* snap = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);  // [2] abort snapshots
     float* xch = reinterpret_cast<float*>(smem + kOffXch);
+    int64_t* pend_off = reinterpret_cast<int64_t*>(smem + kOffPend);        // pending epilogue: out offset (-1: no row)
+    float* pend_l = reinterpret_cast<float*>(smem + kOffPend + 256 * 8);     // and partial row sum, per thread
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + kSmemBytes);  // B + 1 ints past the fixed layout
     __shared__ int32_t scan_scratch[kThreads / 32];
 
@@ -452,6 +476,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         for (int s = 0; s < kStages; ++s) {
             mbar_init(k_full + 8 * s, 1);
             mbar_init(k_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < kStagesV; ++s) {
             mbar_init(v_full + 8 * s, 1);
             mbar_init(v_empty + 8 * s, 1);
         }
@@ -460,7 +486,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             mbar_init(p_full + 8 * s, 8);
             mbar_init(o_done + 8 * s, 1);
         }
-        mbar_init(q_full, 8);
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         mbar_init(mma_done, 1);
         *abort_flag = 0;
         snap[0] = 0;
@@ -532,6 +559,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         const uint32_t empty0 = kv == 0 ? k_empty : v_empty;
         const uint32_t ring = smem_addr(kv == 0 ? sK : sV);
         const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
+        const uint32_t nst = kv == 0 ? kStages : kStagesV;  // ring depth
         uint32_t fill = 0, stage = 0, phase = 0;
         bool ok = true;
         if constexpr (PACKED) {
@@ -554,7 +582,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                     }
                     __syncwarp();
                     ++fill;
-                    if (++stage == kStages) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -605,7 +633,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         tma_load_2d(dst + kBlkBytes, map, 64, row, full);
                     }
                     ++fill;
-                    if (++stage == kStages) {
+                    if (++stage == nst) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -615,43 +643,92 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         // after an abort, wait (bounded) for this ring's copies still landing
         if (lane == 0 && *abort_flag) {
             const uint64_t t0 = global_timer_ns();
-            const uint32_t first = fill > kStages ? fill - kStages : 0u;
+            const uint32_t first = fill > nst ? fill - nst : 0u;
             for (uint32_t f = first; f < fill; ++f)
-                while (!mbar_try_wait(full0 + 8 * (f % kStages), (f / kStages) & 1u))
+                while (!mbar_try_wait(full0 + 8 * (f % nst), (f / nst) & 1u))
                     if (global_timer_ns() - t0 > kWaitLimitNs) break;
+        }
+    } else if (warp == 3) {
+        // ----------------------------- query loader -----------------------------
+        // an item's 128 query rows (row = token * G + head) as a K-major,
+        // 128B-swizzled operand, the layout of a K tile, once the previous
+        // item's last QK has released the buffer: two TMA boxes when the
+        // item's tokens end inside the batch (rows past the sequence then
+        // hold the next sequence's queries: every key is masked for them and
+        // they are never written out), else 16-byte copies zero-filled past
+        // the sequence, handed to the async proxy
+        const int64_t total_q = __ldg(p.cu_q + p.num_seqs);
+        uint32_t qn = 0;
+        bool ok = true;
+        for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
+            const Work w = work_item(p, prefix, order, item);
+            if (w.ntiles == 0) continue;
+            if (lane == 0) ok = mbar_wait(q_empty, (qn & 1u) ^ 1u, p.status, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const int64_t tok0 = static_cast<int64_t>(__ldg(p.cu_q + w.b)) + w.i0;
+            const uint32_t dst0 = smem_addr(sQ);
+            if (tok0 + p.tq <= total_q) {
+                if (lane == 0) {
+                    mbar_expect_tx(q_full, kTileBytes);
+                    tma_load_3d(dst0, &map_q, 0, w.kvh * p.group, static_cast<int>(tok0), q_full);
+                    tma_load_3d(dst0 + kBlkBytes, &map_q, 64, w.kvh * p.group, static_cast<int>(tok0), q_full);
+                }
+                __syncwarp();
+                ++qn;
+                continue;
+            }
+            // (the buffer's previous contents may have come through the async proxy)
+            fence_async_smem();
+            for (int i = lane; i < kRows * 16; i += 32) {
+                const int r = i >> 4, c = i & 15;  // row, 16-byte chunk of the row
+                const int t_row = r / p.group, g_row = r - t_row * p.group;
+                const bool valid = w.i0 + t_row < w.lq;
+                const uint16_t* src =
+                    valid ? p.q + ((tok0 + t_row) * p.num_heads + w.kvh * p.group + g_row) * kD + c * 8 : p.q;
+                cp_async16(dst0 + (c >> 3) * kBlkBytes + sw128(r, c & 7), src, valid ? 16u : 0u);
+            }
+            cp_async_wait_all();
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+            ++qn;
         }
     } else if (warp == 1) {
         // -------------------------------- MMA ---------------------------------
         // per item: S[0] = Q K(0)^T, S[1] = Q K(1)^T, then for each tile t:
-        // O (+)= P[t&1] V(t) once both softmax warpgroups have written P over S, followed
+        // O[c] (+)= P[t&1] V(t) once both softmax warpgroups have written P over S, followed
         // by S[t&1] = Q K(t+2)^T.  One thread issues everything, so the tensor
         // pipe sees each PV before the QK that overwrites its P, and a commit
-        // after QK(t+2) also covers PV(t).
+        // after QK(t+2) also covers PV(t).  The commit after an item's last QK
+        // releases the query buffer to the query loader.
         const uint32_t id_qk = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kBN, 0);
         const uint32_t id_pv = mma_idesc(DT == PA_BF16 ? 1 : 0, kRows, kD, 1);
         // descriptors are built once; a k-step only adds a constant to the
         // start-address field (bits 0..13, in 16-byte units)
         const uint64_t dk = smem_desc(smem_addr(sK), 16, 1024);
         const uint64_t dv = smem_desc(smem_addr(sV), kBlkBytes, 1024);
+        const uint64_t dq = smem_desc(smem_addr(sQ), 16, 1024);
         uint32_t k_stage = 0, k_phase = 0;  // K ring position of the next QK
         uint32_t v_stage = 0, v_phase = 0;  // V ring position of the next PV
         uint32_t p_use[2] = {0, 0};         // P[b] handed over so far
         uint32_t pv_count = 0;              // PVs issued so far (all items)
         uint32_t q_cnt = 0;                 // items with tiles
         bool ok = true;
-        auto issue_qk = [&](int t) -> bool {
+        auto issue_qk = [&](int t, bool last) -> bool {
             if (!mbar_wait(k_full + 8 * k_stage, k_phase, p.status, abort_flag)) return false;
             tc_fence_after();
             if (lane == 0) {
                 const uint64_t dks = dk + k_stage * (kTileBytes >> 4);
 #pragma unroll
                 for (int k = 0; k < kD / 16; ++k) {
-                    // Q: 8 columns per 16-element k-step; K: 32 bytes per k-step in a 64-column block
-                    mma_f16_ts(tmem + kColS + (t & 1) * kBN, tmem + kColQ + k * 8,
-                               dks + ((k / 4) * (kBlkBytes >> 4) + (k % 4) * 2), id_qk, k > 0 ? 1u : 0u);
+                    // Q and K: 32 bytes per k-step in a 64-column block
+                    const uint32_t step = (k / 4) * (kBlkBytes >> 4) + (k % 4) * 2;
+                    mma_f16_ss(tmem + kColS + (t & 1) * kBN, dq + step, dks + step, id_qk, k > 0 ? 1u : 0u);
                 }
                 mma_commit(s_full + 8 * (t & 1));
                 mma_commit(k_empty + 8 * k_stage);
+                if (last) mma_commit(q_empty);
             }
             __syncwarp();
             if (++k_stage == kStages) {
@@ -664,9 +741,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const Work w = work_item(p, prefix, order, item);
             if (w.ntiles == 0) continue;
             ok = mbar_wait(q_full, q_cnt & 1u, p.status, abort_flag);
+            const uint32_t col_o = tmem + kColO + (q_cnt & 1u) * kD;  // this item's O
             ++q_cnt;
-            if (ok) ok = issue_qk(0);
-            if (ok && w.ntiles > 1) ok = issue_qk(1);
+            if (ok) ok = issue_qk(0, w.ntiles == 1);
+            if (ok && w.ntiles > 1) ok = issue_qk(1, w.ntiles == 2);
             for (int t = 0; t < w.ntiles && ok; ++t) {
                 const int y = t & 1;
                 ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag) &&
@@ -683,7 +761,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                         for (int j = 0; j < kBN / 16; ++j) {
                             // keys 16j..16j+15: P at 8 columns of half j/4 (hi at +0, lo at +32);
                             // V: 2048 bytes per 16 keys
-                            mma_f16_ts(tmem + kColO, tmem + kColS + y * kBN + (j / 4) * 64 + part * 32 + (j % 4) * 8,
+                            mma_f16_ts(col_o, tmem + kColS + y * kBN + (j / 4) * 64 + part * 32 + (j % 4) * 8,
                                        dvs + j * (2048 >> 4), id_pv, (t > 0 || part > 0 || j > 0) ? 1u : 0u);
                         }
                     }
@@ -692,11 +770,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 }
                 __syncwarp();
                 ++pv_count;
-                if (++v_stage == kStages) {
+                if (++v_stage == kStagesV) {
                     v_stage = 0;
                     v_phase ^= 1u;
                 }
-                if (t + 2 < w.ntiles) ok = issue_qk(t + 2);
+                if (t + 2 < w.ntiles) ok = issue_qk(t + 2, t + 3 == w.ntiles);
             }
         }
         // every MMA this warp issued is complete before tensor memory is freed
@@ -722,13 +800,18 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         // range, so no precision is lost.  Every thread of both warpgroups
         // passes the same barriers whatever its waits returned, and stops only
         // on an abort snapshot taken right after the previous barrier.
+        // An item's epilogue (O / l out of its O buffer) is deferred to the top
+        // of the next item's second key tile (or the end of its first, if it
+        // has one): the tensor cores meanwhile run that item's first PV into
+        // the other O buffer.
         const int x = (warp - kSoftWarp0) >> 2;   // warpgroup
         const int u = tid - kSoftWarp0 * 32;       // 0..255 over both warpgroups
         const int r = u & 127;                     // row of the tile = tensor-memory lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t sbuf = tmem + kColS + 64 * x + lane_base;   // + b * kBN
-        const uint32_t tmem_o = tmem + kColO + 64 * x + lane_base;
+        const uint32_t tmem_o0 = tmem + kColO + 64 * x + lane_base;  // + c * kD: O[c]
         uint32_t s_use[2] = {0, 0};
+        uint32_t n_tiled = 0;  // items with key tiles so far (O[n_tiled & 1] is the current item's)
         uint32_t nbar = 0;     // barriers passed (same count in all 256 threads)
         uint32_t tiles = 0;    // key tiles (= PVs) before the current item
         constexpr float kSafe = 18446744073709551616.f;  // 2^64: partial sums below it need no new max
@@ -749,27 +832,58 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const int head = w.kvh * p.group + g_row;
             return (static_cast<int64_t>(qrow) * p.num_heads + head) * kD;
         };
-        // ---- Q row -> tensor memory (warpgroup x: elements 64x .. 64x+63), zero past Lq ----
-        auto store_q = [&](int64_t off, bool valid) {
-            uint32_t qw[32];
-            const uint4* src = reinterpret_cast<const uint4*>(p.q + off + 64 * x);
+        // the pending epilogue: the previous item with key tiles, not yet
+        // written out; its per-thread row offset and partial sum wait in
+        // shared memory (pend_off[u], pend_l[u])
+        bool pend = false, pend_ok = false;
+        // all 256 threads: the pending item's O / l out of O buffer o_col (this
+        // thread's columns), its last PV number g; false once an abort
+        // snapshot says stop.  These threads saw an S committed after the
+        // item's last PV (the next item's first QK) or, when no item follows,
+        // after the PV before it (the item's last QK); and the PV two after it
+        // needs weights not written yet: the wait neither aliases nor passes early.
+        auto finish = [&](uint32_t o_col, uint32_t g) -> bool {
+            pend = false;
+            bool okf = pend_ok && mbar_wait(o_done + 8 * (g & 1u), (g >> 1) & 1u, p.status, abort_flag);
+            okf = __all_sync(0xffffffffu, okf);
+            const float my_l = pend_l[u];
+            const int64_t my_off = pend_off[u];
+            xch[((nbar & 1) * 2 + x) * kRows + r] = my_l;
+            named_bar_sync(3, 256);
+            if (snapshot()) return false;
+            if (okf) {
+                tc_fence_after();
+                const float L = my_l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                uint16_t* dst_e = static_cast<uint16_t*>(p.out) + my_off + 64 * x;
+                // 32-byte stores (whole sectors) when out allows them: a row's
+                // 16 columns start at a multiple of 32 bytes from out
+                const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint4 v = valid ? __ldg(src + j) : make_uint4(0u, 0u, 0u, 0u);
-                qw[4 * j] = v.x;
-                qw[4 * j + 1] = v.y;
-                qw[4 * j + 2] = v.z;
-                qw[4 * j + 3] = v.w;
+                for (int c0 = 0; c0 < 64; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(o_col + c0, o);
+                    if (my_off >= 0) {
+                        uint32_t wv[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) wv[j] = pack2<DT>(o[2 * j] * inv, o[2 * j + 1] * inv);
+                        if (wide) {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) st_global_v8(dst_e + c0 + 16 * j, wv + 8 * j);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                *reinterpret_cast<uint4*>(dst_e + c0 + 8 * j) =
+                                    make_uint4(wv[4 * j], wv[4 * j + 1], wv[4 * j + 2], wv[4 * j + 3]);
+                        }
+                    }
+                }
+                // a later item's first PV overwrites this O buffer: its p_full
+                // arrival orders that after these reads
+                tc_fence_before();
             }
-            const uint32_t qcol = tmem + kColQ + 32 * x + lane_base;
-            tmem_st16(qcol, *reinterpret_cast<const uint32_t(*)[16]>(qw));
-            tmem_st16(qcol + 16, *reinterpret_cast<const uint32_t(*)[16]>(qw + 16));
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(q_full);
+            return true;
         };
-        bool q_ready = false;  // this item's Q already in tensor memory (stored after the previous item's last tile)
         for (int rnd = 0, item; !stop && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
             const Work w = work_item(p, prefix, order, item);
             const int shift = w.lk - w.lq;
@@ -787,23 +901,18 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 }
                 continue;
             }
-            if (!q_ready) store_q(row_off, row_valid);
-            q_ready = false;
-            // the next item's queries to L2 now, an item ahead of their load:
-            // one bulk prefetch per token of the G rows (heads) it shares
-            if (x == 0 && r % p.group == 0) {
-                const int item2 = snake_item(rnd + 1, n_items);
-                if (item2 >= 0) {
-                    const Work w2 = work_item(p, prefix, order, item2);
-                    bool valid2;
-                    const int64_t off2 = row_of(w2, valid2);
-                    if (valid2 && w2.ntiles > 0) prefetch_l2(p.q + off2, static_cast<uint32_t>(p.group * kD * 2));
-                }
-            }
+            const uint32_t tmem_o = tmem_o0 + (n_tiled & 1u) * kD;  // this item's O
+            ++n_tiled;
             float m = -INFINITY, l = 0.f;  // reference max (same in both warpgroups), own partial sum
             bool ok = true;
             const uint64_t sc2 = f2pack(p.scale_log2, p.scale_log2);
             for (int t = 0; t < w.ntiles; ++t) {
+                // the previous item's O is the other buffer; its last PV is
+                // the one before this item's first
+                if (t == 1 && pend && !finish(tmem_o0 + (n_tiled & 1u) * kD, tiles - 1)) {
+                    stop = true;
+                    break;
+                }
                 const int b = t & 1;
                 const int key0 = t * kBN + 64 * x;  // first key of this thread's 64 columns
                 const int vis = row_valid ? lim - key0 : 0;  // visible keys of these columns: [0, vis)
@@ -933,10 +1042,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 // V rows (after the tile landed) so zero weights never meet NaN
                 if (t * kBN + kBN > w.lk) {
                     const uint32_t f = tiles + t;
-                    ok = mbar_wait(v_full + 8 * (f % kStages), (f / kStages) & 1u, p.status, abort_flag);
+                    ok = mbar_wait(v_full + 8 * (f % kStagesV), (f / kStagesV) & 1u, p.status, abort_flag);
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) continue;
-                    uint8_t* vt = sV + (f % kStages) * kTileBytes;
+                    uint8_t* vt = sV + (f % kStagesV) * kTileBytes;
                     const int first = max(0, w.lk - t * kBN);
                     for (int ci = u; ci < (kBN - first) * 16; ci += 256) {
                         const int rr = first + (ci >> 4), c = ci & 15;
@@ -972,67 +1081,17 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
                 if (lane == 0) mbar_arrive(p_full + 8 * b);
             }
             if (stop) break;
+            // an item with one key tile reaches no second tile: the previous
+            // item's epilogue comes here, after its only weights are out
+            if (pend && !finish(tmem_o0 + (n_tiled & 1u) * kD, tiles - 1)) break;
             tiles += w.ntiles;
-            // The next item's Q goes to tensor memory now, before this item's
-            // epilogue: every QK of this item is complete (this thread saw its
-            // last S), so the MMA thread can start the next item's first QKs
-            // while the epilogue runs.  Its first PV, which overwrites O, waits
-            // for the weights of its first tile, written after the epilogue.
-            if (ok) {
-                const int item2 = snake_item(rnd + 1, n_items);
-                if (item2 >= 0) {
-                    const Work w2 = work_item(p, prefix, order, item2);
-                    if (w2.ntiles > 0) {
-                        bool valid2;
-                        const int64_t off2 = row_of(w2, valid2);
-                        store_q(off2, valid2);
-                        q_ready = true;
-                    }
-                }
-            }
-            // ---- epilogue: the last PV done, row sums combined, O / l ----
-            // both warpgroups saw QK(n-1), so PV(n-3) -- the previous phase of
-            // the last PV's barrier -- is complete and the wait cannot alias
-            {
-                const uint32_t g = tiles - 1;
-                ok = ok && mbar_wait(o_done + 8 * (g & 1u), (g >> 1) & 1u, p.status, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-            }
-            xch[((nbar & 1) * 2 + x) * kRows + r] = l;
-            named_bar_sync(3, 256);
-            if (snapshot()) break;
-            if (ok) {
-                tc_fence_after();
-                const float L = l + xch[((((nbar - 1) & 1) * 2) + (x ^ 1)) * kRows + r];
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                uint16_t* dst_e = static_cast<uint16_t*>(p.out) + row_off + 64 * x;
-                // 32-byte stores (whole sectors) when out allows them: a row's
-                // 16 columns start at a multiple of 32 bytes from out
-                const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
-#pragma unroll
-                for (int c0 = 0; c0 < 64; c0 += 32) {
-                    float o[32];
-                    tmem_ld32(tmem_o + c0, o);
-                    if (row_valid) {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) w[j] = pack2<DT>(o[2 * j] * inv, o[2 * j + 1] * inv);
-                        if (wide) {
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) st_global_v8(dst_e + c0 + 16 * j, w + 8 * j);
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                *reinterpret_cast<uint4*>(dst_e + c0 + 8 * j) =
-                                    make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                        }
-                    }
-                }
-                // the next item's Q store and first PV overwrite tensor memory
-                // read here; its q_full / p_full arrivals order them after this
-                tc_fence_before();
-            }
+            pend = true;
+            pend_ok = ok;
+            pend_l[u] = l;
+            pend_off[u] = row_valid ? row_off : -1;
         }
+        // the last item: its O buffer is the current one, its last PV the last of all
+        if (pend && !stop) finish(tmem_o0 + ((n_tiled - 1u) & 1u) * kD, tiles - 1);
     }
     // ---- teardown: every role is done; free tensor memory ----
     tc_fence_before();
@@ -1090,10 +1149,31 @@ bool make_packed_map(CUtensorMap* map, const void* base, int64_t total_k, int nu
     return r == CUDA_SUCCESS;
 }
 
+// q as a 3-D tensor {head_size, num_heads, tokens}; a box is 64 elements x G
+// heads x 128/G tokens: one item's rows in the layout of a K tile.  The token
+// extent is num_seqs * max_seqlen_q, a bound on the real count (which only
+// the device knows): boxes are loaded only for items whose tokens end before
+// the real count, so no copy reaches past the real rows.
+bool make_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int num_seqs, int max_q, int dtype) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const int64_t bound = static_cast<int64_t>(num_seqs) * max_q;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_heads),
+                                static_cast<cuuint64_t>(bound < INT32_MAX ? bound : INT32_MAX)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(num_heads) * kD * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(kRows / group)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(map, dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // launch shared by the paged and packed entry points (p filled in, maps built)
 template <bool PACKED>
 pa_status launch_prefill(const PrefillParams& p, pa_dtype dtype, const CUtensorMap& map_k,
-                         const CUtensorMap& map_v, pa_stream_t stream) {
+                         const CUtensorMap& map_v, const CUtensorMap& map_q, pa_stream_t stream) {
     // shared memory past the fixed layout: the tile prefix (B+1 ints), the
     // work order (up to every query tile the bounds allow, within what the
     // device offers) and the sort's [12 warps][64 classes] counts
@@ -1114,7 +1194,7 @@ pa_status launch_prefill(const PrefillParams& p, pa_dtype dtype, const CUtensorM
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * per_sm;
     const int grid = static_cast<int>(max_items < cap ? max_items : cap);
     if (grid <= 0) return PA_OK;
-    return launch_pdl(kern, grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream), map_k, map_v, q) ==
+    return launch_pdl(kern, grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream), map_k, map_v, map_q, q) ==
                    cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
@@ -1180,7 +1260,9 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
     if (!make_cache_map(&map_k, cache->k_cache, rows, q_dtype, bs) ||
         !make_cache_map(&map_v, cache->v_cache, rows, q_dtype, bs))
         return PA_ERR_CUDA;
-    return launch_prefill<false>(p, q_dtype, map_k, map_v, stream);
+    CUtensorMap map_q;
+    if (!make_q_map(&map_q, q, num_heads, group, num_seqs, max_seqlen_q, q_dtype)) return PA_ERR_CUDA;
+    return launch_prefill<false>(p, q_dtype, map_k, map_v, map_q, stream);
 }
 
 extern "C" pa_status pa_prefill_varlen_packed(void* out, const void* q, const void* k, const void* v,
@@ -1232,5 +1314,7 @@ extern "C" pa_status pa_prefill_varlen_packed(void* out, const void* q, const vo
     if (!make_packed_map(&map_k, total_k > 0 ? k : q, rows, num_kv_heads, dtype) ||
         !make_packed_map(&map_v, total_k > 0 ? v : q, rows, num_kv_heads, dtype))
         return PA_ERR_CUDA;
-    return launch_prefill<true>(p, dtype, map_k, map_v, stream);
+    CUtensorMap map_q;
+    if (!make_q_map(&map_q, q, num_heads, group, num_seqs, max_seqlen_q, dtype)) return PA_ERR_CUDA;
+    return launch_prefill<true>(p, dtype, map_k, map_v, map_q, stream);
 }
