@@ -104,6 +104,32 @@ def test_output_16_byte_aligned_only(dtype):
     assert_close(ref_bits, run_oracle(q, kc, vc, bt, cu_q, cu_k, 0.1, True, dtype), dtype, dtype)
 
 
+def test_unsorted_work_order_with_keyless_items():
+    """More query tiles (1800 sequences x 3 at G = 8) than the shared-memory
+    work order holds (about 6089 - B tiles): the items keep sequence order, so items with no visible
+    key (most 7th sequences have none, every 11th fewer keys than queries) sit
+    between items with key tiles, and each item's deferred epilogue must wait
+    across them.  Every row against the oracle."""
+    rng = np.random.default_rng(91)
+    B = 1800
+    lq = [34] * B
+    lk = [34 + int(x) for x in rng.integers(0, 41, size=B)]
+    for b in range(0, B, 7):
+        lk[b] = 0
+    for b in range(3, B, 11):
+        lk[b] = 5
+    q, kc, vc, bt, cu_q, cu_k = make(92, lq, lk, 8, 1, 16)
+    out, st = run_gpu(q, kc, vc, bt, cu_q, cu_k, 0.1, True, W.BF16)
+    assert st == 0
+    ref = run_oracle(q, kc, vc, bt, cu_q, cu_k, 0.1, True, W.BF16)
+    assert_close(out, ref, W.BF16, W.BF16)
+    # rows with no visible key are exact zeros
+    keyless = [b for b in range(B) if lk[b] == 0]
+    assert len(keyless) > 200
+    zero_rows = np.concatenate([np.arange(cu_q[b], cu_q[b + 1]) for b in keyless])
+    assert np.all(out[zero_rows] == 0)
+
+
 def test_single_query_rows_match_decode():
     lens = [33, 1, 700, 64]
     case = W.make_decode_case(3, lens, 8, 2, 128, 16, 60, W.BF16, W.BF16)
