@@ -694,6 +694,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             if (lane == 0) mbar_arrive(q_full);
             ++qn;
         }
+        // after an abort, wait (bounded) for a query copy still landing (one
+        // at most: each load waits for the buffer's release)
+        if (lane == 0 && *abort_flag && qn > 0) {
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(q_full, (qn - 1u) & 1u))
+                if (global_timer_ns() - t0 > kWaitLimitNs) break;
+        }
     } else if (warp == 1) {
         // -------------------------------- MMA ---------------------------------
         // per item: S[0] = Q K(0)^T, S[1] = Q K(1)^T, then for each tile t:
