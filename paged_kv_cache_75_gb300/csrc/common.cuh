@@ -71,11 +71,13 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Bounded wait on an mbarrier phase.  Also gives up (returning false) as soon
-// as *abort is set by another warp of the block.
+// as *abort is set by another warp of the block; a phase already complete is
+// taken without reading the flag (its data has landed), so the common case
+// costs one try_wait.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
                                           volatile int* abort) {
-    if (*abort) return false;
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
     uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
