@@ -744,14 +744,26 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             }
             return true;
         };
-        for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
-            const Work w = work_item(p, prefix, order, item);
-            if (w.ntiles == 0) continue;
+        // the next item's bookkeeping is done after an item's first QKs, while
+        // the softmax warps work on its first tile, not between two items
+        int item = snake_item(0, n_items);
+        Work w_next{};
+        if (item >= 0) w_next = work_item(p, prefix, order, item);
+        for (int rnd = 0; ok && item >= 0; ++rnd) {
+            const Work w = w_next;
+            const int item2 = snake_item(rnd + 1, n_items);
+            if (w.ntiles == 0) {
+                item = item2;
+                if (item >= 0) w_next = work_item(p, prefix, order, item);
+                continue;
+            }
             ok = mbar_wait(q_full, q_cnt & 1u, p.status, abort_flag);
             const uint32_t col_o = tmem + kColO + (q_cnt & 1u) * kD;  // this item's O
             ++q_cnt;
             if (ok) ok = issue_qk(0, w.ntiles == 1);
             if (ok && w.ntiles > 1) ok = issue_qk(1, w.ntiles == 2);
+            item = item2;
+            if (item >= 0) w_next = work_item(p, prefix, order, item);
             for (int t = 0; t < w.ntiles && ok; ++t) {
                 const int y = t & 1;
                 ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag) &&
