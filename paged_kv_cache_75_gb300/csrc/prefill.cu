@@ -77,7 +77,9 @@ constexpr int kNumBars = 2 * kStages + 2 * kStagesV + 3 * 2 + 3;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kOffXch = kOffMisc + 64;                   // [2 slots][2 warpgroups][128 rows] floats
 constexpr int kOffPend = kOffXch + 2 * 2 * kRows * 4;  // [256] int64 row offsets, then [256] float row sums
-constexpr int kSmemBytes = kOffPend + 256 * 12;
+constexpr int kItemCache = 64;                          // a CTA's first items, worked out once
+constexpr int kOffItems = kOffPend + 256 * 12;          // [kItemCache] Work
+constexpr int kSmemBytes = kOffItems + kItemCache * 32;
 constexpr int kMaxSeqs = 6144;                           // prefix of query tiles: (B + 1) ints
 
 struct PrefillParams {
@@ -324,7 +326,9 @@ __device__ __forceinline__ bool seq_lens_ok(const PrefillParams& p, int b, int& 
 
 struct Work {
     int b, i0, kvh, lq, lk, kend, ntiles;
+    int q0;  // cu_q[b]: the sequence's first query row
 };
+static_assert(sizeof(Work) == 32, "the item cache holds 32-byte entries");
 
 // Work order.  An item's cost is its number of key tiles, which under the
 // causal mask grows along a sequence's query tiles and differs widely between
@@ -426,6 +430,7 @@ __device__ __forceinline__ Work work_item(const PrefillParams& p, const int32_t*
     }
     w.b = lo;
     seq_lens_ok(p, lo, w.lq, w.lk);
+    w.q0 = __ldg(p.cu_q + lo);
     w.i0 = (tile_id - prefix[lo]) * p.tq;
     const int shift = w.lk - w.lq;
     w.kend = w.lk;
@@ -547,6 +552,18 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
     }
     const uint32_t tmem = *tmem_slot;
     const int n_items = prefix[B] * p.num_kv_heads;
+    // this CTA's first kItemCache items, worked out once: every role's item
+    // loop reads them from here (item_work) instead of searching the tile
+    // prefix and reading the sequence lengths at each item boundary
+    Work* item_cache = reinterpret_cast<Work*>(smem + kOffItems);
+    if (tid < kItemCache) {
+        const int item = snake_item(tid, n_items);
+        if (item >= 0) item_cache[tid] = work_item(p, prefix, order, item);
+    }
+    __syncthreads();
+    auto item_work = [&](int rnd, int item) -> Work {
+        return rnd < kItemCache ? item_cache[rnd] : work_item(p, prefix, order, item);
+    };
     if (warp == 0 || warp == 2) {
         // ------------------------------- loaders -------------------------------
         // K (warp 0) and V (warp 2) have rings and loader warps of their own: a
@@ -567,7 +584,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             // 64-column half (rows past the tensor read as zero; rows past the
             // sequence are masked / zeroed by the softmax warps)
             for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
-                const Work w = work_item(p, prefix, order, item);
+                const Work w = item_work(rnd, item);
                 const int row0 = __ldg(p.cu_k + w.b);
                 for (int t = 0; t < w.ntiles && ok; ++t) {
                     const uint32_t full = full0 + 8 * stage;
@@ -591,7 +608,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         } else {
             const int ppt = kBN / p.block_size;  // pages per tile (2, 4 or 8)
             for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
-                const Work w = work_item(p, prefix, order, item);
+                const Work w = item_work(rnd, item);
                 const int32_t* bt_row = p.block_table + static_cast<int64_t>(w.b) * p.max_blocks;
                 // page ids come in batches of 32 (one per lane, -1: past Lk, -2:
                 // bad id), so the table's latency is paid once per batch
@@ -661,12 +678,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         uint32_t qn = 0;
         bool ok = true;
         for (int rnd = 0, item; ok && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
-            const Work w = work_item(p, prefix, order, item);
+            const Work w = item_work(rnd, item);
             if (w.ntiles == 0) continue;
             if (lane == 0) ok = mbar_wait(q_empty, (qn & 1u) ^ 1u, p.status, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            const int64_t tok0 = static_cast<int64_t>(__ldg(p.cu_q + w.b)) + w.i0;
+            const int64_t tok0 = static_cast<int64_t>(w.q0) + w.i0;
             const uint32_t dst0 = smem_addr(sQ);
             if (tok0 + p.tq <= total_q) {
                 if (lane == 0) {
@@ -748,13 +765,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         // the softmax warps work on its first tile, not between two items
         int item = snake_item(0, n_items);
         Work w_next{};
-        if (item >= 0) w_next = work_item(p, prefix, order, item);
+        if (item >= 0) w_next = item_work(0, item);
         for (int rnd = 0; ok && item >= 0; ++rnd) {
             const Work w = w_next;
             const int item2 = snake_item(rnd + 1, n_items);
             if (w.ntiles == 0) {
                 item = item2;
-                if (item >= 0) w_next = work_item(p, prefix, order, item);
+                if (item >= 0) w_next = item_work(rnd + 1, item);
                 continue;
             }
             ok = mbar_wait(q_full, q_cnt & 1u, p.status, abort_flag);
@@ -763,7 +780,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             if (ok) ok = issue_qk(0, w.ntiles == 1);
             if (ok && w.ntiles > 1) ok = issue_qk(1, w.ntiles == 2);
             item = item2;
-            if (item >= 0) w_next = work_item(p, prefix, order, item);
+            if (item >= 0) w_next = item_work(rnd + 1, item);
             for (int t = 0; t < w.ntiles && ok; ++t) {
                 const int y = t & 1;
                 ok = mbar_wait(p_full + 8 * y, p_use[y] & 1u, p.status, abort_flag) &&
@@ -847,7 +864,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             const int t_row = r / p.group, g_row = r - t_row * p.group;
             const int qi = w.i0 + t_row;  // query index of this row in its sequence
             valid = qi < w.lq;
-            const int qrow = __ldg(p.cu_q + w.b) + qi;
+            const int qrow = w.q0 + qi;
             const int head = w.kvh * p.group + g_row;
             return (static_cast<int64_t>(qrow) * p.num_heads + head) * kD;
         };
@@ -904,7 +921,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             return true;
         };
         for (int rnd = 0, item; !stop && (item = snake_item(rnd, n_items)) >= 0; ++rnd) {
-            const Work w = work_item(p, prefix, order, item);
+            const Work w = item_work(rnd, item);
             const int shift = w.lk - w.lq;
             const int t_row = r / p.group;
             const int qi = w.i0 + t_row;  // query index of this row in its sequence
