@@ -130,6 +130,22 @@ def test_unsorted_work_order_with_keyless_items():
     assert np.all(out[zero_rows] == 0)
 
 
+def test_more_items_per_block_than_the_item_table():
+    """3000 sequences of one query tile each at 32 query / 4 KV heads: 12000
+    items, about 79 per persistent block, past the 64 each block works out at
+    its start (the rest take the tile search).  Every row against the
+    oracle."""
+    rng = np.random.default_rng(93)
+    B = 3000
+    lq = [16] * B
+    lk = [16 + int(x) for x in rng.integers(0, 17, size=B)]
+    q, kc, vc, bt, cu_q, cu_k = make(94, lq, lk, 32, 4, 16)
+    out, st = run_gpu(q, kc, vc, bt, cu_q, cu_k, 0.1, True, W.BF16)
+    assert st == 0
+    ref = run_oracle(q, kc, vc, bt, cu_q, cu_k, 0.1, True, W.BF16)
+    assert_close(out, ref, W.BF16, W.BF16)
+
+
 def test_single_query_rows_match_decode():
     lens = [33, 1, 700, 64]
     case = W.make_decode_case(3, lens, 8, 2, 128, 16, 60, W.BF16, W.BF16)
