@@ -103,6 +103,7 @@ struct PrefillParams {
     float scale_log2;  // scale * log2(e)
     int64_t total_k;   // packed K/V: rows of K and V (Σ key lengths); -1 for the paged cache
     int32_t order_cap; // query tiles the shared-memory work order holds (set by the launch)
+    int32_t q_rows;    // token extent of the query tensor map: min(num_seqs * max_seqlen_q, INT32_MAX)
 };
 
 // ---------------------------------------------------------------------------
@@ -670,10 +671,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
         // an item's 128 query rows (row = token * G + head) as a K-major,
         // 128B-swizzled operand, the layout of a K tile, once the previous
         // item's last QK has released the buffer: two TMA boxes when the
-        // item's tokens end inside the batch (rows past the sequence then
-        // hold the next sequence's queries: every key is masked for them and
-        // they are never written out), else 16-byte copies zero-filled past
-        // the sequence, handed to the async proxy
+        // item's tokens end inside the batch and inside the map's extent
+        // (rows past the sequence then hold the next sequence's queries:
+        // every key is masked for them and they are never written out), else
+        // 16-byte copies zero-filled past the sequence, handed to the async
+        // proxy (also when a sequence before it broke max_seqlen_q and pushed
+        // its rows past num_seqs * max_seqlen_q)
         const int64_t total_q = __ldg(p.cu_q + p.num_seqs);
         uint32_t qn = 0;
         bool ok = true;
@@ -685,7 +688,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_
             if (!ok) break;
             const int64_t tok0 = static_cast<int64_t>(w.q0) + w.i0;
             const uint32_t dst0 = smem_addr(sQ);
-            if (tok0 + p.tq <= total_q) {
+            if (tok0 + p.tq <= total_q && tok0 + p.tq <= p.q_rows) {
                 if (lane == 0) {
                     mbar_expect_tx(q_full, kTileBytes);
                     tma_load_3d(dst0, &map_q, 0, w.kvh * p.group, static_cast<int>(tok0), q_full);
@@ -1189,13 +1192,16 @@ bool make_packed_map(CUtensorMap* map, const void* base, int64_t total_k, int nu
 // heads x 128/G tokens: one item's rows in the layout of a K tile.  The token
 // extent is num_seqs * max_seqlen_q, a bound on the real count (which only
 // the device knows): boxes are loaded only for items whose tokens end before
-// the real count, so no copy reaches past the real rows.
+// the real count and inside this extent, so no copy reaches past the real rows.
+int32_t q_map_rows(int num_seqs, int max_q) {
+    const int64_t bound = static_cast<int64_t>(num_seqs) * max_q;
+    return static_cast<int32_t>(bound < INT32_MAX ? bound : INT32_MAX);
+}
 bool make_q_map(CUtensorMap* map, const void* q, int num_heads, int group, int num_seqs, int max_q, int dtype) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
-    const int64_t bound = static_cast<int64_t>(num_seqs) * max_q;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_heads),
-                                static_cast<cuuint64_t>(bound < INT32_MAX ? bound : INT32_MAX)};
+                                static_cast<cuuint64_t>(q_map_rows(num_seqs, max_q))};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2, static_cast<cuuint64_t>(num_heads) * kD * 2};
     const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(kRows / group)};
     const cuuint32_t estr[3] = {1, 1, 1};
@@ -1298,6 +1304,7 @@ extern "C" pa_status pa_prefill_varlen(void* out, const void* q, pa_dtype q_dtyp
         return PA_ERR_CUDA;
     CUtensorMap map_q;
     if (!make_q_map(&map_q, q, num_heads, group, num_seqs, max_seqlen_q, q_dtype)) return PA_ERR_CUDA;
+    p.q_rows = q_map_rows(num_seqs, max_seqlen_q);
     return launch_prefill<false>(p, q_dtype, map_k, map_v, map_q, stream);
 }
 
@@ -1352,5 +1359,6 @@ extern "C" pa_status pa_prefill_varlen_packed(void* out, const void* q, const vo
         return PA_ERR_CUDA;
     CUtensorMap map_q;
     if (!make_q_map(&map_q, q, num_heads, group, num_seqs, max_seqlen_q, dtype)) return PA_ERR_CUDA;
+    p.q_rows = q_map_rows(num_seqs, max_seqlen_q);
     return launch_prefill<true>(p, dtype, map_k, map_v, map_q, stream);
 }

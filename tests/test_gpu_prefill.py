@@ -169,6 +169,20 @@ def test_status_on_bad_block_and_length():
     assert st == 1
 
 
+def test_sequences_after_one_past_max_seqlen_q_are_still_computed():
+    """A sequence longer than max_seqlen_q is reported and skipped; the ones
+    after it, whose rows then lie past num_seqs * max_seqlen_q, still match
+    the oracle."""
+    lq = [300, 40, 17, 64]
+    lk = [300, 70, 17, 100]
+    q, kc, vc, bt, cu_q, cu_k = make(95, lq, lk, 8, 2, 16)
+    out, st = run_gpu(q, kc, vc, bt, cu_q, cu_k, 0.1, True, W.BF16, max_q=64, max_k=300)
+    assert st == 1  # PA_ERR_INVALID_ARG for the first sequence
+    ref = run_oracle(q, kc, vc, bt, cu_q, cu_k, 0.1, True, W.BF16)
+    rows = slice(int(cu_q[1]), int(cu_q[4]))
+    assert_close(out[rows], ref[rows], W.BF16, W.BF16)
+
+
 def test_full_mixed_varlen_sampled():
     """The mixed batch (8 prefill + 120 decode sequences) in one call.  The
     oracle checks, for every prefill sequence, its first and last 16 query
