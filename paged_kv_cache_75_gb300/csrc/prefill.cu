@@ -21,8 +21,9 @@
 //               block table (or 3-D boxes of packed K/V): warp 0 the K ring,
 //               warp 2 the V ring;
 //   warp 3      loads each item's 128 query rows into shared memory in the
-//               layout of a K tile (16-byte asynchronous copies, zero past
-//               the sequence) once the previous item's last QK is done;
+//               layout of a K tile once the previous item's last QK is done
+//               (two 3-D TMA boxes; at the batch's end 16-byte asynchronous
+//               copies, zero past the sequence);
 //   warp 1      allocates tensor memory and issues every MMA from one thread:
 //               S[t & 1] = Q K(t)^T from shared memory, then
 //               O[c] += P V(t) with the weights P written over S[t & 1]; two
